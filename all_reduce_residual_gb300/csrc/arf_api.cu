@@ -1,0 +1,512 @@
+// arf_api.cu: the C ABI of include/arf.h: validation, launch planning,
+// dispatch, and the host-buffer entry point.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <new>
+#include <tuple>
+
+#include "arf.h"
+#include "arf_internal.h"
+
+struct arf_workspace {
+    int device = 0;
+    arf_device_caps_t caps = {};
+    bool log = false;
+    std::mutex mu;
+    std::map<std::tuple<int, int, int64_t, int64_t, int>, arf_plan_t> plans;
+    std::atomic<int> last_err{0};
+};
+
+namespace {
+
+using arf::kMaxThreads;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_pattern(int p) { return p == ARF_ALLREDUCE || p == ARF_AR_RESIDUAL_RMSNORM; }
+bool valid_dtype(int d) { return d == ARF_BF16 || d == ARF_FP16; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+arf_status_t cuda_fail(arf_workspace_t ws, cudaError_t e) {
+    if (ws) ws->last_err.store((int)e);
+    return ARF_ERR_CUDA;
+}
+
+// Threads and chunks per thread for a slice of `slice` 16-byte chunks: the
+// fewest chunks per thread that keep the CTA at <= 256 threads (<= 512 for
+// the widest rows), threads rounded up to whole warps.
+void shape_cta(int slice, int* threads, int* vpt) {
+    int v = 1;
+    while (v < 8 && ceil_div(slice, v) > 256) v *= 2;
+    int t = (int)ceil_div(ceil_div(slice, v), 32) * 32;
+    *vpt = v;
+    *threads = t < 32 ? 32 : t;
+}
+
+// The RMS plan for a given cluster size.
+arf_plan_t rms_plan(const arf_device_caps_t& caps, int w_spec, int64_t M, int64_t H, int cs) {
+    arf_plan_t pl = {};
+    const int C = (int)(H / 8);
+    const int slice = (int)ceil_div(C, cs);
+    shape_cta(slice, &pl.threads, &pl.vpt);
+    pl.w_spec = w_spec;
+    pl.cluster = cs;
+    const int per_sm = caps.max_threads_per_sm / pl.threads > 0 ? caps.max_threads_per_sm / pl.threads : 1;
+    if (cs == 1) {
+        pl.path = ARF_PATH_ROW;
+        int64_t g = M < (int64_t)caps.num_sms * per_sm ? M : (int64_t)caps.num_sms * per_sm;
+        pl.grid = (int)(g > 0 ? g : 1);
+    } else {
+        pl.path = ARF_PATH_CLUSTER;
+        int64_t max_clusters = (int64_t)caps.num_sms * per_sm / cs;
+        if (max_clusters < 1) max_clusters = 1;
+        int64_t g = M < max_clusters ? M : max_clusters;
+        pl.grid = (int)((g > 0 ? g : 1) * cs);
+    }
+    return pl;
+}
+
+const char* pattern_name(int p) { return p == ARF_ALLREDUCE ? "kAllReduce" : "kARResidualRMSNorm"; }
+const char* path_name(int p) {
+    return p == ARF_PATH_FLAT ? "flat" : p == ARF_PATH_ROW ? "row" : "cluster";
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// status, workspace
+// ---------------------------------------------------------------------------
+
+extern "C" const char* arf_status_string(arf_status_t s) {
+    switch (s) {
+        case ARF_OK: return "ok";
+        case ARF_ERR_INVALID_ARG: return "invalid argument";
+        case ARF_ERR_UNSUPPORTED: return "unsupported size, alignment or plan";
+        case ARF_ERR_CUDA: return "CUDA error";
+        case ARF_ERR_DEVICE_MISMATCH: return "current device or stream device differs from the workspace device";
+    }
+    return "unknown status";
+}
+
+extern "C" arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out) {
+    if (!ws_out) return ARF_ERR_INVALID_ARG;
+    *ws_out = nullptr;
+    arf_workspace* ws = new (std::nothrow) arf_workspace();
+    if (!ws) return ARF_ERR_CUDA;
+    int count = 0;
+    cudaError_t e = cudaGetDeviceCount(&count);
+    if (e == cudaSuccess && (device < 0 || device >= count)) e = cudaErrorInvalidDevice;
+    if (e == cudaSuccess) e = cudaSetDevice(device);
+    int sms = 0, thr = 0, cl = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&thr, cudaDevAttrMaxThreadsPerMultiProcessor, device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&cl, cudaDevAttrClusterLaunch, device);
+    if (e == cudaSuccess && cl) {
+        e = arf::allow_large_clusters_bf16();
+        if (e == cudaSuccess) e = arf::allow_large_clusters_fp16();
+    }
+    if (e != cudaSuccess) {
+        delete ws;
+        (void)cudaGetLastError();
+        return ARF_ERR_CUDA;
+    }
+    ws->device = device;
+    ws->caps.num_sms = sms;
+    ws->caps.max_threads_per_sm = thr;
+    ws->caps.max_cluster = 1;
+    if (cl) {
+        // The largest cluster the row-split kernel can be launched with,
+        // probed on a representative instance (128 threads).
+        for (int cs = 16; cs >= 2; cs /= 2) {
+            arf_plan_t probe = {};
+            probe.path = ARF_PATH_CLUSTER;
+            probe.threads = 128;
+            probe.vpt = 1;
+            probe.cluster = cs;
+            probe.grid = cs;
+            probe.w_spec = 8;
+            int n = 0;
+            if (arf::rms_max_active_clusters_bf16(probe, &n) == cudaSuccess && n > 0) {
+                ws->caps.max_cluster = cs;
+                break;
+            }
+            (void)cudaGetLastError();
+        }
+    }
+    const char* lg = std::getenv("ARF_LOG");
+    ws->log = lg && lg[0] == '1';
+    if (ws->log)
+        std::fprintf(stderr, "[arf] device %d: %d SMs, %d threads/SM, max cluster %d\n", device, sms, thr,
+                     ws->caps.max_cluster);
+    *ws_out = ws;
+    return ARF_OK;
+}
+
+extern "C" arf_status_t arf_workspace_destroy(arf_workspace_t ws) {
+    delete ws;
+    return ARF_OK;
+}
+
+extern "C" arf_status_t arf_workspace_caps(arf_workspace_t ws, arf_device_caps_t* caps_out) {
+    if (!ws || !caps_out) return ARF_ERR_INVALID_ARG;
+    *caps_out = ws->caps;
+    return ARF_OK;
+}
+
+extern "C" int arf_last_cuda_error(arf_workspace_t ws) { return ws ? ws->last_err.load() : 0; }
+
+// ---------------------------------------------------------------------------
+// capability and planning
+// ---------------------------------------------------------------------------
+
+extern "C" arf_status_t arf_supports(arf_workspace_t, arf_pattern_t pattern, int W, int64_t M, int64_t H,
+                                     arf_dtype_t dtype) {
+    if (!valid_pattern(pattern) || !valid_dtype(dtype)) return ARF_ERR_INVALID_ARG;
+    if (H <= 0 || M < 0) return ARF_ERR_INVALID_ARG;
+    if (W < 1 || W > ARF_MAX_W) return ARF_ERR_UNSUPPORTED;
+    if (H % 8 != 0 || H > ARF_MAX_H) return ARF_ERR_UNSUPPORTED;
+    // [M,H] indices and the chunk count stay far inside int64
+    if (M > ((int64_t)1 << 40) / H) return ARF_ERR_UNSUPPORTED;
+    return ARF_OK;
+}
+
+extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pattern_t pattern, int W,
+                                          int64_t M, int64_t H, arf_dtype_t dtype, arf_plan_t* plan_out) {
+    if (!caps || !plan_out) return ARF_ERR_INVALID_ARG;
+    arf_status_t st = arf_supports(nullptr, pattern, W, M, H, dtype);
+    if (st != ARF_OK) return st;
+    if (caps->num_sms < 1 || caps->max_threads_per_sm < 32 || caps->max_cluster < 1) return ARF_ERR_INVALID_ARG;
+    const int w_spec = arf::w_spec_compiled(W) ? W : 0;
+    arf_plan_t pl = {};
+    if (pattern == ARF_ALLREDUCE) {
+        // ~8 outstanding 16-byte loads per thread per loop trip
+        int u = 1;
+        if (w_spec > 0) u = w_spec <= 2 ? 4 : (w_spec <= 4 ? 2 : 1);
+        while (!arf::flat_unroll_compiled(w_spec, u)) u /= 2;
+        pl.path = ARF_PATH_FLAT;
+        pl.threads = 256;
+        pl.vpt = u;
+        pl.cluster = 1;
+        pl.w_spec = w_spec;
+        const int64_t nchunks = M * H / 8;
+        const int64_t need = ceil_div(nchunks, (int64_t)pl.threads * u);
+        const int64_t cap = (int64_t)caps->num_sms * (caps->max_threads_per_sm / pl.threads);
+        int64_t g = need < cap ? need : cap;
+        pl.grid = (int)(g > 0 ? g : 1);
+    } else {
+        // Rows fewer than SMs: split each row over a cluster so that about
+        // every SM gets a CTA, keeping at least a warp's worth of chunks per CTA.
+        const int C = (int)(H / 8);
+        int cs = 1;
+        if (M > 0 && M < caps->num_sms && caps->max_cluster > 1) {
+            const int64_t want = ceil_div(caps->num_sms, M);
+            while (cs < want && cs < caps->max_cluster && cs < 16) cs *= 2;
+            while (cs > 1 && ceil_div(C, cs) < 32) cs /= 2;
+        }
+        pl = rms_plan(*caps, w_spec, M, H, cs);
+    }
+    *plan_out = pl;
+    return ARF_OK;
+}
+
+extern "C" arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_plan_t* pl, arf_pattern_t pattern,
+                                       int W, int64_t M, int64_t H, arf_dtype_t dtype) {
+    if (!caps || !pl) return ARF_ERR_INVALID_ARG;
+    arf_status_t st = arf_supports(nullptr, pattern, W, M, H, dtype);
+    if (st != ARF_OK) return st;
+    if (pl->w_spec != 0 && pl->w_spec != W) return ARF_ERR_UNSUPPORTED;
+    if (!arf::w_spec_compiled(pl->w_spec)) return ARF_ERR_UNSUPPORTED;
+    if (pl->threads < 32 || pl->threads > kMaxThreads || pl->threads % 32 != 0) return ARF_ERR_UNSUPPORTED;
+    if (pl->cluster < 1 || pl->grid < 1 || pl->grid % pl->cluster != 0) return ARF_ERR_UNSUPPORTED;
+    if (pattern == ARF_ALLREDUCE) {
+        if (pl->path != ARF_PATH_FLAT || pl->cluster != 1) return ARF_ERR_UNSUPPORTED;
+        if (!(pl->vpt == 1 || pl->vpt == 2 || pl->vpt == 4) || !arf::flat_unroll_compiled(pl->w_spec, pl->vpt))
+            return ARF_ERR_UNSUPPORTED;
+    } else {
+        if (pl->path == ARF_PATH_ROW) {
+            if (pl->cluster != 1) return ARF_ERR_UNSUPPORTED;
+        } else if (pl->path == ARF_PATH_CLUSTER) {
+            const int c = pl->cluster;
+            if (!(c == 2 || c == 4 || c == 8 || c == 16) || c > caps->max_cluster) return ARF_ERR_UNSUPPORTED;
+        } else {
+            return ARF_ERR_UNSUPPORTED;
+        }
+        if (!arf::rms_vpt_compiled(pl->vpt)) return ARF_ERR_UNSUPPORTED;
+        const int64_t slice = ceil_div(H / 8, pl->cluster);
+        if ((int64_t)pl->threads * pl->vpt < slice) return ARF_ERR_UNSUPPORTED;
+    }
+    return ARF_OK;
+}
+
+namespace {
+
+cudaError_t max_active_clusters(arf_dtype_t dt, const arf_plan_t& pl, int* n) {
+    return dt == ARF_BF16 ? arf::rms_max_active_clusters_bf16(pl, n) : arf::rms_max_active_clusters_fp16(pl, n);
+}
+
+// The planner's plan, with the cluster size lowered until the cluster kernel
+// instance can actually be made resident on this device.
+arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64_t M, int64_t H,
+                         arf_dtype_t dtype, arf_plan_t* out) {
+    const auto key = std::make_tuple((int)pattern, W, M, H, (int)dtype);
+    {
+        std::lock_guard<std::mutex> lk(ws->mu);
+        auto it = ws->plans.find(key);
+        if (it != ws->plans.end()) {
+            *out = it->second;
+            return ARF_OK;
+        }
+    }
+    arf_plan_t pl;
+    arf_status_t st = arf_plan_for_caps(&ws->caps, pattern, W, M, H, dtype, &pl);
+    if (st != ARF_OK) return st;
+    while (pl.path == ARF_PATH_CLUSTER) {
+        int n = 0;
+        cudaError_t e = max_active_clusters(dtype, pl, &n);
+        if (e == cudaSuccess && n > 0) break;
+        (void)cudaGetLastError();
+        const int cs = pl.cluster / 2;
+        const int w_spec = pl.w_spec;
+        pl = rms_plan(ws->caps, w_spec, M, H, cs);
+    }
+    if (ws->log)
+        std::fprintf(stderr, "[arf] plan %s W=%d M=%lld H=%lld %s: path=%s threads=%d vpt=%d cluster=%d grid=%d w_spec=%d\n",
+                     pattern_name(pattern), W, (long long)M, (long long)H, dtype == ARF_BF16 ? "bf16" : "fp16",
+                     path_name(pl.path), pl.threads, pl.vpt, pl.cluster, pl.grid, pl.w_spec);
+    std::lock_guard<std::mutex> lk(ws->mu);
+    ws->plans[key] = pl;
+    *out = pl;
+    return ARF_OK;
+}
+
+// Everything arf_run checks before it launches (sizes already supported).
+arf_status_t check_call(arf_workspace_t ws, arf_pattern_t pattern, const void* const* partials,
+                        const void* residual, const void* gamma, float eps, const void* out,
+                        const void* residual_out) {
+    if (!partials || !out) return ARF_ERR_INVALID_ARG;
+    const bool rms = pattern == ARF_AR_RESIDUAL_RMSNORM;
+    if (rms) {
+        if (!residual || !gamma || !residual_out) return ARF_ERR_INVALID_ARG;
+        if (!std::isfinite(eps) || eps < 0.0f) return ARF_ERR_INVALID_ARG;
+        if (out == residual_out) return ARF_ERR_INVALID_ARG;
+        if (!aligned16(residual) || !aligned16(gamma) || !aligned16(residual_out)) return ARF_ERR_UNSUPPORTED;
+    }
+    if (!aligned16(out)) return ARF_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(partials) & 7u) != 0) return ARF_ERR_UNSUPPORTED;
+    (void)ws;
+    return ARF_OK;
+}
+
+arf_status_t check_device(arf_workspace_t ws, cudaStream_t stream) {
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(ws, e);
+    if (cur != ws->device) return ARF_ERR_DEVICE_MISMATCH;
+    int sdev = -1;
+    e = cudaStreamGetDevice(stream, &sdev);
+    if (e != cudaSuccess) return cuda_fail(ws, e);
+    if (sdev != ws->device) return ARF_ERR_DEVICE_MISMATCH;
+    return ARF_OK;
+}
+
+arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t pattern, int W,
+                    const void* const* partials, const void* residual, const void* gamma, float eps, void* out,
+                    void* residual_out, int64_t M, int64_t H, arf_dtype_t dtype, cudaStream_t stream) {
+    cudaError_t e;
+    if (pattern == ARF_ALLREDUCE) {
+        arf::FlatParams p = {};
+        p.partials = partials;
+        p.out = static_cast<uint4*>(out);
+        p.nchunks = M * H / 8;
+        p.W = W;
+        e = dtype == ARF_BF16 ? arf::launch_flat_bf16(p, pl, stream) : arf::launch_flat_fp16(p, pl, stream);
+    } else {
+        arf::RmsParams p = {};
+        p.partials = partials;
+        p.residual = static_cast<const uint4*>(residual);
+        p.gamma = static_cast<const uint4*>(gamma);
+        p.out = static_cast<uint4*>(out);
+        p.residual_out = static_cast<uint4*>(residual_out);
+        p.M = M;
+        p.C = (int)(H / 8);
+        p.H = (int)H;
+        p.W = W;
+        p.cs = pl.cluster;
+        p.slice = (int)ceil_div(p.C, pl.cluster);
+        p.eps = eps;
+        e = dtype == ARF_BF16 ? arf::launch_rms_bf16(p, pl, stream) : arf::launch_rms_fp16(p, pl, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(ws, e);
+    return ARF_OK;
+}
+
+arf_status_t run_impl(arf_workspace_t ws, const arf_plan_t* forced, arf_pattern_t pattern, int W,
+                      const void* const* partials, const void* residual, const void* gamma, float eps, void* out,
+                      void* residual_out, int64_t M, int64_t H, arf_dtype_t dtype, void* stream_v) {
+    if (!ws) return ARF_ERR_INVALID_ARG;
+    arf_status_t st = arf_supports(ws, pattern, W, M, H, dtype);
+    if (st != ARF_OK) return st;
+    if (forced) {
+        st = arf_plan_check(&ws->caps, forced, pattern, W, M, H, dtype);
+        if (st != ARF_OK) return st;
+    }
+    if (M == 0) return ARF_OK;
+    st = check_call(ws, pattern, partials, residual, gamma, eps, out, residual_out);
+    if (st != ARF_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    st = check_device(ws, stream);
+    if (st != ARF_OK) return st;
+    arf_plan_t pl;
+    if (forced) {
+        pl = *forced;
+        if (pl.path == ARF_PATH_CLUSTER) {
+            // a cluster shape must fit the device: no launch that cannot start
+            int n = 0;
+            cudaError_t e = max_active_clusters(dtype, pl, &n);
+            if (e != cudaSuccess) return cuda_fail(ws, e);
+            if (n < 1) return ARF_ERR_UNSUPPORTED;
+        }
+    } else {
+        st = device_plan(ws, pattern, W, M, H, dtype, &pl);
+        if (st != ARF_OK) return st;
+    }
+    return launch(ws, pl, pattern, W, partials, residual, gamma, eps, out, residual_out, M, H, dtype, stream);
+}
+
+}  // namespace
+
+extern "C" arf_status_t arf_workspace_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64_t M, int64_t H,
+                                           arf_dtype_t dtype, arf_plan_t* plan_out) {
+    if (!ws || !plan_out) return ARF_ERR_INVALID_ARG;
+    arf_status_t st = arf_supports(ws, pattern, W, M, H, dtype);
+    if (st != ARF_OK) return st;
+    return device_plan(ws, pattern, W, M, H, dtype, plan_out);
+}
+
+// ---------------------------------------------------------------------------
+// the epilogue
+// ---------------------------------------------------------------------------
+
+extern "C" arf_status_t arf_run(arf_workspace_t ws, arf_pattern_t pattern, int W, const void* const* partials_dev,
+                                const void* residual, const void* gamma, float eps, void* out, void* residual_out,
+                                int64_t M, int64_t H, arf_dtype_t dtype, void* stream) {
+    return run_impl(ws, nullptr, pattern, W, partials_dev, residual, gamma, eps, out, residual_out, M, H, dtype,
+                    stream);
+}
+
+extern "C" arf_status_t arf_run_planned(arf_workspace_t ws, const arf_plan_t* plan, arf_pattern_t pattern, int W,
+                                        const void* const* partials_dev, const void* residual, const void* gamma,
+                                        float eps, void* out, void* residual_out, int64_t M, int64_t H,
+                                        arf_dtype_t dtype, void* stream) {
+    if (!plan) return ARF_ERR_INVALID_ARG;
+    return run_impl(ws, plan, pattern, W, partials_dev, residual, gamma, eps, out, residual_out, M, H, dtype,
+                    stream);
+}
+
+// ---------------------------------------------------------------------------
+// host buffers
+// ---------------------------------------------------------------------------
+
+namespace arf {
+
+__global__ void fill_pointer_array(const void** array, const char* first, int64_t stride, int W) {
+    for (int r = threadIdx.x; r < W; r += blockDim.x) array[r] = first + (int64_t)r * stride;
+}
+
+cudaError_t launch_fill_pointer_array(const void** array, const char* first, int64_t stride, int W,
+                                      cudaStream_t s) {
+    fill_pointer_array<<<1, 64, 0, s>>>(array, first, stride, W);
+    return cudaGetLastError();
+}
+
+}  // namespace arf
+
+namespace {
+
+// Staging layout, each region 256-byte aligned:
+//   [pointer array: W x 8 B][P_0] ... [P_{W-1}][residual][gamma][out][residual_out]
+struct Staging {
+    size_t ptrs, p0, plane, residual, gamma, out, residual_out, total;
+};
+
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+Staging staging_layout(arf_pattern_t pattern, int W, int64_t M, int64_t H) {
+    Staging s = {};
+    const size_t plane = up256((size_t)M * (size_t)H * 2);
+    const bool rms = pattern == ARF_AR_RESIDUAL_RMSNORM;
+    s.ptrs = 0;
+    s.p0 = up256((size_t)W * sizeof(void*));
+    s.plane = plane;
+    size_t at = s.p0 + (size_t)W * plane;
+    s.residual = at;
+    if (rms) at += plane;
+    s.gamma = at;
+    if (rms) at += up256((size_t)H * 2);
+    s.out = at;
+    at += plane;
+    s.residual_out = at;
+    if (rms) at += plane;
+    s.total = at;
+    return s;
+}
+
+}  // namespace
+
+extern "C" size_t arf_host_staging_bytes(arf_pattern_t pattern, int W, int64_t M, int64_t H, arf_dtype_t dtype) {
+    if (arf_supports(nullptr, pattern, W, M, H, dtype) != ARF_OK) return 0;
+    return staging_layout(pattern, W, M, H).total;
+}
+
+extern "C" arf_status_t arf_run_host(arf_workspace_t ws, arf_pattern_t pattern, int W,
+                                     const void* const* partials_host, const void* residual_host,
+                                     const void* gamma_host, float eps, void* out_host, void* residual_out_host,
+                                     int64_t M, int64_t H, arf_dtype_t dtype, void* staging_dev,
+                                     size_t staging_bytes, void* stream_v) {
+    if (!ws) return ARF_ERR_INVALID_ARG;
+    arf_status_t st = arf_supports(ws, pattern, W, M, H, dtype);
+    if (st != ARF_OK) return st;
+    if (M == 0) return ARF_OK;
+    const bool rms = pattern == ARF_AR_RESIDUAL_RMSNORM;
+    if (!partials_host || !out_host) return ARF_ERR_INVALID_ARG;
+    for (int r = 0; r < W; ++r)
+        if (!partials_host[r]) return ARF_ERR_INVALID_ARG;
+    if (rms) {
+        if (!residual_host || !gamma_host || !residual_out_host) return ARF_ERR_INVALID_ARG;
+        if (!std::isfinite(eps) || eps < 0.0f) return ARF_ERR_INVALID_ARG;
+        if (out_host == residual_out_host) return ARF_ERR_INVALID_ARG;
+    }
+    const Staging L = staging_layout(pattern, W, M, H);
+    if (!staging_dev || (reinterpret_cast<uintptr_t>(staging_dev) & 255u) != 0 || staging_bytes < L.total)
+        return ARF_ERR_INVALID_ARG;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    st = check_device(ws, stream);
+    if (st != ARF_OK) return st;
+
+    char* base = static_cast<char*>(staging_dev);
+    const size_t bytes = (size_t)M * (size_t)H * 2;
+    cudaError_t e = arf::launch_fill_pointer_array(reinterpret_cast<const void**>(base + L.ptrs), base + L.p0,
+                                                   (int64_t)L.plane, W, stream);
+    for (int r = 0; r < W && e == cudaSuccess; ++r)
+        e = cudaMemcpyAsync(base + L.p0 + (size_t)r * L.plane, partials_host[r], bytes, cudaMemcpyHostToDevice,
+                            stream);
+    if (rms && e == cudaSuccess)
+        e = cudaMemcpyAsync(base + L.residual, residual_host, bytes, cudaMemcpyHostToDevice, stream);
+    if (rms && e == cudaSuccess)
+        e = cudaMemcpyAsync(base + L.gamma, gamma_host, (size_t)H * 2, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(ws, e);
+
+    st = run_impl(ws, nullptr, pattern, W, reinterpret_cast<const void* const*>(base + L.ptrs),
+                  rms ? base + L.residual : nullptr, rms ? base + L.gamma : nullptr, eps, base + L.out,
+                  rms ? base + L.residual_out : nullptr, M, H, dtype, stream);
+    if (st != ARF_OK) return st;
+
+    e = cudaMemcpyAsync(out_host, base + L.out, bytes, cudaMemcpyDeviceToHost, stream);
+    if (rms && e == cudaSuccess)
+        e = cudaMemcpyAsync(residual_out_host, base + L.residual_out, bytes, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return cuda_fail(ws, e);
+    return ARF_OK;
+}

@@ -1,0 +1,68 @@
+// arf_internal.h: declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "arf.h"
+
+namespace arf {
+
+// Every kernel is compiled for at most this many threads per CTA.
+constexpr int kMaxThreads = 512;
+
+// Rank counts with a kernel specialised at compile time (0 = generic).
+constexpr bool w_spec_compiled(int ws) {
+    return ws == 0 || ws == 1 || ws == 2 || ws == 4 || ws == 8 || ws == 16;
+}
+// Flat-kernel unroll factors compiled per rank count (registers: U*W vectors).
+constexpr bool flat_unroll_compiled(int ws, int u) {
+    return (u == 1) || (u == 2 && ws <= 8) || (u == 4 && ws <= 4);
+}
+// Chunks per thread compiled for the RMS kernel.
+constexpr bool rms_vpt_compiled(int vpt) { return vpt == 1 || vpt == 2 || vpt == 4 || vpt == 8; }
+
+struct FlatParams {
+    const void* const* partials;  // device array of W device pointers
+    uint4* out;
+    int64_t nchunks;              // M*H/8
+    int W;
+};
+
+struct RmsParams {
+    const void* const* partials;  // device array of W device pointers
+    const uint4* residual;
+    const uint4* gamma;
+    uint4* out;
+    uint4* residual_out;
+    int64_t M;
+    int C;      // 16-byte chunks per row, H/8
+    int H;
+    int W;
+    int cs;     // CTAs per row (cluster size), 1 = no cluster
+    int slice;  // chunks per CTA: ceil(C / cs)
+    float eps;
+};
+
+// Launchers, one per I/O type (arf_launch_bf16.cu / arf_launch_fp16.cu).
+// They assume a plan that passed arf_plan_check.
+cudaError_t launch_flat_bf16(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s);
+cudaError_t launch_flat_fp16(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s);
+cudaError_t launch_rms_bf16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s);
+cudaError_t launch_rms_fp16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s);
+
+// Allow 16-CTA clusters on every cluster kernel of one I/O type (once per
+// device, at workspace creation).
+cudaError_t allow_large_clusters_bf16();
+cudaError_t allow_large_clusters_fp16();
+
+// How many clusters of plan.cluster CTAs of plan.threads threads the RMS
+// kernel instance of `plan` can keep resident at once (0 = cannot launch).
+cudaError_t rms_max_active_clusters_bf16(const arf_plan_t& plan, int* n);
+cudaError_t rms_max_active_clusters_fp16(const arf_plan_t& plan, int* n);
+
+// Host-buffer helper kernel launcher (arf_api.cu).
+cudaError_t launch_fill_pointer_array(const void** array, const char* first, int64_t stride, int W,
+                                      cudaStream_t s);
+
+}  // namespace arf

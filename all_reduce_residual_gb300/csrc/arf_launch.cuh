@@ -1,0 +1,120 @@
+// arf_launch.cuh: kernel tables and launchers for one I/O type. Included by
+// arf_launch_bf16.cu and arf_launch_fp16.cu, which instantiate it once each.
+#pragma once
+
+#include "arf_kernels.cuh"
+
+namespace arf {
+
+using FlatFn = void (*)(FlatParams);
+using RmsFn = void (*)(RmsParams);
+
+template <typename T, int WS>
+FlatFn flat_by_unroll(int u) {
+    switch (u) {
+        case 1: return ar_flat_kernel<T, WS, 1>;
+        case 2: if constexpr (flat_unroll_compiled(WS, 2)) return ar_flat_kernel<T, WS, 2>; else return nullptr;
+        case 4: if constexpr (flat_unroll_compiled(WS, 4)) return ar_flat_kernel<T, WS, 4>; else return nullptr;
+        default: return nullptr;
+    }
+}
+
+template <typename T>
+FlatFn flat_kernel_for(int ws, int u) {
+    switch (ws) {
+        case 0: return flat_by_unroll<T, 0>(u);
+        case 1: return flat_by_unroll<T, 1>(u);
+        case 2: return flat_by_unroll<T, 2>(u);
+        case 4: return flat_by_unroll<T, 4>(u);
+        case 8: return flat_by_unroll<T, 8>(u);
+        case 16: return flat_by_unroll<T, 16>(u);
+        default: return nullptr;
+    }
+}
+
+template <typename T, int WS>
+RmsFn rms_by_vpt(int vpt) {
+    switch (vpt) {
+        case 1: return rms_kernel<T, WS, 1>;
+        case 2: return rms_kernel<T, WS, 2>;
+        case 4: return rms_kernel<T, WS, 4>;
+        case 8: return rms_kernel<T, WS, 8>;
+        default: return nullptr;
+    }
+}
+
+template <typename T>
+RmsFn rms_kernel_for(int ws, int vpt) {
+    switch (ws) {
+        case 0: return rms_by_vpt<T, 0>(vpt);
+        case 1: return rms_by_vpt<T, 1>(vpt);
+        case 2: return rms_by_vpt<T, 2>(vpt);
+        case 4: return rms_by_vpt<T, 4>(vpt);
+        case 8: return rms_by_vpt<T, 8>(vpt);
+        case 16: return rms_by_vpt<T, 16>(vpt);
+        default: return nullptr;
+    }
+}
+
+template <typename T>
+cudaError_t launch_flat_t(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s) {
+    FlatFn fn = flat_kernel_for<T>(plan.w_spec, plan.vpt);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.grid);
+    cfg.blockDim = dim3((unsigned)plan.threads);
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+template <typename T>
+cudaError_t launch_rms_t(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s) {
+    RmsFn fn = rms_kernel_for<T>(plan.w_spec, plan.vpt);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.grid);
+    cfg.blockDim = dim3((unsigned)plan.threads);
+    cfg.stream = s;
+    if (plan.cluster > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)plan.cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+template <typename T>
+cudaError_t allow_large_clusters_t() {
+    const int ws_list[] = {0, 1, 2, 4, 8, 16};
+    const int vpt_list[] = {1, 2, 4, 8};
+    for (int ws : ws_list)
+        for (int vpt : vpt_list) {
+            cudaError_t e = cudaFuncSetAttribute(rms_kernel_for<T>(ws, vpt),
+                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+    return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t rms_max_active_clusters_t(const arf_plan_t& plan, int* n) {
+    RmsFn fn = rms_kernel_for<T>(plan.w_spec, plan.vpt);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.grid);
+    cfg.blockDim = dim3((unsigned)plan.threads);
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)plan.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(n, fn, &cfg);
+}
+
+}  // namespace arf

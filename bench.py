@@ -1,0 +1,485 @@
+"""Benchmark of the all-reduce fusion epilogue on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl arf|reference]
+                    [--workload NAME] [--no-sweep]
+
+One step = one pass of the whole hot path over one batch: a kAllReduce call
+and a kARResidualRMSNorm call on the workload's partials (default workload:
+Llama-3-8B-like TP2 decode, W=2, M=128, H=4096, bf16). The L2 is flushed
+(a write of twice its size) before every step, outside the timed events.
+Metric: achieved HBM GB/s = algorithmic bytes / device time, where the
+algorithmic bytes read every partial and the residual once, gamma once and
+write each output once. Rank 0 prints one JSON line.
+
+N > 1 (torchrun, one process per GPU): every rank runs its own replica of the
+workload (the path has no exchange step on one GPU); value = bytes of all
+ranks / the slowest rank's time.
+
+--impl reference times the CPU oracle (single-threaded C) on the host cores,
+on a bounded sample of the same workload, for the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/call and achieved HBM GB/s (% of GB300 roofline) vs M, per W and pattern"
+FALLBACK_HBM_GBS = 6800.0
+PATTERNS = ("allreduce", "rmsnorm")
+KERNEL_SOURCE = os.path.join(ROOT, "all_reduce_residual_gb300", "csrc", "arf_kernels.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("arf", "reference"), default="arf")
+    ap.add_argument("--workload", default="llama_tp2")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-config sweep table")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def aggregate(units: float, seconds: float, world: int):
+    """(total units over ranks, slowest rank's seconds). Replicas: each rank
+    contributes its own units; the job takes as long as its slowest rank."""
+    if world == 1:
+        return units, seconds
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(u.item()), float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# measurement helpers
+# ---------------------------------------------------------------------------
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+        e = rec.get(f"{kernel}/{workload}")
+        if e and e.get("kernel_source_sha256") == src:
+            return int(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+                self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+
+def run_arf(args):
+    import torch
+
+    import all_reduce_residual_gb300 as arf
+    from all_reduce_residual_gb300 import build as arf_build
+    from all_reduce_residual_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    arf_build.build()
+    ws = arf.Workspace(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    w = wl.WORKLOADS[args.workload]
+    pats = [p for p in PATTERNS if p in w.patterns]
+    inp = wl.make_inputs(w)
+    P = [p.to(dev) for p in inp.partials]
+    R, G = inp.residual.to(dev), inp.gamma.to(dev)
+    ptrs = arf.pointer_array(P, dev)
+    outs = {p: torch.empty_like(R) for p in pats}
+    ro = torch.empty_like(R)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    bytes_call = {p: w.bytes_per_call(p) for p in pats}
+    step_bytes = sum(bytes_call.values())
+
+    def call(p):
+        arf.run(ws, p, P, R, G, w.eps, out=outs[p], residual_out=ro if p == "rmsnorm" else None, ptrs=ptrs)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        for p in pats:
+            call(p)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(pats) + 1)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for k in range(K):
+            flush.zero_()
+            ev[k][0].record(stream)
+            for i, p in enumerate(pats):
+                call(p)
+                ev[k][i + 1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    per_call = {p: [ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)] for i, p in enumerate(pats)}
+    step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
+    total_s = sum(step_ms) / 1e3
+    units, slowest = aggregate(step_bytes * K, total_s, world)
+    value = units / slowest / 1e9
+
+    peak, peak_src = measured_peak()
+    dom = "rmsnorm" if "rmsnorm" in pats else pats[0]
+    dom_s = statistics.mean(per_call[dom]) / 1e3
+    achieved = bytes_call[dom] / dom_s / 1e9
+    kname = "rms_kernel" if dom == "rmsnorm" else "ar_flat_kernel"
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kname, args.workload),
+                "kernel": kname, "algorithmic_bytes_per_launch": bytes_call[dom], "peak_source": peak_src,
+                "timing": "mean CUDA-event time per launch, L2 flushed before each step"}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(statistics.mean(step_ms), 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,s) partials, residual N(0,1), gamma U(0.5,1.5), rounded to the I/O dtype)",
+        "config": {"workload": f"{w.name}: W={w.W} M={w.M} H={w.H} {w.dtype}, one {' + one '.join(pats)} call per step",
+                   "W": w.W, "M": w.M, "H": w.H, "io_dtype": w.dtype, "accumulate": "f32",
+                   "patterns": list(pats), "bytes_per_step": step_bytes,
+                   "l2": f"flushed before every step by writing {flush.numel() >> 20} MiB",
+                   "parallelism": f"replicas x{world}",
+                   "plans": {p: ws.plan(p, w.W, w.M, w.H, torch.bfloat16 if w.dtype == "bf16"
+                                        else torch.float16).as_dict() for p in pats}},
+        "us_per_call": {p: round(statistics.median(v) * 1e3, 3) for p, v in per_call.items()},
+        "roofline": roofline,
+        "gpu_launches": len(pats) * K,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        result["e2e"] = e2e_leg(ws, w, inp, pats, flush, dev, K, world)
+    if not args.no_sweep:
+        result["sweep"] = sweep(ws, dev, flush, peak)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(w, inp, budget_s=10.0)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    ws.close()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def e2e_leg(ws, w, inp, pats, flush, dev, K, world):
+    """The same step through arf_run_host: host (page-locked) inputs copied
+    in and outputs copied back inside the timed events."""
+    import torch
+
+    import all_reduce_residual_gb300 as arf
+
+    dt = inp.partials[0].dtype
+    P = [p.pin_memory() for p in inp.partials]
+    R, G = inp.residual.pin_memory(), inp.gamma.pin_memory()
+    outs = {p: torch.empty_like(inp.residual).pin_memory() for p in pats}
+    ro = torch.empty_like(inp.residual).pin_memory()
+    runners = {p: arf.HostRunner(ws, p, w.W, w.M, w.H, dt) for p in pats}
+    stream = torch.cuda.current_stream(dev)
+    n = min(K, 500)
+
+    def step():
+        for p in pats:
+            runners[p](P, R, G, w.eps, outs[p], ro)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    barrier(world)
+    for _ in range(n):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b) / 1e3)
+    barrier(world)
+    step_bytes = sum(w.bytes_per_call(p) for p in pats)
+    units, slowest = aggregate(step_bytes * n, sum(times), world)
+    plane = w.M * w.H * 2
+    h2d = sum((w.W * plane) + ((plane + w.H * 2) if p == "rmsnorm" else 0) for p in pats)
+    d2h = sum(plane * (2 if p == "rmsnorm" else 1) for p in pats)
+    return {"value": round(units / slowest / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": round(statistics.mean(times) * 1e3, 4),
+            "api": "arf_run_host (page-locked host buffers; H2D + kernels + D2H inside the events)"}
+
+
+def sweep(ws, dev, flush, peak):
+    """µs/call and GB/s for every workload, pattern and (k3_tp8) M: cold
+    (L2 flushed before each call, median of 50 CUDA-event timings) and warm
+    (a CUDA graph of 20 back-to-back calls, per-call mean over 5 replays)."""
+    import torch
+
+    import all_reduce_residual_gb300 as arf
+    from all_reduce_residual_gb300 import workloads as wl
+
+    rows = []
+    stream = torch.cuda.current_stream(dev)
+    for name, w in wl.WORKLOADS.items():
+        Ms = wl.K3_M_SWEEP if name == "k3_tp8" else (w.M,)
+        for M in Ms:
+            inp = wl.make_inputs(w, device=dev, M=M)
+            ww = w.with_m(M)
+            P, R, G = inp.partials, inp.residual, inp.gamma
+            ptrs = arf.pointer_array(P, dev)
+            out, ro = torch.empty_like(R), torch.empty_like(R)
+            for pat in w.patterns:
+                def call():
+                    arf.run(ws, pat, P, R, G, w.eps, out=out, residual_out=ro if pat == "rmsnorm" else None,
+                            ptrs=ptrs)
+                for _ in range(10):
+                    call()
+                cold = []
+                for _ in range(50):
+                    flush.zero_()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    call()
+                    b.record(stream)
+                    b.synchronize()
+                    cold.append(a.elapsed_time(b) * 1e3)
+                g = torch.cuda.CUDAGraph()
+                s = torch.cuda.Stream(dev)
+                s.wait_stream(stream)
+                with torch.cuda.stream(s):
+                    with torch.cuda.graph(g, stream=s):
+                        for _ in range(20):
+                            call()
+                stream.wait_stream(s)
+                torch.cuda.synchronize()
+                warm = []
+                for _ in range(5):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    g.replay()
+                    b.record(stream)
+                    b.synchronize()
+                    warm.append(a.elapsed_time(b) * 1e3 / 20)
+                us = statistics.median(cold)
+                nbytes = ww.bytes_per_call(pat)
+                plan = ws.plan(pat, w.W, M, w.H, torch.bfloat16 if w.dtype == "bf16" else torch.float16)
+                rows.append({"workload": name, "W": w.W, "M": M, "H": w.H, "dtype": w.dtype, "pattern": pat,
+                             "bytes": nbytes, "us_cold": round(us, 3), "us_warm_graph": round(min(warm), 3),
+                             "gbs_cold": round(nbytes / us / 1e3, 1), "frac_cold": round(nbytes / us / 1e3 / peak, 4),
+                             "plan": [plan.path, plan.threads, plan.vpt, plan.cluster, plan.grid, plan.w_spec]})
+                del g
+            del inp, P, R, G, out, ro, ptrs
+            torch.cuda.empty_cache()
+    return rows
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle legs
+# ---------------------------------------------------------------------------
+
+
+def _oracle_step(oracle, w, codes, rows, pats):
+    P = [c[:rows] for c in codes["P"]]
+    dt = oracle.BF16 if w.dtype == "bf16" else oracle.FP16
+    for p in pats:
+        if p == "allreduce":
+            oracle.run(oracle.ALLREDUCE, P, dtype=dt)
+        else:
+            oracle.run(oracle.AR_RESIDUAL_RMSNORM, P, codes["R"][:rows], codes["G"], w.eps, dtype=dt)
+
+
+def _codes(inp):
+    from all_reduce_residual_gb300 import workloads as wl
+
+    return {"P": [wl.codes(p) for p in inp.partials], "R": wl.codes(inp.residual), "G": wl.codes(inp.gamma)}
+
+
+def _bytes(w, rows, pats):
+    return sum(w.with_m(rows).bytes_per_call(p) for p in pats)
+
+
+def cpu_baseline(w, inp, budget_s=10.0):
+    """The oracle as it stands, single-threaded, repeated on the full workload
+    step until about budget_s of CPU time has run."""
+    import oracle
+
+    pats = [p for p in PATTERNS if p in w.patterns]
+    codes = _codes(inp)
+    oracle.default()
+    done, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(oracle, w, codes, w.M, pats)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    gbs = _bytes(w, w.M, pats) * done / el / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} full steps of {w.name} ({' + '.join(pats)}, M={w.M}) in {el:.1f} s, "
+                      f"single-threaded C oracle"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores, same metric. Under
+    torchrun only rank 0 runs; the others exit at once."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from all_reduce_residual_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[args.workload]
+    pats = [p for p in PATTERNS if p in w.patterns]
+    inp = wl.make_inputs(w)
+    codes = _codes(inp)
+    oracle.default()
+    t0 = time.perf_counter()
+    _oracle_step(oracle, w, codes, w.M, pats)
+    full = time.perf_counter() - t0
+    budget = 90.0  # seconds for the whole timed run
+    rows = max(1, min(w.M, int(w.M * budget / max(1e-9, full * max(1, args.steps)))))
+    for _ in range(args.warmup):
+        _oracle_step(oracle, w, codes, rows, pats)
+    times = []
+    for _ in range(args.steps):
+        a = time.perf_counter()
+        _oracle_step(oracle, w, codes, rows, pats)
+        times.append(time.perf_counter() - a)
+    total = sum(times)
+    value = _bytes(w, rows, pats) * args.steps / total / 1e9
+    sample = f"{rows} of {w.M} rows of {w.name} per step ({' + '.join(pats)}), single-threaded C oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (same seeded inputs as the GPU arm)",
+            "config": {"workload": f"{w.name}: W={w.W} M={w.M} H={w.H} {w.dtype}, one {' + one '.join(pats)} call per step",
+                       "W": w.W, "M": w.M, "H": w.H, "io_dtype": w.dtype, "sample_rows": rows},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_arf(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+/*
+ * arf.h: the all-reduce fusion epilogue on one GPU (C ABI).
+ *
+ * What the library computes. In tensor-parallel decode each of W ranks holds
+ * a partial activation [M,H]; the all-reduce sums them, and a fused epilogue
+ * may follow. tokenspeed PR #1075 "route generic MNNVL AR patterns to
+ * upstream flashinfer" (description, Summary) names the two generic fusion
+ * patterns built here:
+ *   kAllReduce          out          = sum_r P_r
+ *   kARResidualRMSNorm  residual_out = sum_r P_r + residual
+ *                       out          = RMSNorm(residual_out) * gamma
+ * Here all W partials sit in this GPU's own memory and are reached through a
+ * device-resident array of W pointers, the form flashinfer PR #1321
+ * "Optimizations for TRTLLM MNNVL Allreduce" (Description: "Use GPU array to
+ * pass the uc pointers") gives for the per-rank buffers. Nothing crosses GPUs.
+ *
+ * Numeric contract (both dtypes, bf16 and fp16: flashinfer PR #1321,
+ * Highlights, __nv_half support):
+ *   acc = 0.0f; for r = 0..W-1 in array order: acc = acc + f32(P_r[m,i])
+ *       binary32 round-to-nearest adds, no reassociation, no FMA, no FTZ;
+ *   kAllReduce:  out[m,i] = rn(acc)                      (bitwise defined)
+ *   kARResidualRMSNorm:
+ *       residual_out[m,i] = rn(acc + f32(residual[m,i])) (one rounding;
+ *                                                          bitwise defined)
+ *       x_i = f32(residual_out[m,i])                      (the stored value)
+ *       inv = rsqrt(sum_i x_i^2 / H + eps)                (mean over H, eps
+ *                                                          inside the root)
+ *       out[m,i] = rn((x_i * inv) * f32(gamma[i]))        (binary32, within
+ *                                                          1 ulp of the exact
+ *                                                          value rounded once)
+ *   rn() = round to nearest even into the I/O dtype.
+ * The sum of squares is reduced in a fixed tree for a given launch plan, so
+ * repeated calls with the same plan are bitwise identical.
+ *
+ * Layout. Every [M,H] tensor is contiguous row-major (row stride H elements),
+ * gamma is [H]. Element type is bf16 or fp16 (16-bit codes).
+ *
+ * Ownership. The caller owns every tensor and the pointer array; they must
+ * stay valid until the stream work completes. The library keeps no tensor
+ * pointer after a call returns. A workspace owns host state only (device id,
+ * SM count, cluster limits, plan cache) and no device memory.
+ *
+ * Errors. Every entry point returns a status and never throws. On any error
+ * nothing is launched and no output is written.
+ */
+#ifndef ARF_H
+#define ARF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum arf_status {
+    ARF_OK = 0,
+    ARF_ERR_INVALID_ARG = 1,     /* NULL pointer, negative size, bad eps, aliasing */
+    ARF_ERR_UNSUPPORTED = 2,     /* valid but outside what this build handles */
+    ARF_ERR_CUDA = 3,            /* a CUDA call failed; see arf_last_cuda_error */
+    ARF_ERR_DEVICE_MISMATCH = 4  /* current device or stream device != workspace device */
+} arf_status_t;
+
+/* Fusion patterns, named as in tokenspeed PR #1075 (Summary). */
+typedef enum arf_pattern {
+    ARF_ALLREDUCE = 0,           /* kAllReduce */
+    ARF_AR_RESIDUAL_RMSNORM = 1  /* kARResidualRMSNorm */
+} arf_pattern_t;
+
+typedef enum arf_dtype {
+    ARF_BF16 = 0,
+    ARF_FP16 = 1
+} arf_dtype_t;
+
+/* Kernel shapes a plan can select. */
+typedef enum arf_path {
+    ARF_PATH_FLAT = 0,    /* kAllReduce: grid-stride over 16-byte chunks of [M,H] */
+    ARF_PATH_ROW = 1,     /* kARResidualRMSNorm: one CTA owns a whole row */
+    ARF_PATH_CLUSTER = 2  /* kARResidualRMSNorm: a row split over a thread-block
+                             cluster, sum of squares exchanged through DSMEM */
+} arf_path_t;
+
+/* Limits of this build. */
+#define ARF_MAX_W 64      /* ranks: the pages' world sizes {2,...,64}, plus 1 */
+#define ARF_MAX_H 32768   /* hidden size; H must also be a multiple of 8 */
+
+/* What the planner needs to know about a device. */
+typedef struct arf_device_caps {
+    int num_sms;            /* streaming multiprocessors */
+    int max_cluster;        /* largest usable cluster size (1, 2, 4, 8 or 16) */
+    int max_threads_per_sm; /* resident threads per SM */
+} arf_device_caps_t;
+
+/* A launch plan: which kernel shape and launch configuration one call uses. */
+typedef struct arf_plan {
+    int path;     /* arf_path_t */
+    int threads;  /* threads per CTA, a multiple of 32 in [32, 1024] */
+    int vpt;      /* 16-byte chunks per thread per row (row/cluster paths) or
+                     chunks per thread per loop trip (flat path): 1, 2, 4 or 8 */
+    int cluster;  /* CTAs per row (cluster path: 2, 4, 8 or 16; else 1) */
+    int grid;     /* CTAs launched; a multiple of `cluster` */
+    int w_spec;   /* rank count compiled into the kernel, or 0 for the generic
+                     kernel that reads W at run time */
+} arf_plan_t;
+
+typedef struct arf_workspace* arf_workspace_t;
+
+/* ---- workspace -------------------------------------------------------- */
+
+/* Create a workspace for CUDA device `device`: reads the SM count and the
+ * resident-thread limit, and probes the largest cluster size the cluster
+ * kernel can be launched with (the launch configuration is then derived
+ * from these, as flashinfer PR #1507 "update allreduce to match trtllm",
+ * Highlights, derives threads_per_block and cluster_size from the SM count).
+ * Makes `device` current on the calling thread.
+ * Errors: ws_out NULL -> INVALID_ARG; no such device or a CUDA failure -> CUDA. */
+arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out);
+
+/* Destroy a workspace. NULL is accepted and returns ARF_OK. */
+arf_status_t arf_workspace_destroy(arf_workspace_t ws);
+
+/* The device capabilities the workspace plans with. */
+arf_status_t arf_workspace_caps(arf_workspace_t ws, arf_device_caps_t* caps_out);
+
+/* The cudaError_t of the workspace's last ARF_ERR_CUDA (0 if none). */
+int arf_last_cuda_error(arf_workspace_t ws);
+
+/* Static text for a status code (never NULL). */
+const char* arf_status_string(arf_status_t status);
+
+/* ---- capability and planning (host only, no device work) --------------- */
+
+/* Whether (pattern, W, M, H, dtype) is handled, judged on the sizes alone in
+ * the manner of the supports()/dispatch contract of tokenspeed PR #1075
+ * (Summary). ws may be NULL (shape rules only). Returns ARF_OK, or the status
+ * arf_run would return for these sizes: W outside [1, ARF_MAX_W], H % 8 != 0,
+ * H > ARF_MAX_H -> UNSUPPORTED; H <= 0 or M < 0 or a bad enum -> INVALID_ARG. */
+arf_status_t arf_supports(arf_workspace_t ws, arf_pattern_t pattern, int W,
+                          int64_t M, int64_t H, arf_dtype_t dtype);
+
+/* The plan the library picks for these sizes on a device with `caps`.
+ * Pure function of its arguments. */
+arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pattern_t pattern,
+                               int W, int64_t M, int64_t H, arf_dtype_t dtype,
+                               arf_plan_t* plan_out);
+
+/* The plan arf_run would use on this workspace (memoised per shape). */
+arf_status_t arf_workspace_plan(arf_workspace_t ws, arf_pattern_t pattern, int W,
+                                int64_t M, int64_t H, arf_dtype_t dtype,
+                                arf_plan_t* plan_out);
+
+/* Whether `plan` is a legal plan for these sizes on `caps` (ARF_OK) or not
+ * (UNSUPPORTED), the check arf_run_planned applies. */
+arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_plan_t* plan,
+                            arf_pattern_t pattern, int W, int64_t M, int64_t H,
+                            arf_dtype_t dtype);
+
+/* ---- the epilogue ------------------------------------------------------ */
+
+/* Run one pattern, asynchronously on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream). No allocation, no host synchronisation and no host
+ * read of device data, so the call can be captured into a CUDA graph; a
+ * captured graph bakes in the pointer values, so keep them stable.
+ *
+ *   partials_dev  DEVICE array of W device pointers, each to an [M,H] tensor;
+ *                 ranks are summed in this array's order. Every pointer must
+ *                 be 16-byte aligned (a precondition: it is not readable from
+ *                 the host without a synchronisation).
+ *   residual      [M,H] device, read      (kARResidualRMSNorm; else ignored)
+ *   gamma         [H]   device, read      (kARResidualRMSNorm; else ignored)
+ *   eps           finite, >= 0            (kARResidualRMSNorm; else ignored)
+ *   out           [M,H] device, written
+ *   residual_out  [M,H] device, written   (kARResidualRMSNorm; else ignored)
+ *
+ * Inputs are never modified. residual_out == residual is allowed (in place):
+ * each element is read before the same thread overwrites it. out ==
+ * residual_out is rejected (INVALID_ARG); other overlaps are undefined.
+ * M == 0 returns ARF_OK and launches nothing.
+ * Errors: see arf_supports; NULL required pointer, non-finite or negative eps
+ * -> INVALID_ARG; residual, gamma, out or residual_out not 16-byte aligned ->
+ * UNSUPPORTED; current device or stream device != workspace device ->
+ * DEVICE_MISMATCH; launch failure -> CUDA (code in arf_last_cuda_error). */
+arf_status_t arf_run(arf_workspace_t ws, arf_pattern_t pattern, int W,
+                     const void* const* partials_dev,
+                     const void* residual, const void* gamma, float eps,
+                     void* out, void* residual_out,
+                     int64_t M, int64_t H, arf_dtype_t dtype, void* stream);
+
+/* arf_run with an explicit launch plan instead of the planner's (tuning
+ * sweeps and tests of every kernel shape). The plan must pass
+ * arf_plan_check for the workspace's caps, and a cluster plan must be one the
+ * device can keep resident, else UNSUPPORTED. Same semantics
+ * and results contract as arf_run; out may differ from arf_run's by the
+ * reduction tree of the sum of squares (within the 1 ulp bound). */
+arf_status_t arf_run_planned(arf_workspace_t ws, const arf_plan_t* plan,
+                             arf_pattern_t pattern, int W,
+                             const void* const* partials_dev,
+                             const void* residual, const void* gamma, float eps,
+                             void* out, void* residual_out,
+                             int64_t M, int64_t H, arf_dtype_t dtype, void* stream);
+
+/* ---- host buffers ------------------------------------------------------ */
+
+/* Bytes of device staging that arf_run_host needs for these sizes. */
+size_t arf_host_staging_bytes(arf_pattern_t pattern, int W, int64_t M, int64_t H,
+                              arf_dtype_t dtype);
+
+/* The epilogue on HOST buffers: copies the inputs to `staging_dev`, runs
+ * the pattern there and copies the outputs back, all enqueued on `stream`
+ * (returns before they finish; synchronise the stream before reading the
+ * outputs). Copies overlap other work only from page-locked host memory.
+ *
+ *   partials_host  HOST array of W host pointers, each to an [M,H] tensor
+ *   residual_host, gamma_host, out_host, residual_out_host: host buffers with
+ *                  the roles and layouts of arf_run's arguments
+ *   staging_dev    device buffer of at least arf_host_staging_bytes(...)
+ *                  bytes, 256-byte aligned, owned by the caller, not used by
+ *                  anything else until the stream work completes
+ * Errors: as arf_run; staging_dev NULL, misaligned or too small -> INVALID_ARG. */
+arf_status_t arf_run_host(arf_workspace_t ws, arf_pattern_t pattern, int W,
+                          const void* const* partials_host,
+                          const void* residual_host, const void* gamma_host, float eps,
+                          void* out_host, void* residual_out_host,
+                          int64_t M, int64_t H, arf_dtype_t dtype,
+                          void* staging_dev, size_t staging_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ARF_H */

@@ -1,0 +1,165 @@
+"""The C-ABI library on the host (no GPU): it loads, exports every entry
+point include/arf.h declares, and its host logic (shape rules, planner, plan
+checker, staging layout, argument checks) behaves as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import all_reduce_residual_gb300 as arf
+from all_reduce_residual_gb300 import _binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "arf.h")
+
+GB300 = arf.DeviceCaps(num_sms=152, max_cluster=16, max_threads_per_sm=2048)
+K3_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048)
+SHAPES = [(2, 8, 1024), (2, 128, 4096), *[(8, m, 7168) for m in K3_M], (4, 5851, 7168), (16, 585, 7168),
+          (1, 1, 8), (3, 7, 8), (64, 3, 32768), (5, 1000, 1000), (17, 200, 2048)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build.build()
+    arf.load()
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(arf_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ("arf_workspace_create", "arf_workspace_destroy", "arf_supports", "arf_run", "arf_run_planned",
+              "arf_run_host", "arf_status_string", "arf_last_cuda_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(build.LIB)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared in arf.h but not exported: {missing}"
+
+
+def test_binding_covers_every_declared_symbol():
+    assert sorted(_binding.exported_names()) == declared_functions()
+    for n in declared_functions():
+        assert callable(getattr(arf, n)), n
+
+
+def test_status_strings():
+    for s in range(5):
+        assert arf.arf_status_string(s)
+    assert arf.arf_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("pattern", [arf.ARF_ALLREDUCE, arf.ARF_AR_RESIDUAL_RMSNORM])
+def test_supports_rules(pattern):
+    S = arf.arf_supports
+    bf = arf.ARF_BF16
+    assert S(None, pattern, 8, 2048, 7168, bf) == arf.ARF_OK
+    assert S(None, pattern, 1, 0, 8, arf.ARF_FP16) == arf.ARF_OK
+    assert S(None, pattern, 64, 1, 32768, bf) == arf.ARF_OK
+    assert S(None, pattern, 0, 1, 8, bf) == arf.ARF_ERR_UNSUPPORTED
+    assert S(None, pattern, 65, 1, 8, bf) == arf.ARF_ERR_UNSUPPORTED
+    assert S(None, pattern, 2, 1, 12, bf) == arf.ARF_ERR_UNSUPPORTED      # H % 8
+    assert S(None, pattern, 2, 1, 32776, bf) == arf.ARF_ERR_UNSUPPORTED   # H > max
+    assert S(None, pattern, 2, 1, 0, bf) == arf.ARF_ERR_INVALID_ARG
+    assert S(None, pattern, 2, -1, 8, bf) == arf.ARF_ERR_INVALID_ARG
+    assert S(None, pattern, 2, 1, 8, 7) == arf.ARF_ERR_INVALID_ARG
+    assert S(None, 9, 2, 1, 8, bf) == arf.ARF_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("pattern", [arf.ARF_ALLREDUCE, arf.ARF_AR_RESIDUAL_RMSNORM])
+@pytest.mark.parametrize("W,M,H", SHAPES)
+def test_planner_plans_are_legal(pattern, W, M, H):
+    for caps in (GB300, arf.DeviceCaps(148, 8, 2048), arf.DeviceCaps(132, 1, 2048), arf.DeviceCaps(1, 1, 1024)):
+        p = arf.Plan()
+        assert arf.arf_plan_for_caps(caps, pattern, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+        assert arf.arf_plan_check(caps, p, pattern, W, M, H, arf.ARF_BF16) == arf.ARF_OK, p
+        assert p.grid % p.cluster == 0 and p.threads % 32 == 0
+        assert p.w_spec in (0, W)
+        per_sm = caps.max_threads_per_sm // p.threads
+        if pattern == arf.ARF_ALLREDUCE:
+            assert p.path == arf.ARF_PATH_FLAT and p.cluster == 1
+            assert p.grid <= caps.num_sms * per_sm
+        else:
+            C = H // 8
+            assert p.threads * p.vpt * p.cluster >= C
+            if p.path == arf.ARF_PATH_CLUSTER:
+                assert M < caps.num_sms and 2 <= p.cluster <= caps.max_cluster
+                assert p.grid == p.cluster * min(M, max(1, caps.num_sms * per_sm // p.cluster))
+            else:
+                assert p.cluster == 1 and p.grid == max(1, min(M, caps.num_sms * per_sm))
+
+
+def test_planner_uses_the_sm_count():
+    """Small-M rows spread over about every SM; large M fills the device."""
+    p = arf.Plan()
+    arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 1, 7168, arf.ARF_BF16, p)
+    assert p.path == arf.ARF_PATH_CLUSTER and p.cluster == 16
+    arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 2048, 7168, arf.ARF_BF16, p)
+    assert p.path == arf.ARF_PATH_ROW and p.grid % 152 == 0
+    arf.arf_plan_for_caps(GB300, arf.ARF_ALLREDUCE, 4, 5851, 7168, arf.ARF_BF16, p)
+    assert p.grid % 152 == 0
+    no_cluster = arf.DeviceCaps(152, 1, 2048)
+    arf.arf_plan_for_caps(no_cluster, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 1, 7168, arf.ARF_BF16, p)
+    assert p.path == arf.ARF_PATH_ROW and p.grid == 1
+
+
+def test_plan_check_rejects_bad_plans():
+    good = arf.Plan()
+    args = (arf.ARF_AR_RESIDUAL_RMSNORM, 8, 64, 7168, arf.ARF_BF16)
+    assert arf.arf_plan_for_caps(GB300, *args, good) == arf.ARF_OK
+
+    def with_(**kw):
+        p = arf.Plan(**good.as_dict())
+        for k, v in kw.items():
+            setattr(p, k, v)
+        return arf.arf_plan_check(GB300, p, *args)
+
+    assert with_() == arf.ARF_OK
+    assert with_(threads=48) == arf.ARF_ERR_UNSUPPORTED
+    assert with_(threads=1024) == arf.ARF_ERR_UNSUPPORTED
+    assert with_(vpt=3) == arf.ARF_ERR_UNSUPPORTED
+    assert with_(w_spec=4) == arf.ARF_ERR_UNSUPPORTED
+    assert with_(path=arf.ARF_PATH_FLAT) == arf.ARF_ERR_UNSUPPORTED
+    assert with_(path=arf.ARF_PATH_CLUSTER, cluster=32, grid=64) == arf.ARF_ERR_UNSUPPORTED
+    assert with_(path=arf.ARF_PATH_CLUSTER, cluster=4, grid=6) == arf.ARF_ERR_UNSUPPORTED
+    assert with_(path=arf.ARF_PATH_ROW, cluster=1, threads=32, vpt=1) == arf.ARF_ERR_UNSUPPORTED  # 896 chunks
+    small = arf.DeviceCaps(152, 4, 2048)
+    p = arf.Plan(path=arf.ARF_PATH_CLUSTER, threads=64, vpt=1, cluster=16, grid=16, w_spec=8)
+    assert arf.arf_plan_check(small, p, *args) == arf.ARF_ERR_UNSUPPORTED
+    flat = arf.Plan(path=arf.ARF_PATH_FLAT, threads=256, vpt=4, cluster=1, grid=10, w_spec=16)
+    assert arf.arf_plan_check(GB300, flat, arf.ARF_ALLREDUCE, 16, 4, 64, arf.ARF_BF16) == arf.ARF_ERR_UNSUPPORTED
+    flat.vpt = 1
+    assert arf.arf_plan_check(GB300, flat, arf.ARF_ALLREDUCE, 16, 4, 64, arf.ARF_BF16) == arf.ARF_OK
+
+
+def test_staging_bytes():
+    M, H, W = 128, 4096, 2
+    plane = M * H * 2
+    ar = arf.arf_host_staging_bytes(arf.ARF_ALLREDUCE, W, M, H, arf.ARF_BF16)
+    rms = arf.arf_host_staging_bytes(arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16)
+    assert ar == 256 + (W + 1) * plane
+    assert rms == 256 + (W + 3) * plane + 8192
+    assert arf.arf_host_staging_bytes(arf.ARF_ALLREDUCE, 0, M, H, arf.ARF_BF16) == 0
+
+
+def test_calls_without_a_workspace_are_rejected():
+    assert arf.arf_run(None, 0, 2, None, None, None, 0.0, None, None, 1, 8, 0, None) == arf.ARF_ERR_INVALID_ARG
+    assert arf.arf_workspace_destroy(None) == arf.ARF_OK
+    assert arf.arf_last_cuda_error(None) == 0
+    c = arf.DeviceCaps()
+    assert arf.arf_workspace_caps(None, c) == arf.ARF_ERR_INVALID_ARG
+
+
+def test_workspace_create_without_gpu_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    assert arf.arf_workspace_create(0, h) == arf.ARF_ERR_CUDA
+    assert not h.value

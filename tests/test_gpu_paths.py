@@ -1,0 +1,358 @@
+"""Every kernel shape, ragged and edge sizes, and the call semantics of
+arf_run on the GPU, each checked against the CPU oracle.
+
+Covers: every launch plan shape (flat unroll factors, row and cluster paths
+with 2..16 CTAs, every chunks-per-thread count, grids smaller than the work),
+generic and specialised rank counts, W up to 64 and H up to 32768, ragged
+sizes, M = 0, in-place residual, input preservation, guard bands around the
+outputs, run-to-run determinism, rank-order permutations, the hand-worked
+rows, non-finite inputs, rejected calls, workspace churn, CUDA-graph replay
+and the host-buffer entry point."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import all_reduce_residual_gb300 as arf
+import oracle
+import pins
+from all_reduce_residual_gb300 import workloads as wl
+from gpu_util import DT, assert_parity, bitwise_equal, gpu_run, oracle_run, to_device
+
+pytestmark = pytest.mark.gpu
+RMS, AR = arf.ARF_AR_RESIDUAL_RMSNORM, arf.ARF_ALLREDUCE
+
+
+@pytest.fixture(scope="module")
+def ws():
+    with arf.Workspace(0) as w:
+        yield w
+
+
+def inputs(W, M, H, dtype="bf16", sigma=1.0, eps=1e-6, cid=900):
+    return wl.make_inputs(wl.custom(W, M, H, dtype, sigma, eps, config_id=cid))
+
+
+def check(ws, pattern, inp, plan=None, in_place=False, what=""):
+    P, R, G = to_device(inp)
+    got = gpu_run(ws, pattern, P, R, G, inp.workload.eps, plan=plan, in_place=in_place)
+    ref = oracle_run(pattern, inp)
+    assert_parity(DT[inp.workload.dtype], pattern, got, ref, what)
+    return got
+
+
+def rms_plans(ws, W, M, H, grids=("full", 1)):
+    """Every legal RMS plan shape for these sizes on this device."""
+    caps = ws.caps
+    C = H // 8
+    plans = []
+    for cs in (1, 2, 4, 8, 16):
+        if cs > caps.max_cluster:
+            continue
+        slice_ = -(-C // cs)
+        for vpt in (1, 2, 4, 8):
+            per_thread = -(-slice_ // vpt)
+            threads = max(32, -(-per_thread // 32) * 32)
+            if threads > 512:
+                continue
+            for g in grids:
+                nclus = min(M, 2 * caps.num_sms) if g == "full" else g
+                for w_spec in {0, W if W in (1, 2, 4, 8, 16) else 0}:
+                    p = arf.Plan(path=arf.ARF_PATH_ROW if cs == 1 else arf.ARF_PATH_CLUSTER, threads=threads,
+                                 vpt=vpt, cluster=cs, grid=max(1, nclus) * cs, w_spec=w_spec)
+                    assert arf.arf_plan_check(caps, p, RMS, W, M, H, arf.ARF_BF16) == arf.ARF_OK, p
+                    plans.append(p)
+    return plans
+
+
+@pytest.mark.parametrize("W,M,H,dtype", [(3, 37, 1000, "bf16"), (8, 5, 7168, "bf16"), (16, 3, 4096, "fp16"),
+                                         (1, 9, 8, "bf16"), (64, 2, 256, "fp16"), (5, 4, 32768, "bf16"),
+                                         (2, 19, 2056, "bf16")])
+def test_every_rms_plan(ws, W, M, H, dtype):
+    inp = inputs(W, M, H, dtype)
+    ref = oracle_run(RMS, inp)
+    P, R, G = to_device(inp)
+    ro_first = None
+    ran = 0
+    for plan in rms_plans(ws, W, M, H):
+        try:
+            got = gpu_run(ws, RMS, P, R, G, inp.workload.eps, plan=plan)
+        except arf.ArfError as e:  # a cluster shape this device cannot keep resident
+            assert e.status == arf.ARF_ERR_UNSUPPORTED and plan.cluster > 1, e
+            continue
+        ran += 1
+        assert_parity(DT[dtype], RMS, got, ref, f"{plan}")
+        if ro_first is None:
+            ro_first = got[1]
+        assert np.array_equal(got[1], ro_first)
+    assert ran >= 4
+
+
+@pytest.mark.parametrize("W,M,H,dtype", [(3, 37, 1000, "bf16"), (2, 1, 8, "bf16"), (16, 11, 2056, "fp16"),
+                                         (8, 3, 7168, "bf16"), (4, 5, 264, "fp16"), (1, 7, 24, "bf16")])
+def test_every_flat_plan(ws, W, M, H, dtype):
+    inp = inputs(W, M, H, dtype)
+    ref = oracle_run(AR, inp)
+    P, R, G = to_device(inp)
+    specs = {0, W if W in (1, 2, 4, 8, 16) else 0}
+    for w_spec in specs:
+        for u in (1, 2, 4):
+            for threads in (32, 256, 512):
+                for grid in (1, 7, 1000):
+                    p = arf.Plan(path=arf.ARF_PATH_FLAT, threads=threads, vpt=u, cluster=1, grid=grid, w_spec=w_spec)
+                    if arf.arf_plan_check(ws.caps, p, AR, W, M, H, DT[dtype]) != arf.ARF_OK:
+                        continue
+                    got = gpu_run(ws, AR, P, R, G, 0.0, plan=p)
+                    assert_parity(DT[dtype], AR, got, ref, f"{p}")
+
+
+@pytest.mark.parametrize("W", [3, 5, 6, 7, 9, 12, 17, 31, 32, 33, 63, 64])
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_generic_rank_counts(ws, W, pattern):
+    check(ws, pattern, inputs(W, 3, 264, "bf16" if W % 2 else "fp16", sigma=0.3), what=f"W={W}")
+
+
+@pytest.mark.parametrize("M,H", [(1, 8), (1, 32768), (2500, 64), (5000, 8), (3, 7176)])
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_ragged_and_extreme_shapes(ws, M, H, pattern):
+    check(ws, pattern, inputs(4, M, H), what=f"M={M} H={H}")
+
+
+def test_zero_rows_launch_nothing(ws):
+    P = [torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    out = torch.full((16,), 7, dtype=torch.int16, device="cuda")
+    st = arf.arf_run(ws.handle, RMS, 2, arf.pointer_array(P).data_ptr(), out.data_ptr(), out.data_ptr(), 1e-6,
+                     out.data_ptr(), out.data_ptr() + 16, 0, 64, arf.ARF_BF16, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == arf.ARF_OK
+    assert (out == 7).all()
+
+
+def _guarded(M, H, dt, pad=2048):
+    buf = torch.full((M * H + 2 * pad,), -12345, dtype=torch.int16, device="cuda")
+    return buf, buf[pad:pad + M * H].view(dt).view(M, H)
+
+
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_guard_bands_and_input_preservation(ws, pattern):
+    inp = inputs(8, 33, 7168)
+    P, R, G = to_device(inp)
+    copies = [p.clone() for p in P] + [R.clone(), G.clone()]
+    ob, out = _guarded(33, 7168, torch.bfloat16)
+    rb, ro = _guarded(33, 7168, torch.bfloat16)
+    arf.run(ws, pattern, P, R, G, 1e-6, out=out, residual_out=ro if pattern == RMS else None)
+    torch.cuda.synchronize()
+    for buf in (ob, rb):
+        assert (buf[:2048] == -12345).all() and (buf[-2048:] == -12345).all(), "write outside the output"
+    for a, b in zip(P + [R, G], copies):
+        assert torch.equal(a, b), "an input was modified"
+    ref = oracle_run(pattern, inp)
+    got = (wl.codes(out.cpu()), wl.codes(ro.cpu()) if pattern == RMS else None)
+    assert_parity(oracle.BF16, pattern, got, ref)
+
+
+def test_in_place_residual(ws):
+    inp = inputs(8, 70, 7168)
+    P, R, G = to_device(inp)
+    for plan in rms_plans(ws, 8, 70, 7168, grids=("full",))[:6] + [None]:
+        a = gpu_run(ws, RMS, P, R, G, 1e-6, plan=plan)
+        b = gpu_run(ws, RMS, P, R, G, 1e-6, plan=plan, in_place=True)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert_parity(oracle.BF16, RMS, b, oracle_run(RMS, inp))
+
+
+def test_run_to_run_determinism(ws):
+    inp = inputs(8, 64, 7168, sigma=0.25)
+    P, R, G = to_device(inp)
+    first = gpu_run(ws, RMS, P, R, G, 1e-6)
+    outs = []
+    ro = torch.empty_like(R)
+    for _ in range(100):
+        o, _ = arf.run(ws, RMS, P, R, G, 1e-6, residual_out=ro)
+        outs.append(o)
+    torch.cuda.synchronize()
+    for o in outs:
+        assert np.array_equal(wl.codes(o.cpu()), first[0])
+    assert np.array_equal(wl.codes(ro.cpu()), first[1])
+
+
+def test_rank_order_permutations(ws):
+    inp = inputs(8, 16, 1024, sigma=2.0)
+    P, R, G = to_device(inp)
+    for order in ([7, 6, 5, 4, 3, 2, 1, 0], [3, 1, 4, 0, 5, 2, 7, 6]):
+        Pp = [P[i] for i in order]
+        got = gpu_run(ws, RMS, Pp, R, G, 1e-6)
+        assert_parity(oracle.BF16, RMS, got, oracle_run(RMS, inp, order=order), f"order {order}")
+    same = [P[0]] * 8
+    a = gpu_run(ws, RMS, same, R, G, 1e-6)
+    b = gpu_run(ws, RMS, same[::-1], R, G, 1e-6)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    two = inputs(2, 16, 1024, sigma=3.0)
+    P2, R2, G2 = to_device(two)
+    a = gpu_run(ws, RMS, P2, R2, G2, 1e-6)
+    b = gpu_run(ws, RMS, P2[::-1], R2, G2, 1e-6)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_worked_rows_on_gpu(ws):
+    for case in pins.load_golden():
+        dtype = DT[case["dtype"]]
+        pat = AR if case["pattern"] == "allreduce" else RMS
+        W = sum(1 for k in case if k.startswith("p") and k[1:].isdigit())
+        dt = torch.bfloat16 if dtype == oracle.BF16 else torch.float16
+        dname = case["dtype"]
+        P = [wl.from_codes(pins.exact_codes(dtype, case[f"p{r}"])[None, :], dname).cuda() for r in range(W)]
+        R = G = None
+        eps = 0.0
+        if pat == RMS:
+            R = wl.from_codes(pins.exact_codes(dtype, case["residual"])[None, :], dname).cuda()
+            G = wl.from_codes(pins.exact_codes(dtype, case["gamma"]), dname).cuda()
+            eps = float(case["eps"])
+        out, ro = arf.run(ws, pat, P, R, G, eps)
+        torch.cuda.synchronize()
+        want = pins.exact_codes(dtype, case["expect_out"])
+        got = wl.codes(out.cpu())[0]
+        assert out.dtype == dt
+        if pat == RMS:
+            assert np.array_equal(wl.codes(ro.cpu())[0], pins.exact_codes(dtype, case["expect_residual_out"])), \
+                case["case"]
+        assert np.array_equal(got, want), (case["case"], got, want)
+
+
+def test_non_finite_inputs_propagate(ws):
+    H = 64
+    p0 = torch.zeros((2, H), dtype=torch.bfloat16)
+    p1 = torch.zeros((2, H), dtype=torch.bfloat16)
+    p0[0, 0], p1[0, 0] = float("inf"), float("-inf")   # inf + -inf = NaN
+    p0[0, 1] = float("nan")
+    p0[1, 0] = float("inf")                            # inf row: inf * 0 in the norm
+    R = torch.zeros((2, H), dtype=torch.bfloat16)
+    G = torch.ones((H,), dtype=torch.bfloat16)
+    P = [p0.cuda(), p1.cuda()]
+    out, ro = arf.run(ws, RMS, P, R.cuda(), G.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    ref = oracle.run(oracle.AR_RESIDUAL_RMSNORM, [wl.codes(p0), wl.codes(p1)], wl.codes(R), wl.codes(G), 1e-6)
+    assert bitwise_equal(oracle.BF16, wl.codes(ro.cpu()), ref[1]).all()
+    assert bitwise_equal(oracle.BF16, wl.codes(out.cpu()), ref[0]).all()
+    assert torch.isnan(ro[0, 0].float()) and torch.isnan(ro[0, 1].float()) and torch.isinf(ro[1, 0].float())
+
+
+def test_zero_rows_and_eps(ws):
+    P = [torch.zeros((3, 64), dtype=torch.bfloat16, device="cuda")] * 2
+    R = torch.zeros((3, 64), dtype=torch.bfloat16, device="cuda")
+    G = torch.ones((64,), dtype=torch.bfloat16, device="cuda")
+    out, _ = arf.run(ws, RMS, P, R, G, 1e-6)
+    assert (out.float() == 0).all()
+    out, _ = arf.run(ws, RMS, P, R, G, 0.0)  # 0 * rsqrt(0) = 0 * inf = NaN, as the formula says
+    assert torch.isnan(out.float()).all()
+
+
+def test_rejected_calls_write_nothing(ws):
+    M, H = 4, 64
+    P = [torch.randn((M, H), device="cuda").to(torch.bfloat16) for _ in range(2)]
+    R = torch.randn((M, H), device="cuda").to(torch.bfloat16)
+    G = torch.ones((H,), device="cuda", dtype=torch.bfloat16)
+    ptrs = arf.pointer_array(P)
+    out = torch.full((M * H + 8,), 99, dtype=torch.int16, device="cuda")
+    ro = torch.full((M * H + 8,), 99, dtype=torch.int16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    o, r = out.data_ptr(), ro.data_ptr()
+
+    def call(pattern=RMS, W=2, pp=ptrs.data_ptr(), res=R.data_ptr(), g=G.data_ptr(), eps=1e-6, oo=o, rr=r, m=M,
+             h=H, dt=arf.ARF_BF16):
+        return arf.arf_run(ws.handle, pattern, W, pp, res, g, eps, oo, rr, m, h, dt, s)
+
+    assert call(W=0) == arf.ARF_ERR_UNSUPPORTED
+    assert call(W=65) == arf.ARF_ERR_UNSUPPORTED
+    assert call(h=12) == arf.ARF_ERR_UNSUPPORTED
+    assert call(h=32776) == arf.ARF_ERR_UNSUPPORTED
+    assert call(m=-1) == arf.ARF_ERR_INVALID_ARG
+    assert call(pp=None) == arf.ARF_ERR_INVALID_ARG
+    assert call(res=None) == arf.ARF_ERR_INVALID_ARG
+    assert call(g=None) == arf.ARF_ERR_INVALID_ARG
+    assert call(rr=None) == arf.ARF_ERR_INVALID_ARG
+    assert call(oo=None) == arf.ARF_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == arf.ARF_ERR_INVALID_ARG
+    assert call(eps=float("inf")) == arf.ARF_ERR_INVALID_ARG
+    assert call(eps=-1e-6) == arf.ARF_ERR_INVALID_ARG
+    assert call(rr=o) == arf.ARF_ERR_INVALID_ARG                 # out == residual_out
+    assert call(oo=o + 2) == arf.ARF_ERR_UNSUPPORTED             # misaligned out
+    assert call(rr=r + 8) == arf.ARF_ERR_UNSUPPORTED             # misaligned residual_out
+    assert call(res=R.data_ptr() + 2) == arf.ARF_ERR_UNSUPPORTED
+    assert call(pattern=7) == arf.ARF_ERR_INVALID_ARG
+    assert call(dt=5) == arf.ARF_ERR_INVALID_ARG
+    bad = arf.Plan(path=arf.ARF_PATH_ROW, threads=48, vpt=1, cluster=1, grid=1, w_spec=2)  # not whole warps
+    assert arf.arf_run_planned(ws.handle, bad, RMS, 2, ptrs.data_ptr(), R.data_ptr(), G.data_ptr(), 1e-6, o, r, M, H,
+                               arf.ARF_BF16, s) == arf.ARF_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert (out == 99).all() and (ro == 99).all()
+    assert call() == arf.ARF_OK
+    torch.cuda.synchronize()
+    assert not (out[:M * H] == 99).all()
+
+
+def test_device_mismatch_on_wrong_current_device():
+    # Only one device is visible: a workspace for a device that does not exist fails cleanly.
+    h = ctypes.c_void_p()
+    assert arf.arf_workspace_create(torch.cuda.device_count(), h) == arf.ARF_ERR_CUDA
+    assert arf.arf_workspace_create(-1, h) == arf.ARF_ERR_CUDA
+
+
+def test_workspace_churn(ws):
+    inp = inputs(2, 4, 64)
+    P, R, G = to_device(inp)
+    for _ in range(100):
+        with arf.Workspace(0) as w:
+            out, _ = arf.run(w, AR, P)
+    torch.cuda.synchronize()
+    assert_parity(oracle.BF16, AR, (wl.codes(out.cpu()), None), oracle_run(AR, inp))
+
+
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_cuda_graph_replay(ws, pattern):
+    """Capture once, replay with new values in the same buffers: results
+    match the oracle and the inputs are preserved across replays."""
+    W, M, H = 4, 64, 4096
+    first = inputs(W, M, H, cid=910)
+    P, R, G = to_device(first)
+    ptrs = arf.pointer_array(P)
+    out = torch.empty_like(R)
+    ro = torch.empty_like(R)
+    # warm the plan cache outside capture
+    arf.run(ws, pattern, P, R, G, 1e-6, out=out, residual_out=ro if pattern == RMS else None, ptrs=ptrs)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            arf.run(ws, pattern, P, R, G, 1e-6, out=out, residual_out=ro if pattern == RMS else None, ptrs=ptrs)
+    for k in range(3):
+        inp = inputs(W, M, H, cid=920 + k)
+        for dst, src in zip(P + [R, G], inp.partials + [inp.residual, inp.gamma]):
+            dst.copy_(src)
+        keep = [t.clone() for t in P + [R, G]]
+        g.replay()
+        torch.cuda.synchronize()
+        got = (wl.codes(out.cpu()), wl.codes(ro.cpu()) if pattern == RMS else None)
+        assert_parity(oracle.BF16, pattern, got, oracle_run(pattern, inp), f"replay {k}")
+        for a, b in zip(P + [R, G], keep):
+            assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("name,pattern", [("small", RMS), ("llama_tp2", AR), ("llama_tp2", RMS)])
+def test_host_buffer_entry_point(ws, name, pattern, pinned):
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w)
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
+    P = [pin(p) for p in inp.partials]
+    R, G = pin(inp.residual), pin(inp.gamma)
+    out = pin(torch.empty_like(inp.residual))
+    ro = pin(torch.empty_like(inp.residual))
+    runner = arf.HostRunner(ws, pattern, w.W, w.M, w.H, torch.bfloat16)
+    for _ in range(2):
+        runner(P, R, G, w.eps, out, ro)
+        torch.cuda.synchronize()
+        got = (wl.codes(out), wl.codes(ro) if pattern == RMS else None)
+        assert_parity(DT[w.dtype], pattern, got, oracle_run(pattern, inp))
