@@ -248,9 +248,11 @@ cudaError_t max_active_clusters(arf_dtype_t dt, const arf_plan_t& pl, int* n) {
 }
 
 // The planner's plan, with the cluster size lowered until the cluster kernel
-// instance can actually be made resident on this device.
+// instance can actually be made resident on this device. During stream
+// capture no occupancy query is made: the plan then rests on the cluster
+// limit probed at workspace creation.
 arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64_t M, int64_t H,
-                         arf_dtype_t dtype, arf_plan_t* out) {
+                         arf_dtype_t dtype, arf_plan_t* out, bool capturing = false) {
     const auto key = std::make_tuple((int)pattern, W, M, H, (int)dtype);
     {
         std::lock_guard<std::mutex> lk(ws->mu);
@@ -263,7 +265,7 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
     arf_plan_t pl;
     arf_status_t st = arf_plan_for_caps(&ws->caps, pattern, W, M, H, dtype, &pl);
     if (st != ARF_OK) return st;
-    while (pl.path == ARF_PATH_CLUSTER) {
+    while (!capturing && pl.path == ARF_PATH_CLUSTER) {
         int n = 0;
         cudaError_t e = max_active_clusters(dtype, pl, &n);
         if (e == cudaSuccess && n > 0) break;
@@ -300,11 +302,19 @@ arf_status_t check_call(arf_workspace_t ws, arf_pattern_t pattern, const void* c
     return ARF_OK;
 }
 
-arf_status_t check_device(arf_workspace_t ws, cudaStream_t stream) {
+// Current device and stream device must be the workspace's. While `stream`
+// is being captured into a graph, only capture-safe queries are made (the
+// stream's device cannot be queried then; *capturing reports it).
+arf_status_t check_device(arf_workspace_t ws, cudaStream_t stream, bool* capturing) {
     int cur = -1;
     cudaError_t e = cudaGetDevice(&cur);
     if (e != cudaSuccess) return cuda_fail(ws, e);
     if (cur != ws->device) return ARF_ERR_DEVICE_MISMATCH;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return cuda_fail(ws, e);
+    *capturing = cs != cudaStreamCaptureStatusNone;
+    if (*capturing) return ARF_OK;
     int sdev = -1;
     e = cudaStreamGetDevice(stream, &sdev);
     if (e != cudaSuccess) return cuda_fail(ws, e);
@@ -357,12 +367,13 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_plan_t* forced, arf_pattern_
     st = check_call(ws, pattern, partials, residual, gamma, eps, out, residual_out);
     if (st != ARF_OK) return st;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-    st = check_device(ws, stream);
+    bool capturing = false;
+    st = check_device(ws, stream, &capturing);
     if (st != ARF_OK) return st;
     arf_plan_t pl;
     if (forced) {
         pl = *forced;
-        if (pl.path == ARF_PATH_CLUSTER) {
+        if (pl.path == ARF_PATH_CLUSTER && !capturing) {
             // a cluster shape must fit the device: no launch that cannot start
             int n = 0;
             cudaError_t e = max_active_clusters(dtype, pl, &n);
@@ -370,7 +381,7 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_plan_t* forced, arf_pattern_
             if (n < 1) return ARF_ERR_UNSUPPORTED;
         }
     } else {
-        st = device_plan(ws, pattern, W, M, H, dtype, &pl);
+        st = device_plan(ws, pattern, W, M, H, dtype, &pl, capturing);
         if (st != ARF_OK) return st;
     }
     return launch(ws, pl, pattern, W, partials, residual, gamma, eps, out, residual_out, M, H, dtype, stream);
@@ -483,7 +494,8 @@ extern "C" arf_status_t arf_run_host(arf_workspace_t ws, arf_pattern_t pattern, 
     if (!staging_dev || (reinterpret_cast<uintptr_t>(staging_dev) & 255u) != 0 || staging_bytes < L.total)
         return ARF_ERR_INVALID_ARG;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-    st = check_device(ws, stream);
+    bool capturing = false;
+    st = check_device(ws, stream, &capturing);
     if (st != ARF_OK) return st;
 
     char* base = static_cast<char*>(staging_dev);

@@ -160,7 +160,12 @@ arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_plan_t* pla
 /* Run one pattern, asynchronously on `stream` (a cudaStream_t; NULL = the
  * legacy default stream). No allocation, no host synchronisation and no host
  * read of device data, so the call can be captured into a CUDA graph; a
- * captured graph bakes in the pointer values, so keep them stable.
+ * captured graph bakes in the pointer values, so keep them stable. Make one
+ * uncaptured call per shape first: it memoises the plan after checking on
+ * the device that its cluster shape can be resident (a first call made under
+ * capture skips that query and relies on the cluster limit probed when the
+ * workspace was created). While capturing, the stream's device is not
+ * checked (CUDA does not allow that query then).
  *
  *   partials_dev  DEVICE array of W device pointers, each to an [M,H] tensor;
  *                 ranks are summed in this array's order. Every pointer must

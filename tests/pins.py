@@ -40,7 +40,8 @@ def lib_decode(dtype: int, codes) -> np.ndarray:
     c = np.ascontiguousarray(codes, dtype=np.uint16)
     if dtype == BF16:
         return torch.from_numpy(c.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
-    return c.view(np.float16).astype(np.float32)
+    with np.errstate(invalid="ignore"):
+        return c.view(np.float16).astype(np.float32)
 
 
 _TABLES = {}
@@ -51,7 +52,8 @@ def _table(dtype: int):
     final entry 2^(emax+1) standing for +inf (the value overflow rounds to)."""
     if dtype not in _TABLES:
         all_codes = np.arange(0x8000, dtype=np.uint16)
-        v = lib_decode(dtype, all_codes).astype(np.float64)
+        with np.errstate(invalid="ignore"):
+            v = lib_decode(dtype, all_codes).astype(np.float64)
         fin = np.isfinite(v)
         vals, codes = v[fin], all_codes[fin]
         order = np.argsort(vals, kind="stable")
