@@ -32,6 +32,7 @@ ARF_PATH_ROW = 1
 ARF_PATH_CLUSTER = 2
 ARF_MAX_W = 64
 ARF_MAX_H = 32768
+ARF_STATIC_STAGING_BYTES = 16 << 20
 
 STATUS_NAMES = {0: "ARF_OK", 1: "ARF_ERR_INVALID_ARG", 2: "ARF_ERR_UNSUPPORTED", 3: "ARF_ERR_CUDA",
                 4: "ARF_ERR_DEVICE_MISMATCH"}
@@ -78,6 +79,8 @@ _SIGNATURES = {
     "arf_host_staging_bytes": (_c.c_size_t, [_c.c_int, _c.c_int, _i64, _i64, _c.c_int]),
     "arf_run_host": (_c.c_int, [_vp, _c.c_int, _c.c_int, _c.POINTER(_vp), _vp, _vp, _c.c_float, _vp, _vp, _i64,
                                 _i64, _c.c_int, _vp, _c.c_size_t, _vp]),
+    "arf_run_host_static": (_c.c_int, [_vp, _c.c_int, _c.c_int, _c.POINTER(_vp), _vp, _vp, _c.c_float, _vp, _vp,
+                                       _i64, _i64, _c.c_int, _vp]),
 }
 
 _lib = None
@@ -177,3 +180,12 @@ def arf_run_host(ws, pattern, W, partials_host, residual_host, gamma_host, eps, 
     arr = (ctypes.c_void_p * W)(*partials_host)
     return load().arf_run_host(ws, pattern, W, arr, residual_host, gamma_host, eps, out_host, residual_out_host,
                                M, H, dtype, staging_dev, staging_bytes, stream)
+
+
+def arf_run_host_static(ws, pattern, W, partials_host, residual_host, gamma_host, eps, out_host,
+                        residual_out_host, M, H, dtype, stream) -> int:
+    """arf_run_host with the library's built-in staging array (allocates
+    nothing). partials_host: a sequence of W host addresses (ints)."""
+    arr = (ctypes.c_void_p * W)(*partials_host)
+    return load().arf_run_host_static(ws, pattern, W, arr, residual_host, gamma_host, eps, out_host,
+                                      residual_out_host, M, H, dtype, stream)

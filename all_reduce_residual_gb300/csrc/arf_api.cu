@@ -423,6 +423,8 @@ extern "C" arf_status_t arf_run_planned(arf_workspace_t ws, const arf_plan_t* pl
 
 namespace arf {
 
+void note_cuda_error(arf_workspace_t ws, cudaError_t e) { (void)cuda_fail(ws, e); }
+
 __global__ void fill_pointer_array(const void** array, const char* first, int64_t stride, int W) {
     for (int r = threadIdx.x; r < W; r += blockDim.x) array[r] = first + (int64_t)r * stride;
 }

@@ -61,6 +61,9 @@ cudaError_t allow_large_clusters_fp16();
 cudaError_t rms_max_active_clusters_bf16(const arf_plan_t& plan, int* n);
 cudaError_t rms_max_active_clusters_fp16(const arf_plan_t& plan, int* n);
 
+// Record a CUDA error as the workspace's last one (arf_last_cuda_error).
+void note_cuda_error(arf_workspace_t ws, cudaError_t e);
+
 // Host-buffer helper kernel launcher (arf_api.cu).
 cudaError_t launch_fill_pointer_array(const void** array, const char* first, int64_t stride, int W,
                                       cudaStream_t s);

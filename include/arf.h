@@ -229,6 +229,37 @@ arf_status_t arf_run_host(arf_workspace_t ws, arf_pattern_t pattern, int W,
                           int64_t M, int64_t H, arf_dtype_t dtype,
                           void* staging_dev, size_t staging_bytes, void* stream);
 
+/* ---- host buffers, no device allocation ------------------------------- */
+
+/* Size of the staging array built into the library for arf_run_host_static. */
+#define ARF_STATIC_STAGING_BYTES (16u << 20) /* 16 MiB */
+
+/* arf_run_host for callers that cannot allocate device memory. There is no
+ * counterpart on the source pages: it exists for callers such as a plugin
+ * inside a framework or serving engine whose allocator owns the device
+ * memory, or a latency-critical host thread that cannot pay for cudaMalloc's
+ * implicit synchronisation, neither of which can hand arf_run_host a staging
+ * buffer. It allocates nothing (no cudaMalloc, no cudaFree, no allocating
+ * library call): the staging lives in a file-scope device array of
+ * ARF_STATIC_STAGING_BYTES bytes compiled into the library, which every GPU
+ * that loads the library holds until the process exits.
+ *
+ * Arguments, results and errors are those of arf_run_host without the staging
+ * arguments; sizes whose staging (arf_host_staging_bytes) exceeds
+ * ARF_STATIC_STAGING_BYTES are rejected with ARF_ERR_UNSUPPORTED before
+ * anything is enqueued. The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current); make that
+ * first call before any stream capture. Every call on a device shares the one
+ * array, which keeps the last call's contents (no call relies on it starting
+ * at zero: each call writes every byte it reads). Calls whose GPU work can
+ * overlap (other streams, other threads) race on the array: serialise them,
+ * for example on one stream. */
+arf_status_t arf_run_host_static(arf_workspace_t ws, arf_pattern_t pattern, int W,
+                                 const void* const* partials_host,
+                                 const void* residual_host, const void* gamma_host, float eps,
+                                 void* out_host, void* residual_out_host,
+                                 int64_t M, int64_t H, arf_dtype_t dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
