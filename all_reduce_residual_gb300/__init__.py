@@ -12,9 +12,9 @@ import ctypes
 from ._binding import (  # noqa: F401  (re-exported C-ABI names)
     ARF_AR_RESIDUAL_RMSNORM, ARF_ALLREDUCE, ARF_BF16, ARF_ERR_CUDA, ARF_ERR_DEVICE_MISMATCH,
     ARF_ERR_INVALID_ARG, ARF_ERR_UNSUPPORTED, ARF_FP16, ARF_MAX_H, ARF_MAX_W, ARF_OK, ARF_PATH_CLUSTER,
-    ARF_PATH_FLAT, ARF_PATH_ROW, ARF_STATIC_STAGING_BYTES, ArfError, DeviceCaps, Plan, arf_host_staging_bytes,
-    arf_last_cuda_error, arf_plan_check, arf_plan_for_caps, arf_run, arf_run_host, arf_run_host_static,
-    arf_run_planned, arf_status_string, arf_supports,
+    ARF_PATH_FLAT, ARF_PATH_ROW, ARF_STATIC_STAGING_BYTES, ArfError, DeviceCaps, Plan, RunOpts,
+    arf_host_staging_bytes, arf_last_cuda_error, arf_plan_check, arf_plan_for_caps, arf_run, arf_run_ex,
+    arf_run_host, arf_run_host_static, arf_run_planned, arf_status_string, arf_supports,
     arf_workspace_caps, arf_workspace_create, arf_workspace_destroy, arf_workspace_plan, load,
 )
 
@@ -104,12 +104,15 @@ def _check_operand(t, name, shape, dtype, device):
 
 
 def run(ws: Workspace, pattern, partials, residual=None, gamma=None, eps: float = 0.0, out=None,
-        residual_out=None, stream=None, plan: Plan | None = None, ptrs=None):
+        residual_out=None, stream=None, plan: Plan | None = None, ptrs=None, by_value: bool = False,
+        pdl: bool = False):
     """Run one pattern on CUDA tensors.
 
     partials: list of W [M,H] tensors (rank order). ``ptrs`` may be passed
     instead of building the pointer array here (for CUDA-graph capture, keep
     it alive and stable). out / residual_out are allocated when None.
+    by_value / pdl / plan: the options of arf_run_ex (partials passed in the
+    launch, programmatic dependent launch, an explicit launch plan).
     Returns (out, residual_out); residual_out is None for kAllReduce.
     """
     torch = _torch()
@@ -137,13 +140,26 @@ def run(ws: Workspace, pattern, partials, residual=None, gamma=None, eps: float 
         _check_operand(residual_out, "residual_out", (M, H), dt, dev)
         r_ptr, g_ptr, ro_ptr = residual.data_ptr(), gamma.data_ptr(), residual_out.data_ptr()
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    if ptrs is None:
-        ptrs = pointer_array(P, dev)
-        if stream is not None and M > 0:
-            ptrs.record_stream(s)  # the temporary array must outlive the kernel
-    args = (pat, W, ptrs.data_ptr(), r_ptr, g_ptr, float(eps), out.data_ptr(), ro_ptr, M, H, dtype_code(dt),
-            s.cuda_stream)
-    st = arf_run_planned(ws.handle, plan, *args) if plan is not None else arf_run(ws.handle, *args)
+    tail = (r_ptr, g_ptr, float(eps), out.data_ptr(), ro_ptr, M, H, dtype_code(dt), s.cuda_stream)
+    if by_value or pdl:
+        opts = RunOpts(plan=ctypes.pointer(plan) if plan is not None else None, partials_by_value=int(by_value),
+                       pdl=int(pdl))
+        if by_value:
+            parts = [p.data_ptr() for p in P]
+        else:
+            if ptrs is None:
+                ptrs = pointer_array(P, dev)
+                if stream is not None and M > 0:
+                    ptrs.record_stream(s)
+            parts = ptrs.data_ptr()
+        st = arf_run_ex(ws.handle, opts, pat, W, parts, *tail)
+    else:
+        if ptrs is None:
+            ptrs = pointer_array(P, dev)
+            if stream is not None and M > 0:
+                ptrs.record_stream(s)  # the temporary array must outlive the kernel
+        args = (pat, W, ptrs.data_ptr(), *tail)
+        st = arf_run_planned(ws.handle, plan, *args) if plan is not None else arf_run(ws.handle, *args)
     if st != ARF_OK:
         raise ArfError(st, "arf_run", arf_last_cuda_error(ws.handle) if st == ARF_ERR_CUDA else 0)
     return out, (residual_out if rms else None)

@@ -57,6 +57,10 @@ class Plan(ctypes.Structure):
         return "Plan(" + ", ".join(f"{k}={v}" for k, v in self.as_dict().items()) + ")"
 
 
+class RunOpts(ctypes.Structure):
+    _fields_ = [("plan", ctypes.POINTER(Plan)), ("partials_by_value", ctypes.c_int), ("pdl", ctypes.c_int)]
+
+
 _c = ctypes
 _vp = _c.c_void_p
 _i64 = _c.c_int64
@@ -76,6 +80,8 @@ _SIGNATURES = {
                            _vp]),
     "arf_run_planned": (_c.c_int, [_vp, _c.POINTER(Plan), _c.c_int, _c.c_int, _vp, _vp, _vp, _c.c_float, _vp,
                                    _vp, _i64, _i64, _c.c_int, _vp]),
+    "arf_run_ex": (_c.c_int, [_vp, _c.POINTER(RunOpts), _c.c_int, _c.c_int, _vp, _vp, _vp, _c.c_float, _vp, _vp,
+                              _i64, _i64, _c.c_int, _vp]),
     "arf_host_staging_bytes": (_c.c_size_t, [_c.c_int, _c.c_int, _i64, _i64, _c.c_int]),
     "arf_run_host": (_c.c_int, [_vp, _c.c_int, _c.c_int, _c.POINTER(_vp), _vp, _vp, _c.c_float, _vp, _vp, _i64,
                                 _i64, _c.c_int, _vp, _c.c_size_t, _vp]),
@@ -168,6 +174,17 @@ def arf_run_planned(ws, plan: Plan, pattern, W, partials_dev, residual, gamma, e
                     dtype, stream) -> int:
     return load().arf_run_planned(ws, ctypes.byref(plan), pattern, W, partials_dev, residual, gamma, eps, out,
                                   residual_out, M, H, dtype, stream)
+
+
+def arf_run_ex(ws, opts, pattern, W, partials, residual, gamma, eps, out, residual_out, M, H, dtype,
+               stream) -> int:
+    """opts: a RunOpts or None. With opts.partials_by_value, `partials` is a
+    sequence of W device addresses (a host array is built here); else the
+    address of a device array of W pointers."""
+    if opts is not None and opts.partials_by_value:
+        partials = ctypes.cast((ctypes.c_void_p * W)(*partials), ctypes.c_void_p)
+    return load().arf_run_ex(ws, ctypes.byref(opts) if opts is not None else None, pattern, W, partials, residual,
+                             gamma, eps, out, residual_out, M, H, dtype, stream)
 
 
 def arf_host_staging_bytes(pattern, W, M, H, dtype) -> int:

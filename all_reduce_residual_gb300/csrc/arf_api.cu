@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
+#include <climits>
 #include <map>
 #include <mutex>
 #include <new>
@@ -35,37 +36,25 @@ arf_status_t cuda_fail(arf_workspace_t ws, cudaError_t e) {
     return ARF_ERR_CUDA;
 }
 
-// Threads and chunks per thread for a slice of `slice` 16-byte chunks: the
-// fewest chunks per thread that keep the CTA at <= 256 threads (<= 512 for
-// the widest rows), threads rounded up to whole warps.
-void shape_cta(int slice, int* threads, int* vpt) {
-    int v = 1;
-    while (v < 8 && ceil_div(slice, v) > 256) v *= 2;
-    int t = (int)ceil_div(ceil_div(slice, v), 32) * 32;
-    *vpt = v;
-    *threads = t < 32 ? 32 : t;
-}
-
-// The RMS plan for a given cluster size.
-arf_plan_t rms_plan(const arf_device_caps_t& caps, int w_spec, int64_t M, int64_t H, int cs) {
+// The RMS plan for a given cluster size and chunks-per-thread count: threads
+// cover the CTA's slice in whole warps; grid = rows (clusters) up to what the
+// SMs can hold by thread count (the workspace refines this by occupancy).
+arf_plan_t rms_plan(const arf_device_caps_t& caps, int w_spec, int64_t M, int64_t H, int cs, int vpt) {
     arf_plan_t pl = {};
     const int C = (int)(H / 8);
     const int slice = (int)ceil_div(C, cs);
-    shape_cta(slice, &pl.threads, &pl.vpt);
+    while (vpt < 8 && ceil_div(slice, vpt) > kMaxThreads) vpt *= 2;
+    const int t = (int)ceil_div(ceil_div(slice, vpt), 32) * 32;
+    pl.threads = t < 32 ? 32 : t;
+    pl.vpt = vpt;
     pl.w_spec = w_spec;
     pl.cluster = cs;
+    pl.path = cs == 1 ? ARF_PATH_ROW : ARF_PATH_CLUSTER;
     const int per_sm = caps.max_threads_per_sm / pl.threads > 0 ? caps.max_threads_per_sm / pl.threads : 1;
-    if (cs == 1) {
-        pl.path = ARF_PATH_ROW;
-        int64_t g = M < (int64_t)caps.num_sms * per_sm ? M : (int64_t)caps.num_sms * per_sm;
-        pl.grid = (int)(g > 0 ? g : 1);
-    } else {
-        pl.path = ARF_PATH_CLUSTER;
-        int64_t max_clusters = (int64_t)caps.num_sms * per_sm / cs;
-        if (max_clusters < 1) max_clusters = 1;
-        int64_t g = M < max_clusters ? M : max_clusters;
-        pl.grid = (int)((g > 0 ? g : 1) * cs);
-    }
+    int64_t max_clusters = (int64_t)caps.num_sms * per_sm / cs;
+    if (max_clusters < 1) max_clusters = 1;
+    const int64_t g = M < max_clusters ? M : max_clusters;
+    pl.grid = (int)((g > 0 ? g : 1) * cs);
     return pl;
 }
 
@@ -182,7 +171,8 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
     const int w_spec = arf::w_spec_compiled(W) ? W : 0;
     arf_plan_t pl = {};
     if (pattern == ARF_ALLREDUCE) {
-        // ~8 outstanding 16-byte loads per thread per loop trip
+        // one pass over all chunks (no grid-stride trips); about 8 loads
+        // outstanding per thread
         int u = 1;
         if (w_spec > 0) u = w_spec <= 2 ? 4 : (w_spec <= 4 ? 2 : 1);
         while (!arf::flat_unroll_compiled(w_spec, u)) u /= 2;
@@ -191,22 +181,24 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
         pl.vpt = u;
         pl.cluster = 1;
         pl.w_spec = w_spec;
-        const int64_t nchunks = M * H / 8;
-        const int64_t need = ceil_div(nchunks, (int64_t)pl.threads * u);
-        const int64_t cap = (int64_t)caps->num_sms * (caps->max_threads_per_sm / pl.threads);
-        int64_t g = need < cap ? need : cap;
-        pl.grid = (int)(g > 0 ? g : 1);
+        const int64_t need = ceil_div(M * H / 8, (int64_t)pl.threads * u);
+        pl.grid = (int)(need < 1 ? 1 : (need > INT32_MAX ? INT32_MAX : need));
     } else {
-        // Rows fewer than SMs: split each row over a cluster so that about
-        // every SM gets a CTA, keeping at least a warp's worth of chunks per CTA.
+        // One CTA per row with the fewest 16-byte chunks per thread that keep
+        // it at <= 512 threads (the kernel then keeps a whole row of loads in
+        // flight per thread, and the next row's across the row barrier, when
+        // VPT*(W+1) <= 18). Only decode-size batches of few, wide rows split a
+        // row over a cluster: one chunk per thread, 4-8 CTAs per row, so that
+        // the few rows still spread over several SMs.
         const int C = (int)(H / 8);
-        int cs = 1;
-        if (M > 0 && M < caps->num_sms && caps->max_cluster > 1) {
-            const int64_t want = ceil_div(caps->num_sms, M);
-            while (cs < want && cs < caps->max_cluster && cs < 16) cs *= 2;
-            while (cs > 1 && ceil_div(C, cs) < 32) cs /= 2;
+        int cs = 1, vpt = 1;
+        while (vpt < 8 && ceil_div(C, vpt) > kMaxThreads) vpt *= 2;
+        if (M > 0 && M < 16 && C >= 512 && caps->max_cluster > 1) {
+            vpt = 1;
+            cs = 2;
+            while (cs < 8 && cs < caps->max_cluster && (int64_t)cs * M < 32) cs *= 2;
         }
-        pl = rms_plan(*caps, w_spec, M, H, cs);
+        pl = rms_plan(*caps, w_spec, M, H, cs, vpt);
     }
     *plan_out = pl;
     return ARF_OK;
@@ -247,6 +239,10 @@ cudaError_t max_active_clusters(arf_dtype_t dt, const arf_plan_t& pl, int* n) {
     return dt == ARF_BF16 ? arf::rms_max_active_clusters_bf16(pl, n) : arf::rms_max_active_clusters_fp16(pl, n);
 }
 
+cudaError_t max_active_blocks(arf_dtype_t dt, const arf_plan_t& pl, int* n) {
+    return dt == ARF_BF16 ? arf::rms_max_active_blocks_bf16(pl, n) : arf::rms_max_active_blocks_fp16(pl, n);
+}
+
 // The planner's plan, with the cluster size lowered until the cluster kernel
 // instance can actually be made resident on this device. During stream
 // capture no occupancy query is made: the plan then rests on the cluster
@@ -268,11 +264,23 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
     while (!capturing && pl.path == ARF_PATH_CLUSTER) {
         int n = 0;
         cudaError_t e = max_active_clusters(dtype, pl, &n);
-        if (e == cudaSuccess && n > 0) break;
+        if (e == cudaSuccess && n > 0) {
+            // no more clusters than can be resident at once (rows loop)
+            if ((int64_t)n * pl.cluster < pl.grid) pl.grid = n * pl.cluster;
+            break;
+        }
         (void)cudaGetLastError();
-        const int cs = pl.cluster / 2;
-        const int w_spec = pl.w_spec;
-        pl = rms_plan(ws->caps, w_spec, M, H, cs);
+        pl = rms_plan(ws->caps, pl.w_spec, M, H, pl.cluster / 2, pl.vpt);
+    }
+    if (!capturing && pl.path == ARF_PATH_ROW) {
+        int b = 0;
+        cudaError_t e = max_active_blocks(dtype, pl, &b);
+        if (e == cudaSuccess && b > 0) {
+            const int64_t cap = (int64_t)ws->caps.num_sms * b;
+            if (cap < pl.grid) pl.grid = (int)cap;
+        } else {
+            (void)cudaGetLastError();
+        }
     }
     if (ws->log)
         std::fprintf(stderr, "[arf] plan %s W=%d M=%lld H=%lld %s: path=%s threads=%d vpt=%d cluster=%d grid=%d w_spec=%d\n",
@@ -322,20 +330,32 @@ arf_status_t check_device(arf_workspace_t ws, cudaStream_t stream, bool* capturi
     return ARF_OK;
 }
 
+void fill_common(arf::LaunchCommon& lc, const void* const* partials, int W, bool by_value, bool pdl) {
+    if (by_value) {
+        for (int r = 0; r < W; ++r) lc.ptrs[r] = partials[r];
+        lc.partials = nullptr;
+    } else {
+        lc.partials = partials;
+    }
+    lc.by_value = by_value ? 1 : 0;
+    lc.pdl = pdl ? 1 : 0;
+}
+
 arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t pattern, int W,
-                    const void* const* partials, const void* residual, const void* gamma, float eps, void* out,
-                    void* residual_out, int64_t M, int64_t H, arf_dtype_t dtype, cudaStream_t stream) {
+                    const void* const* partials, bool by_value, bool pdl, const void* residual, const void* gamma,
+                    float eps, void* out, void* residual_out, int64_t M, int64_t H, arf_dtype_t dtype,
+                    cudaStream_t stream) {
     cudaError_t e;
     if (pattern == ARF_ALLREDUCE) {
         arf::FlatParams p = {};
-        p.partials = partials;
+        fill_common(p.lc, partials, W, by_value, pdl);
         p.out = static_cast<uint4*>(out);
         p.nchunks = M * H / 8;
         p.W = W;
         e = dtype == ARF_BF16 ? arf::launch_flat_bf16(p, pl, stream) : arf::launch_flat_fp16(p, pl, stream);
     } else {
         arf::RmsParams p = {};
-        p.partials = partials;
+        fill_common(p.lc, partials, W, by_value, pdl);
         p.residual = static_cast<const uint4*>(residual);
         p.gamma = static_cast<const uint4*>(gamma);
         p.out = static_cast<uint4*>(out);
@@ -353,10 +373,13 @@ arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t patt
     return ARF_OK;
 }
 
-arf_status_t run_impl(arf_workspace_t ws, const arf_plan_t* forced, arf_pattern_t pattern, int W,
+arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_pattern_t pattern, int W,
                       const void* const* partials, const void* residual, const void* gamma, float eps, void* out,
                       void* residual_out, int64_t M, int64_t H, arf_dtype_t dtype, void* stream_v) {
     if (!ws) return ARF_ERR_INVALID_ARG;
+    const arf_plan_t* forced = opts ? opts->plan : nullptr;
+    const bool by_value = opts && opts->partials_by_value;
+    const bool pdl = opts && opts->pdl;
     arf_status_t st = arf_supports(ws, pattern, W, M, H, dtype);
     if (st != ARF_OK) return st;
     if (forced) {
@@ -366,6 +389,10 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_plan_t* forced, arf_pattern_
     if (M == 0) return ARF_OK;
     st = check_call(ws, pattern, partials, residual, gamma, eps, out, residual_out);
     if (st != ARF_OK) return st;
+    if (by_value) {
+        for (int r = 0; r < W; ++r)
+            if (!partials[r]) return ARF_ERR_INVALID_ARG;
+    }
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
     bool capturing = false;
     st = check_device(ws, stream, &capturing);
@@ -384,7 +411,8 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_plan_t* forced, arf_pattern_
         st = device_plan(ws, pattern, W, M, H, dtype, &pl, capturing);
         if (st != ARF_OK) return st;
     }
-    return launch(ws, pl, pattern, W, partials, residual, gamma, eps, out, residual_out, M, H, dtype, stream);
+    return launch(ws, pl, pattern, W, partials, by_value, pdl, residual, gamma, eps, out, residual_out, M, H, dtype,
+                  stream);
 }
 
 }  // namespace
@@ -408,12 +436,21 @@ extern "C" arf_status_t arf_run(arf_workspace_t ws, arf_pattern_t pattern, int W
                     stream);
 }
 
+extern "C" arf_status_t arf_run_ex(arf_workspace_t ws, const arf_run_opts_t* opts, arf_pattern_t pattern, int W,
+                                   const void* const* partials, const void* residual, const void* gamma, float eps,
+                                   void* out, void* residual_out, int64_t M, int64_t H, arf_dtype_t dtype,
+                                   void* stream) {
+    return run_impl(ws, opts, pattern, W, partials, residual, gamma, eps, out, residual_out, M, H, dtype, stream);
+}
+
 extern "C" arf_status_t arf_run_planned(arf_workspace_t ws, const arf_plan_t* plan, arf_pattern_t pattern, int W,
                                         const void* const* partials_dev, const void* residual, const void* gamma,
                                         float eps, void* out, void* residual_out, int64_t M, int64_t H,
                                         arf_dtype_t dtype, void* stream) {
     if (!plan) return ARF_ERR_INVALID_ARG;
-    return run_impl(ws, plan, pattern, W, partials_dev, residual, gamma, eps, out, residual_out, M, H, dtype,
+    arf_run_opts_t opts = {};
+    opts.plan = plan;
+    return run_impl(ws, &opts, pattern, W, partials_dev, residual, gamma, eps, out, residual_out, M, H, dtype,
                     stream);
 }
 

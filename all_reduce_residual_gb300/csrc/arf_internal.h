@@ -22,15 +22,23 @@ constexpr bool flat_unroll_compiled(int ws, int u) {
 // Chunks per thread compiled for the RMS kernel.
 constexpr bool rms_vpt_compiled(int vpt) { return vpt == 1 || vpt == 2 || vpt == 4 || vpt == 8; }
 
+// How a kernel finds the W partial pointers and when it may start.
+struct LaunchCommon {
+    const void* const* partials;    // device array of W device pointers, or
+    const void* ptrs[ARF_MAX_W];    // the pointers themselves (by_value)
+    int by_value;                   // 1: read ptrs[] from the launch parameters
+    int pdl;                        // 1: launched as a programmatic dependent
+};
+
 struct FlatParams {
-    const void* const* partials;  // device array of W device pointers
+    LaunchCommon lc;
     uint4* out;
     int64_t nchunks;              // M*H/8
     int W;
 };
 
 struct RmsParams {
-    const void* const* partials;  // device array of W device pointers
+    LaunchCommon lc;
     const uint4* residual;
     const uint4* gamma;
     uint4* out;
@@ -60,6 +68,9 @@ cudaError_t allow_large_clusters_fp16();
 // kernel instance of `plan` can keep resident at once (0 = cannot launch).
 cudaError_t rms_max_active_clusters_bf16(const arf_plan_t& plan, int* n);
 cudaError_t rms_max_active_clusters_fp16(const arf_plan_t& plan, int* n);
+// How many CTAs of the RMS kernel instance of `plan` one SM can hold.
+cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int* n);
+cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int* n);
 
 // Record a CUDA error as the workspace's last one (arf_last_cuda_error).
 void note_cuda_error(arf_workspace_t ws, cudaError_t e);

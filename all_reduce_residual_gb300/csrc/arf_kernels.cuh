@@ -152,9 +152,26 @@ __device__ __forceinline__ void rank_sum(float acc[8], const uint4* const* s_ptr
     }
 }
 
-// Copy the W partial pointers of the device pointer array to shared memory.
-__device__ __forceinline__ void load_pointers(const uint4** s_ptr, const void* const* partials, int W) {
-    for (int i = threadIdx.x; i < W; i += blockDim.x) s_ptr[i] = static_cast<const uint4*>(partials[i]);
+// Kernel prologue. As a programmatic dependent launch (lc.pdl), first let
+// the next kernel in the stream begin launching, then wait until every
+// earlier kernel has completed and its writes are visible: no global memory
+// is touched before that wait, so the kernel is correct after any
+// predecessor. Then copy the W partial pointers to shared memory, from the
+// device pointer array or (by_value) from the launch parameters.
+__device__ __forceinline__ void prologue(const uint4** s_ptr, const LaunchCommon& lc, int W) {
+    if (lc.pdl) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+    if (lc.by_value) {
+        if (threadIdx.x == 0) {
+#pragma unroll
+            for (int i = 0; i < ARF_MAX_W; ++i)
+                if (i < W) s_ptr[i] = static_cast<const uint4*>(lc.ptrs[i]);
+        }
+    } else {
+        for (int i = threadIdx.x; i < W; i += blockDim.x) s_ptr[i] = static_cast<const uint4*>(lc.partials[i]);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -163,7 +180,7 @@ __device__ __forceinline__ void load_pointers(const uint4** s_ptr, const void* c
 template <typename T, int WS, int U>
 __global__ void __launch_bounds__(kMaxThreads) ar_flat_kernel(FlatParams p) {
     __shared__ const uint4* s_ptr[ARF_MAX_W];
-    load_pointers(s_ptr, p.partials, p.W);
+    prologue(s_ptr, p.lc, p.W);
     __syncthreads();
 
     const int64_t nthr = blockDim.x;
@@ -213,14 +230,100 @@ __global__ void __launch_bounds__(kMaxThreads) ar_flat_kernel(FlatParams p) {
 // launched without a cluster); CTA q of the cluster owns chunks
 // [q*slice, min(C, (q+1)*slice)) of the row, and thread t of it the chunks
 // q*slice + t + k*blockDim.x for k < VPT.
+//
+// Bytes in flight: with W known at compile time and VPT*(W+1) <= 18, a
+// thread issues the loads of all its chunks of a row at once (one HBM round
+// trip per row), and issues the next row's loads before the row's
+// reduction barrier, so HBM stays busy while the CTA reduces and normalises.
 // ---------------------------------------------------------------------------
+template <int WS, int VPT>
+struct RmsShape {
+    static constexpr bool kPrefetch = WS > 0 && VPT * (WS + 1) <= 18;
+    static constexpr bool kGammaRegs = VPT <= 2;  // else gamma is re-read from L1 per row
+};
+
+// Issue every load of one row for this thread: L[k][0..WS-1] = partials,
+// L[k][WS] = residual. volatile keeps them where they are written (before
+// the reduction barrier), which is the point of prefetching.
+template <int WS, int VPT>
+__device__ __forceinline__ void issue_row(uint4 (&L)[VPT][WS + 1], const uint4* const* s_ptr,
+                                          const uint4* residual, int64_t rbase, int c0, int c1) {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int c = c0 + threadIdx.x + k * blockDim.x;
+        if (c < c1) {
+            const uint4* rp = residual + rbase + c;
+            asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(L[k][WS].x), "=r"(L[k][WS].y), "=r"(L[k][WS].z), "=r"(L[k][WS].w)
+                         : "l"(rp));
+#pragma unroll
+            for (int r = 0; r < WS; ++r) {
+                const uint4* pp = s_ptr[r] + rbase + c;
+                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(L[k][r].x), "=r"(L[k][r].y), "=r"(L[k][r].z), "=r"(L[k][r].w)
+                             : "l"(pp));
+            }
+        }
+    }
+}
+
+// Row statistic: butterfly in the warp, warps in index order, then (cluster)
+// CTAs in rank order; every thread of every CTA of the cluster ends with the
+// same value. Shared slots alternate with the row parity `it`.
+__device__ __forceinline__ float row_sum_squares(float ss, float (*s_warp)[kMaxThreads / 32], float* s_cta,
+                                                 int cs, int it) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) s_warp[it & 1][warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w = 0; w < nwarps; ++w) tot += s_warp[it & 1][w];
+    if (cs > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        if (threadIdx.x == 0) s_cta[it & 1] = tot;
+        cluster.sync();
+        tot = 0.0f;
+        for (int r = 0; r < cs; ++r) tot += *cluster.map_shared_rank(&s_cta[it & 1], r);
+    }
+    return tot;
+}
+
+// One chunk: t = sum_r P_r + residual (binary32, rank order, one rounding),
+// store residual_out, return the rounded value, accumulate its squares.
+template <typename T>
+__device__ __forceinline__ uint4 residual_chunk(float acc[8], const uint4& rv, uint4* dst, float& ss) {
+    float r[8];
+    Pack8<T>::widen(rv, r);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], r[e]);
+    const uint4 xs = Pack8<T>::narrow(acc);
+    st_out(dst, xs);
+    float x[8];
+    Pack8<T>::widen(xs, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+    return xs;
+}
+
+template <typename T>
+__device__ __forceinline__ void normalise_chunk(const uint4& xs, const uint4& gv, float inv, uint4* dst) {
+    float x[8], gg[8], y[8];
+    Pack8<T>::widen(xs, x);
+    Pack8<T>::widen(gv, gg);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(x[e], inv), gg[e]);
+    st_out(dst, Pack8<T>::narrow(y));
+}
+
 template <typename T, int WS, int VPT>
 __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
+    using Shape = RmsShape<WS, VPT>;
     __shared__ const uint4* s_ptr[ARF_MAX_W];
     __shared__ float s_warp[2][kMaxThreads / 32];  // per-warp partial sums, by row parity
     __shared__ float s_cta[2];                     // this CTA's partial, read by its peers
 
-    load_pointers(s_ptr, p.partials, p.W);
+    prologue(s_ptr, p.lc, p.W);
 
     const int cs = p.cs;
     const int q = cs > 1 ? (int)cg::this_cluster().block_rank() : 0;
@@ -228,69 +331,77 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
     const int64_t nclusters = gridDim.x / cs;
     const int c0 = q * p.slice;
     const int c1 = min(p.C, c0 + p.slice);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 
-    // gamma: the same chunks for every row this thread touches
-    uint4 g[VPT];
+    uint4 g[Shape::kGammaRegs ? VPT : 1];
+    if constexpr (Shape::kGammaRegs) {
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int c = c0 + threadIdx.x + k * blockDim.x;
-        if (c < c1) g[k] = ld_keep(p.gamma + c);
+        for (int k = 0; k < VPT; ++k) {
+            const int c = c0 + threadIdx.x + k * blockDim.x;
+            if (c < c1) g[k] = ld_keep(p.gamma + c);
+        }
     }
     __syncthreads();
 
-    int it = 0;
-    for (int64_t row = cluster_id; row < p.M; row += nclusters, ++it) {
-        const int64_t rbase = row * (int64_t)p.C;
-        uint4 xs[VPT];  // rounded residual_out, kept for the normalisation pass
-        float ss = 0.0f;
+    if constexpr (Shape::kPrefetch) {
+        uint4 L[VPT][WS + 1];
+        int64_t row = cluster_id;
+        if (row < p.M) issue_row<WS, VPT>(L, s_ptr, p.residual, row * (int64_t)p.C, c0, c1);
+        for (int it = 0; row < p.M; row += nclusters, ++it) {
+            const int64_t rbase = row * (int64_t)p.C;
+            uint4 xs[VPT];
+            float ss = 0.0f;
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int c = c0 + threadIdx.x + k * blockDim.x;
-            if (c < c1) {
-                float acc[8];
-                const uint4 rv = ld_resid(p.residual + rbase + c);
-                rank_sum<T, WS>(acc, s_ptr, p.W, rbase + c);
-                float r[8];
-                Pack8<T>::widen(rv, r);
+            for (int k = 0; k < VPT; ++k) {
+                const int c = c0 + threadIdx.x + k * blockDim.x;
+                if (c < c1) {
+                    float acc[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], r[e]);
-                xs[k] = Pack8<T>::narrow(acc);
-                st_out(p.residual_out + rbase + c, xs[k]);
-                float x[8];
-                Pack8<T>::widen(xs[k], x);
+                    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+                    for (int r = 0; r < WS; ++r) accumulate<T>(acc, L[k][r]);
+                    xs[k] = residual_chunk<T>(acc, L[k][WS], p.residual_out + rbase + c, ss);
+                }
+            }
+            const int64_t next = row + nclusters;
+            if (next < p.M) issue_row<WS, VPT>(L, s_ptr, p.residual, next * (int64_t)p.C, c0, c1);
+            const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, it) / (float)p.H + p.eps);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int c = c0 + threadIdx.x + k * blockDim.x;
+                if (c < c1) {
+                    uint4 gv;
+                    if constexpr (Shape::kGammaRegs) gv = g[k];
+                    else gv = ld_keep(p.gamma + c);
+                    normalise_chunk<T>(xs[k], gv, inv, p.out + rbase + c);
+                }
             }
         }
-
-        // row sum of squares: butterfly in the warp, warps in index order,
-        // then (cluster) CTAs in rank order; every thread ends with the same value
+    } else {
+        int it = 0;
+        for (int64_t row = cluster_id; row < p.M; row += nclusters, ++it) {
+            const int64_t rbase = row * (int64_t)p.C;
+            uint4 xs[VPT];
+            float ss = 0.0f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) s_warp[it & 1][warp] = ss;
-        __syncthreads();
-        float tot = 0.0f;
-        for (int w = 0; w < nwarps; ++w) tot += s_warp[it & 1][w];
-        if (cs > 1) {
-            cg::cluster_group cluster = cg::this_cluster();
-            if (threadIdx.x == 0) s_cta[it & 1] = tot;
-            cluster.sync();
-            tot = 0.0f;
-            for (int r = 0; r < cs; ++r) tot += *cluster.map_shared_rank(&s_cta[it & 1], r);
-        }
-        const float inv = rsqrtf(tot / (float)p.H + p.eps);
-
+            for (int k = 0; k < VPT; ++k) {
+                const int c = c0 + threadIdx.x + k * blockDim.x;
+                if (c < c1) {
+                    float acc[8];
+                    const uint4 rv = ld_resid(p.residual + rbase + c);
+                    rank_sum<T, WS>(acc, s_ptr, p.W, rbase + c);
+                    xs[k] = residual_chunk<T>(acc, rv, p.residual_out + rbase + c, ss);
+                }
+            }
+            const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, it) / (float)p.H + p.eps);
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int c = c0 + threadIdx.x + k * blockDim.x;
-            if (c < c1) {
-                float x[8], gg[8], y[8];
-                Pack8<T>::widen(xs[k], x);
-                Pack8<T>::widen(g[k], gg);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(x[e], inv), gg[e]);
-                st_out(p.out + rbase + c, Pack8<T>::narrow(y));
+            for (int k = 0; k < VPT; ++k) {
+                const int c = c0 + threadIdx.x + k * blockDim.x;
+                if (c < c1) {
+                    uint4 gv;
+                    if constexpr (Shape::kGammaRegs) gv = g[k];
+                    else gv = ld_keep(p.gamma + c);
+                    normalise_chunk<T>(xs[k], gv, inv, p.out + rbase + c);
+                }
             }
         }
     }

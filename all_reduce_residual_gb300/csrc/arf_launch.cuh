@@ -60,10 +60,17 @@ template <typename T>
 cudaError_t launch_flat_t(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s) {
     FlatFn fn = flat_kernel_for<T>(plan.w_spec, plan.vpt);
     if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.grid);
     cfg.blockDim = dim3((unsigned)plan.threads);
     cfg.stream = s;
+    if (p.lc.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
@@ -71,19 +78,26 @@ template <typename T>
 cudaError_t launch_rms_t(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s) {
     RmsFn fn = rms_kernel_for<T>(plan.w_spec, plan.vpt);
     if (!fn) return cudaErrorInvalidValue;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.grid);
     cfg.blockDim = dim3((unsigned)plan.threads);
     cfg.stream = s;
+    unsigned n = 0;
     if (plan.cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)plan.cluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)plan.cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
     }
+    if (p.lc.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
@@ -115,6 +129,13 @@ cudaError_t rms_max_active_clusters_t(const arf_plan_t& plan, int* n) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaOccupancyMaxActiveClusters(n, fn, &cfg);
+}
+
+template <typename T>
+cudaError_t rms_max_active_blocks_t(const arf_plan_t& plan, int* n) {
+    RmsFn fn = rms_kernel_for<T>(plan.w_spec, plan.vpt);
+    if (!fn) return cudaErrorInvalidValue;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fn, plan.threads, 0);
 }
 
 }  // namespace arf

@@ -14,4 +14,8 @@ cudaError_t rms_max_active_clusters_bf16(const arf_plan_t& plan, int* n) {
     return rms_max_active_clusters_t<__nv_bfloat16>(plan, n);
 }
 
+cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int* n) {
+    return rms_max_active_blocks_t<__nv_bfloat16>(plan, n);
+}
+
 }  // namespace arf

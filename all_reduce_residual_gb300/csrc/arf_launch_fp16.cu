@@ -14,4 +14,8 @@ cudaError_t rms_max_active_clusters_fp16(const arf_plan_t& plan, int* n) {
     return rms_max_active_clusters_t<__half>(plan, n);
 }
 
+cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int* n) {
+    return rms_max_active_blocks_t<__half>(plan, n);
+}
+
 }  // namespace arf

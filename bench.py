@@ -258,7 +258,7 @@ def run_arf(args):
                    "parallelism": f"replicas x{world}",
                    "plans": {p: ws.plan(p, w.W, w.M, w.H, torch.bfloat16 if w.dtype == "bf16"
                                         else torch.float16).as_dict() for p in pats}},
-        "us_per_call": {p: round(statistics.median(v) * 1e3, 3) for p, v in per_call.items()},
+        "us_per_call": {p: round(statistics.mean(v) * 1e3, 3) for p, v in per_call.items()},
         "roofline": roofline,
         "gpu_launches": len(pats) * K,
         "clocks": clk.summary(),
@@ -323,9 +323,13 @@ def e2e_leg(ws, w, inp, pats, flush, dev, K, world):
 
 
 def sweep(ws, dev, flush, peak):
-    """µs/call and GB/s for every workload, pattern and (k3_tp8) M: cold
-    (L2 flushed before each call, median of 50 CUDA-event timings) and warm
-    (a CUDA graph of 20 back-to-back calls, per-call mean over 5 replays)."""
+    """µs/call and GB/s for every workload, pattern and (k3_tp8) M, through
+    arf_run and through arf_run_ex with partials by value + PDL: cold
+    (L2 flushed before each call, mean of 50 CUDA-event timings: the event
+    clock ticks in steps of about 2 µs here, and the mean of many samples
+    taken at random phases is unbiased where a median is not) and warm (a
+    CUDA graph of 20 back-to-back calls, per-call time of the fastest of 5
+    replays)."""
     import torch
 
     import all_reduce_residual_gb300 as arf
@@ -342,45 +346,55 @@ def sweep(ws, dev, flush, peak):
             ptrs = arf.pointer_array(P, dev)
             out, ro = torch.empty_like(R), torch.empty_like(R)
             for pat in w.patterns:
-                def call():
+                def call(opt=False):
                     arf.run(ws, pat, P, R, G, w.eps, out=out, residual_out=ro if pat == "rmsnorm" else None,
-                            ptrs=ptrs)
-                for _ in range(10):
-                    call()
-                cold = []
-                for _ in range(50):
-                    flush.zero_()
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    call()
-                    b.record(stream)
-                    b.synchronize()
-                    cold.append(a.elapsed_time(b) * 1e3)
-                g = torch.cuda.CUDAGraph()
-                s = torch.cuda.Stream(dev)
-                s.wait_stream(stream)
-                with torch.cuda.stream(s):
-                    with torch.cuda.graph(g, stream=s):
-                        for _ in range(20):
-                            call()
-                stream.wait_stream(s)
-                torch.cuda.synchronize()
-                warm = []
-                for _ in range(5):
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    g.replay()
-                    b.record(stream)
-                    b.synchronize()
-                    warm.append(a.elapsed_time(b) * 1e3 / 20)
-                us = statistics.median(cold)
+                            ptrs=ptrs, by_value=opt, pdl=opt)
+
+                def cold_us(opt):
+                    for _ in range(10):
+                        call(opt)
+                    ts = []
+                    for _ in range(50):
+                        flush.zero_()
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record(stream)
+                        call(opt)
+                        b.record(stream)
+                        b.synchronize()
+                        ts.append(a.elapsed_time(b) * 1e3)
+                    return statistics.mean(ts)
+
+                def warm_us(opt):
+                    g = torch.cuda.CUDAGraph()
+                    s = torch.cuda.Stream(dev)
+                    s.wait_stream(stream)
+                    with torch.cuda.stream(s):
+                        with torch.cuda.graph(g, stream=s):
+                            for _ in range(20):
+                                call(opt)
+                    stream.wait_stream(s)
+                    torch.cuda.synchronize()
+                    best = None
+                    for _ in range(5):
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record(stream)
+                        g.replay()
+                        b.record(stream)
+                        b.synchronize()
+                        t = a.elapsed_time(b) * 1e3 / 20
+                        best = t if best is None else min(best, t)
+                    del g
+                    return best
+
+                us, us_opt = cold_us(False), cold_us(True)
+                warm, warm_opt = warm_us(False), warm_us(True)
                 nbytes = ww.bytes_per_call(pat)
                 plan = ws.plan(pat, w.W, M, w.H, torch.bfloat16 if w.dtype == "bf16" else torch.float16)
                 rows.append({"workload": name, "W": w.W, "M": M, "H": w.H, "dtype": w.dtype, "pattern": pat,
-                             "bytes": nbytes, "us_cold": round(us, 3), "us_warm_graph": round(min(warm), 3),
+                             "bytes": nbytes, "us_cold": round(us, 3), "us_warm_graph": round(warm, 3),
                              "gbs_cold": round(nbytes / us / 1e3, 1), "frac_cold": round(nbytes / us / 1e3 / peak, 4),
+                             "us_cold_byvalue_pdl": round(us_opt, 3), "us_warm_graph_byvalue_pdl": round(warm_opt, 3),
                              "plan": [plan.path, plan.threads, plan.vpt, plan.cluster, plan.grid, plan.w_spec]})
-                del g
             del inp, P, R, G, out, ro, ptrs
             torch.cuda.empty_cache()
     return rows

@@ -204,6 +204,36 @@ arf_status_t arf_run_planned(arf_workspace_t ws, const arf_plan_t* plan,
                              void* out, void* residual_out,
                              int64_t M, int64_t H, arf_dtype_t dtype, void* stream);
 
+/* Per-call options of arf_run_ex. Zero-initialise, then set what is needed
+ * (all zero = arf_run). */
+typedef struct arf_run_opts {
+    const arf_plan_t* plan;  /* NULL: the planner's plan; else an explicit plan,
+                                checked as by arf_run_planned */
+    int partials_by_value;   /* 0: `partials` is a DEVICE array of W device
+                                pointers (as arf_run). 1: `partials` is a HOST
+                                array of W device pointers; the values are
+                                copied into the kernel launch, so the kernel
+                                reads no pointer array (one dependent memory
+                                round trip less); a captured graph keeps the
+                                values, and the host array may be reused as
+                                soon as the call returns. */
+    int pdl;                 /* 1: launch as a programmatic dependent launch:
+                                the kernel may be scheduled while the previous
+                                kernel in the stream still runs, and waits
+                                (griddepcontrol.wait) for it to complete before
+                                it touches any memory, so results are the same;
+                                what overlaps is launch latency. */
+} arf_run_opts_t;
+
+/* arf_run with per-call options (NULL opts = arf_run). Same semantics,
+ * results contract and errors; with partials_by_value, `partials` must point
+ * to W readable host pointers (INVALID_ARG if any is NULL). */
+arf_status_t arf_run_ex(arf_workspace_t ws, const arf_run_opts_t* opts,
+                        arf_pattern_t pattern, int W, const void* const* partials,
+                        const void* residual, const void* gamma, float eps,
+                        void* out, void* residual_out,
+                        int64_t M, int64_t H, arf_dtype_t dtype, void* stream);
+
 /* ---- host buffers ------------------------------------------------------ */
 
 /* Bytes of device staging that arf_run_host needs for these sizes. */

@@ -84,26 +84,33 @@ def test_planner_plans_are_legal(pattern, W, M, H):
         per_sm = caps.max_threads_per_sm // p.threads
         if pattern == arf.ARF_ALLREDUCE:
             assert p.path == arf.ARF_PATH_FLAT and p.cluster == 1
-            assert p.grid <= caps.num_sms * per_sm
+            chunks = M * H // 8
+            assert p.grid == max(1, -(-chunks // (p.threads * p.vpt)))  # one pass, no grid-stride trips
         else:
             C = H // 8
             assert p.threads * p.vpt * p.cluster >= C
             if p.path == arf.ARF_PATH_CLUSTER:
-                assert M < caps.num_sms and 2 <= p.cluster <= caps.max_cluster
+                # only decode-size batches of few, wide rows split a row
+                assert M < 16 and C >= 512 and p.vpt == 1
+                assert 2 <= p.cluster <= min(8, caps.max_cluster)
                 assert p.grid == p.cluster * min(M, max(1, caps.num_sms * per_sm // p.cluster))
             else:
                 assert p.cluster == 1 and p.grid == max(1, min(M, caps.num_sms * per_sm))
 
 
 def test_planner_uses_the_sm_count():
-    """Small-M rows spread over about every SM; large M fills the device."""
+    """Few wide rows spread over several SMs; large M fills the device."""
     p = arf.Plan()
     arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 1, 7168, arf.ARF_BF16, p)
-    assert p.path == arf.ARF_PATH_CLUSTER and p.cluster == 16
+    assert p.path == arf.ARF_PATH_CLUSTER and p.cluster == 8 and p.threads == 128
+    arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 128, 7168, arf.ARF_BF16, p)
+    assert p.path == arf.ARF_PATH_ROW and (p.threads, p.vpt, p.grid) == (448, 2, 128)
     arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 2048, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and p.grid % 152 == 0
-    arf.arf_plan_for_caps(GB300, arf.ARF_ALLREDUCE, 4, 5851, 7168, arf.ARF_BF16, p)
-    assert p.grid % 152 == 0
+    arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 4, 5851, 7168, arf.ARF_BF16, p)
+    assert p.path == arf.ARF_PATH_ROW and p.vpt * (4 + 1) <= 18 and p.grid % 152 == 0
+    arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7168, arf.ARF_BF16, p)
+    assert p.path == arf.ARF_PATH_ROW and (p.threads, p.vpt) == (448, 2)  # 896 chunks > 512 threads
     no_cluster = arf.DeviceCaps(152, 1, 2048)
     arf.arf_plan_for_caps(no_cluster, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 1, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and p.grid == 1

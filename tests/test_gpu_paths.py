@@ -358,3 +358,80 @@ def test_host_buffer_entry_point(ws, name, pattern, pinned):
         torch.cuda.synchronize()
         got = (wl.codes(out), wl.codes(ro) if pattern == RMS else None)
         assert_parity(DT[w.dtype], pattern, got, oracle_run(pattern, inp))
+
+
+@pytest.mark.parametrize("by_value,pdl", [(True, False), (False, True), (True, True)])
+@pytest.mark.parametrize("W,M,H", [(8, 1, 7168), (2, 128, 4096), (8, 300, 7168), (17, 5, 264)])
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_run_ex_options(ws, pattern, W, M, H, by_value, pdl):
+    """Partials passed by value and/or a programmatic dependent launch give
+    exactly the results of arf_run (same plan), and match the oracle."""
+    inp = inputs(W, M, H)
+    P, R, G = to_device(inp)
+    base = gpu_run(ws, pattern, P, R, G, 1e-6)
+    out, ro = arf.run(ws, pattern, P, R, G, 1e-6, by_value=by_value, pdl=pdl)
+    torch.cuda.synchronize()
+    got = (wl.codes(out.cpu()), wl.codes(ro.cpu()) if pattern == RMS else None)
+    assert np.array_equal(got[0], base[0])
+    if pattern == RMS:
+        assert np.array_equal(got[1], base[1])
+    assert_parity(oracle.BF16, pattern, got, oracle_run(pattern, inp))
+
+
+def test_pdl_dependent_chain(ws):
+    """A chain where every call reads the previous call's output: with
+    programmatic dependent launches each kernel still waits for its
+    predecessor's writes. Checked against the same chain without PDL."""
+    M, H = 256, 4096
+    a = torch.randn((M, H), device="cuda").to(torch.bfloat16)
+    b = torch.randn((M, H), device="cuda").to(torch.bfloat16) * 0.01
+    G = torch.ones((H,), device="cuda", dtype=torch.bfloat16)
+
+    def chain(pdl, by_value):
+        x = a.clone()
+        outs = []
+        for k in range(12):
+            if k % 2 == 0:
+                y, _ = arf.run(ws, AR, [x, b], pdl=pdl, by_value=by_value)
+            else:
+                y, _ = arf.run(ws, RMS, [x, b], b, G, 1e-6, pdl=pdl, by_value=by_value)
+            outs.append(y)
+            x = y
+        torch.cuda.synchronize()
+        return [wl.codes(o.cpu()) for o in outs]
+
+    ref = chain(False, False)
+    for pdl, by_value in ((True, False), (True, True)):
+        for _ in range(3):
+            got = chain(pdl, by_value)
+            for k, (g_, r_) in enumerate(zip(got, ref)):
+                assert np.array_equal(g_, r_), f"step {k} differs (pdl={pdl}, by_value={by_value})"
+
+
+def test_pdl_by_value_graph_replay(ws):
+    W, M, H = 4, 64, 4096
+    inp = inputs(W, M, H, cid=930)
+    P, R, G = to_device(inp)
+    out, ro = torch.empty_like(R), torch.empty_like(R)
+    arf.run(ws, RMS, P, R, G, 1e-6, out=out, residual_out=ro, pdl=True, by_value=True)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            arf.run(ws, RMS, P, R, G, 1e-6, out=out, residual_out=ro, pdl=True, by_value=True)
+    for k in range(2):
+        new = inputs(W, M, H, cid=940 + k)
+        for dst, src in zip(P + [R, G], new.partials + [new.residual, new.gamma]):
+            dst.copy_(src)
+        g.replay()
+        torch.cuda.synchronize()
+        assert_parity(oracle.BF16, RMS, (wl.codes(out.cpu()), wl.codes(ro.cpu())), oracle_run(RMS, new))
+
+
+def test_run_ex_rejects_null_by_value_pointer(ws):
+    R = torch.zeros((2, 64), device="cuda", dtype=torch.bfloat16)
+    opts = arf.RunOpts(plan=None, partials_by_value=1, pdl=0)
+    st = arf.arf_run_ex(ws.handle, opts, AR, 2, [R.data_ptr(), 0], None, None, 0.0, R.data_ptr(), None, 2, 64,
+                        arf.ARF_BF16, torch.cuda.current_stream().cuda_stream)
+    assert st == arf.ARF_ERR_INVALID_ARG
