@@ -30,6 +30,7 @@ ARF_FP16 = 1
 ARF_PATH_FLAT = 0
 ARF_PATH_ROW = 1
 ARF_PATH_CLUSTER = 2
+ARF_PATH_ASYNC = 3
 ARF_MAX_W = 64
 ARF_MAX_H = 32768
 ARF_STATIC_STAGING_BYTES = 16 << 20
@@ -39,16 +40,18 @@ STATUS_NAMES = {0: "ARF_OK", 1: "ARF_ERR_INVALID_ARG", 2: "ARF_ERR_UNSUPPORTED",
 
 
 class DeviceCaps(ctypes.Structure):
-    _fields_ = [("num_sms", ctypes.c_int), ("max_cluster", ctypes.c_int), ("max_threads_per_sm", ctypes.c_int)]
+    _fields_ = [("num_sms", ctypes.c_int), ("max_cluster", ctypes.c_int), ("max_threads_per_sm", ctypes.c_int),
+                ("max_smem_per_block", ctypes.c_int)]
 
     def __repr__(self):
         return f"DeviceCaps(num_sms={self.num_sms}, max_cluster={self.max_cluster}, " \
-               f"max_threads_per_sm={self.max_threads_per_sm})"
+               f"max_threads_per_sm={self.max_threads_per_sm}, max_smem_per_block={self.max_smem_per_block})"
 
 
 class Plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("threads", ctypes.c_int), ("vpt", ctypes.c_int),
-                ("cluster", ctypes.c_int), ("grid", ctypes.c_int), ("w_spec", ctypes.c_int)]
+                ("cluster", ctypes.c_int), ("grid", ctypes.c_int), ("w_spec", ctypes.c_int),
+                ("stages", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

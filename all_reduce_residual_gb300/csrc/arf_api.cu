@@ -36,6 +36,30 @@ arf_status_t cuda_fail(arf_workspace_t ws, cudaError_t e) {
     return ARF_ERR_CUDA;
 }
 
+// Ring depth of the streaming kernel that fits in one CTA's shared memory
+// next to a row of rounded residual_out (0 when it does not apply).
+int async_stages(const arf_device_caps_t& caps, int w_spec, int64_t H) {
+    if (w_spec == 0) return 0;
+    const int64_t C = H / 8;
+    const int64_t avail = (int64_t)caps.max_smem_per_block - arf::kAsyncStaticSmem - C * 16;
+    const int64_t per = (int64_t)(w_spec + 1) * arf::kAsyncCtaThreads * 16;
+    const int64_t st = avail > 0 ? avail / per : 0;
+    return st < 2 ? 0 : (int)(st > 8 ? 8 : st);
+}
+
+arf_plan_t async_plan(const arf_device_caps_t& caps, int w_spec, int64_t M, int stages) {
+    arf_plan_t pl = {};
+    pl.path = ARF_PATH_ASYNC;
+    pl.threads = arf::kAsyncCtaThreads;
+    pl.vpt = 1;
+    pl.cluster = 1;
+    pl.w_spec = w_spec;
+    pl.stages = stages;
+    const int64_t g = M < caps.num_sms ? M : caps.num_sms;
+    pl.grid = (int)(g > 0 ? g : 1);
+    return pl;
+}
+
 // The RMS plan for a given cluster size and chunks-per-thread count: threads
 // cover the CTA's slice in whole warps; grid = rows (clusters) up to what the
 // SMs can hold by thread count (the workspace refines this by occupancy).
@@ -60,7 +84,7 @@ arf_plan_t rms_plan(const arf_device_caps_t& caps, int w_spec, int64_t M, int64_
 
 const char* pattern_name(int p) { return p == ARF_ALLREDUCE ? "kAllReduce" : "kARResidualRMSNorm"; }
 const char* path_name(int p) {
-    return p == ARF_PATH_FLAT ? "flat" : p == ARF_PATH_ROW ? "row" : "cluster";
+    return p == ARF_PATH_FLAT ? "flat" : p == ARF_PATH_ROW ? "row" : p == ARF_PATH_CLUSTER ? "cluster" : "async";
 }
 
 }  // namespace
@@ -89,13 +113,15 @@ extern "C" arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out
     cudaError_t e = cudaGetDeviceCount(&count);
     if (e == cudaSuccess && (device < 0 || device >= count)) e = cudaErrorInvalidDevice;
     if (e == cudaSuccess) e = cudaSetDevice(device);
-    int sms = 0, thr = 0, cl = 0;
+    int sms = 0, thr = 0, cl = 0, smem = 0;
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&thr, cudaDevAttrMaxThreadsPerMultiProcessor, device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&cl, cudaDevAttrClusterLaunch, device);
-    if (e == cudaSuccess && cl) {
-        e = arf::allow_large_clusters_bf16();
-        if (e == cudaSuccess) e = arf::allow_large_clusters_fp16();
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    if (e == cudaSuccess) {
+        const int dyn = smem - arf::kAsyncStaticSmem;
+        e = arf::configure_kernels_bf16(cl != 0, dyn);
+        if (e == cudaSuccess) e = arf::configure_kernels_fp16(cl != 0, dyn);
     }
     if (e != cudaSuccess) {
         delete ws;
@@ -105,6 +131,7 @@ extern "C" arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out
     ws->device = device;
     ws->caps.num_sms = sms;
     ws->caps.max_threads_per_sm = thr;
+    ws->caps.max_smem_per_block = smem;
     ws->caps.max_cluster = 1;
     if (cl) {
         // The largest cluster the row-split kernel can be launched with,
@@ -128,8 +155,8 @@ extern "C" arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out
     const char* lg = std::getenv("ARF_LOG");
     ws->log = lg && lg[0] == '1';
     if (ws->log)
-        std::fprintf(stderr, "[arf] device %d: %d SMs, %d threads/SM, max cluster %d\n", device, sms, thr,
-                     ws->caps.max_cluster);
+        std::fprintf(stderr, "[arf] device %d: %d SMs, %d threads/SM, %d B smem/CTA, max cluster %d\n", device,
+                     sms, thr, smem, ws->caps.max_cluster);
     *ws_out = ws;
     return ARF_OK;
 }
@@ -199,6 +226,10 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
             while (cs < 8 && cs < caps->max_cluster && (int64_t)cs * M < 32) cs *= 2;
         }
         pl = rms_plan(*caps, w_spec, M, H, cs, vpt);
+        // Enough rows to give every SM several: stream them through the
+        // asynchronous-copy ring when at least 3 column blocks fit in flight.
+        const int st = async_stages(*caps, w_spec, H);
+        if (M >= caps->num_sms && st >= 3) pl = async_plan(*caps, w_spec, M, st);
     }
     *plan_out = pl;
     return ARF_OK;
@@ -213,6 +244,15 @@ extern "C" arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_
     if (!arf::w_spec_compiled(pl->w_spec)) return ARF_ERR_UNSUPPORTED;
     if (pl->threads < 32 || pl->threads > kMaxThreads || pl->threads % 32 != 0) return ARF_ERR_UNSUPPORTED;
     if (pl->cluster < 1 || pl->grid < 1 || pl->grid % pl->cluster != 0) return ARF_ERR_UNSUPPORTED;
+    if (pl->path == ARF_PATH_ASYNC) {
+        if (pattern != ARF_AR_RESIDUAL_RMSNORM || pl->w_spec == 0 || pl->w_spec != W) return ARF_ERR_UNSUPPORTED;
+        if (pl->threads != arf::kAsyncCtaThreads || pl->cluster != 1 || pl->vpt != 1) return ARF_ERR_UNSUPPORTED;
+        if (pl->stages < 2 || pl->stages > 8) return ARF_ERR_UNSUPPORTED;
+        const size_t need = arf::async_dyn_smem(W, pl->stages, (int)(H / 8)) + arf::kAsyncStaticSmem;
+        if (need > (size_t)caps->max_smem_per_block) return ARF_ERR_UNSUPPORTED;
+        return ARF_OK;
+    }
+    if (pl->stages != 0) return ARF_ERR_UNSUPPORTED;
     if (pattern == ARF_ALLREDUCE) {
         if (pl->path != ARF_PATH_FLAT || pl->cluster != 1) return ARF_ERR_UNSUPPORTED;
         if (!(pl->vpt == 1 || pl->vpt == 2 || pl->vpt == 4) || !arf::flat_unroll_compiled(pl->w_spec, pl->vpt))
@@ -239,8 +279,9 @@ cudaError_t max_active_clusters(arf_dtype_t dt, const arf_plan_t& pl, int* n) {
     return dt == ARF_BF16 ? arf::rms_max_active_clusters_bf16(pl, n) : arf::rms_max_active_clusters_fp16(pl, n);
 }
 
-cudaError_t max_active_blocks(arf_dtype_t dt, const arf_plan_t& pl, int* n) {
-    return dt == ARF_BF16 ? arf::rms_max_active_blocks_bf16(pl, n) : arf::rms_max_active_blocks_fp16(pl, n);
+cudaError_t max_active_blocks(arf_dtype_t dt, const arf_plan_t& pl, int64_t H, int* n) {
+    const int C = (int)(H / 8);
+    return dt == ARF_BF16 ? arf::rms_max_active_blocks_bf16(pl, C, n) : arf::rms_max_active_blocks_fp16(pl, C, n);
 }
 
 // The planner's plan, with the cluster size lowered until the cluster kernel
@@ -261,6 +302,16 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
     arf_plan_t pl;
     arf_status_t st = arf_plan_for_caps(&ws->caps, pattern, W, M, H, dtype, &pl);
     if (st != ARF_OK) return st;
+    if (!capturing && pl.path == ARF_PATH_ASYNC) {
+        int b = 0;
+        cudaError_t e = max_active_blocks(dtype, pl, H, &b);
+        if (e != cudaSuccess || b < 1) {  // the ring does not fit: one CTA per row instead
+            (void)cudaGetLastError();
+            int vpt = 1;
+            while (vpt < 8 && ceil_div(H / 8, vpt) > kMaxThreads) vpt *= 2;
+            pl = rms_plan(ws->caps, pl.w_spec, M, H, 1, vpt);
+        }
+    }
     while (!capturing && pl.path == ARF_PATH_CLUSTER) {
         int n = 0;
         cudaError_t e = max_active_clusters(dtype, pl, &n);
@@ -274,7 +325,7 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
     }
     if (!capturing && pl.path == ARF_PATH_ROW) {
         int b = 0;
-        cudaError_t e = max_active_blocks(dtype, pl, &b);
+        cudaError_t e = max_active_blocks(dtype, pl, H, &b);
         if (e == cudaSuccess && b > 0) {
             const int64_t cap = (int64_t)ws->caps.num_sms * b;
             if (cap < pl.grid) pl.grid = (int)cap;
@@ -283,9 +334,9 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
         }
     }
     if (ws->log)
-        std::fprintf(stderr, "[arf] plan %s W=%d M=%lld H=%lld %s: path=%s threads=%d vpt=%d cluster=%d grid=%d w_spec=%d\n",
+        std::fprintf(stderr, "[arf] plan %s W=%d M=%lld H=%lld %s: path=%s threads=%d vpt=%d cluster=%d grid=%d w_spec=%d stages=%d\n",
                      pattern_name(pattern), W, (long long)M, (long long)H, dtype == ARF_BF16 ? "bf16" : "fp16",
-                     path_name(pl.path), pl.threads, pl.vpt, pl.cluster, pl.grid, pl.w_spec);
+                     path_name(pl.path), pl.threads, pl.vpt, pl.cluster, pl.grid, pl.w_spec, pl.stages);
     std::lock_guard<std::mutex> lk(ws->mu);
     ws->plans[key] = pl;
     *out = pl;
@@ -366,6 +417,7 @@ arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t patt
         p.W = W;
         p.cs = pl.cluster;
         p.slice = (int)ceil_div(p.C, pl.cluster);
+        p.stages = pl.stages;
         p.eps = eps;
         e = dtype == ARF_BF16 ? arf::launch_rms_bf16(p, pl, stream) : arf::launch_rms_fp16(p, pl, stream);
     }
@@ -406,6 +458,12 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
             cudaError_t e = max_active_clusters(dtype, pl, &n);
             if (e != cudaSuccess) return cuda_fail(ws, e);
             if (n < 1) return ARF_ERR_UNSUPPORTED;
+        }
+        if (pl.path == ARF_PATH_ASYNC && !capturing) {
+            int b = 0;
+            cudaError_t e = max_active_blocks(dtype, pl, H, &b);
+            if (e != cudaSuccess) return cuda_fail(ws, e);
+            if (b < 1) return ARF_ERR_UNSUPPORTED;
         }
     } else {
         st = device_plan(ws, pattern, W, M, H, dtype, &pl, capturing);

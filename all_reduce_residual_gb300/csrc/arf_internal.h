@@ -49,6 +49,7 @@ struct RmsParams {
     int W;
     int cs;     // CTAs per row (cluster size), 1 = no cluster
     int slice;  // chunks per CTA: ceil(C / cs)
+    int stages; // streaming path: copy groups in flight per thread
     float eps;
 };
 
@@ -59,18 +60,29 @@ cudaError_t launch_flat_fp16(const FlatParams& p, const arf_plan_t& plan, cudaSt
 cudaError_t launch_rms_bf16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s);
 cudaError_t launch_rms_fp16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s);
 
-// Allow 16-CTA clusters on every cluster kernel of one I/O type (once per
-// device, at workspace creation).
-cudaError_t allow_large_clusters_bf16();
-cudaError_t allow_large_clusters_fp16();
+// Per-device kernel attributes, set once at workspace creation: 16-CTA
+// clusters for the cluster kernels (when the device has clusters) and
+// `max_dyn_smem` bytes of dynamic shared memory for the streaming kernels.
+cudaError_t configure_kernels_bf16(bool clusters, int max_dyn_smem);
+cudaError_t configure_kernels_fp16(bool clusters, int max_dyn_smem);
+
+// Threads per CTA and static shared memory of the streaming kernel.
+constexpr int kAsyncCtaThreads = 256;
+constexpr int kAsyncStaticSmem = 1024;  // upper bound, for the planner
+// Dynamic shared memory of the streaming kernel for W ranks, `stages` ring
+// slots and rows of C chunks.
+constexpr size_t async_dyn_smem(int W, int stages, int C) {
+    return (size_t)stages * (size_t)(W + 1) * kAsyncCtaThreads * 16u + (size_t)C * 16u;
+}
 
 // How many clusters of plan.cluster CTAs of plan.threads threads the RMS
 // kernel instance of `plan` can keep resident at once (0 = cannot launch).
 cudaError_t rms_max_active_clusters_bf16(const arf_plan_t& plan, int* n);
 cudaError_t rms_max_active_clusters_fp16(const arf_plan_t& plan, int* n);
-// How many CTAs of the RMS kernel instance of `plan` one SM can hold.
-cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int* n);
-cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int* n);
+// How many CTAs of the RMS kernel instance of `plan` (rows of C chunks) one
+// SM can hold.
+cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int C, int* n);
+cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int C, int* n);
 
 // Record a CUDA error as the workspace's last one (arf_last_cuda_error).
 void note_cuda_error(arf_workspace_t ws, cudaError_t e);

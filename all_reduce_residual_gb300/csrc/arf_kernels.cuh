@@ -409,6 +409,118 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
     if (cs > 1) cg::this_cluster().sync();
 }
 
+// ---------------------------------------------------------------------------
+// kARResidualRMSNorm, streaming form (ARF_PATH_ASYNC). One CTA of
+// kAsyncThreads threads per SM walks its rows (blockIdx.x + i*gridDim.x) in
+// column blocks of kAsyncThreads chunks; thread t owns chunk t of every block.
+// For the work item `stages-1` items ahead, each thread copies its chunk's
+// W+1 vectors (partials, residual) into its own slots of a shared-memory ring
+// with cp.async (16 bytes, cached in L2 only). Copies therefore stay in
+// flight across row boundaries and barriers without holding registers, which
+// lets wide rank counts (W = 16) keep as many bytes in flight as narrow ones.
+// A thread reads only the slots it filled, so the hardware wait on its own
+// copy groups (cp.async.wait_group) is all the data synchronisation there is.
+// The rounded residual_out of the row stays in shared memory (same thread
+// reads it back) until the row's statistic is known.
+// ---------------------------------------------------------------------------
+constexpr int kAsyncThreads = kAsyncCtaThreads;
+
+__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* gptr) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr), "l"(gptr) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most n of this thread's most recent copy groups are pending
+// (n >= 7 waits down to 7, which is stricter and still correct).
+__device__ __forceinline__ void cp_async_wait(int n) {
+    switch (n) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+        case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    }
+}
+
+template <typename T, int WS>
+__global__ void __launch_bounds__(kAsyncThreads, 1) rms_async_kernel(RmsParams p) {
+    static_assert(WS > 0, "the streaming kernel needs the rank count at compile time");
+    extern __shared__ __align__(16) uint4 dyn_smem[];
+    __shared__ const uint4* s_ptr[ARF_MAX_W];
+    __shared__ float s_warp[2][kMaxThreads / 32];
+
+    prologue(s_ptr, p.lc, p.W);
+    __syncthreads();
+
+    const int S = p.stages;
+    const int C = p.C;
+    const int tid = threadIdx.x;
+    const int nb = (C + kAsyncThreads - 1) / kAsyncThreads;
+    uint4* ring = dyn_smem;                                           // [S][WS+1][kAsyncThreads]
+    uint4* xrow = dyn_smem + (size_t)S * (WS + 1) * kAsyncThreads;    // [C]
+    const uint32_t ring_addr = (uint32_t)__cvta_generic_to_shared(ring);
+    constexpr uint32_t kRankStride = kAsyncThreads * 16;              // bytes between ranks in a slot
+    constexpr uint32_t kSlotStride = (WS + 1) * kRankStride;          // bytes between ring slots
+
+    // The producer side walks work items (row, column block) `S-1` ahead of
+    // the consumer side; both advance (row, block, slot) by counting, no
+    // division. Every item commits one copy group (empty past the last row),
+    // so "at most S-1 groups pending" always means "my oldest item landed".
+    int64_t in_row = blockIdx.x;
+    int in_b = 0, in_slot = 0;
+    auto issue_next = [&]() {
+        if (in_row < p.M) {
+            const int c = in_b * kAsyncThreads + tid;
+            if (c < C) {
+                const int64_t off = in_row * (int64_t)C + c;
+                const uint32_t slot = ring_addr + (uint32_t)in_slot * kSlotStride + (uint32_t)tid * 16u;
+#pragma unroll
+                for (int r = 0; r < WS; ++r) cp_async16(slot + r * kRankStride, s_ptr[r] + off);
+                cp_async16(slot + WS * kRankStride, p.residual + off);
+            }
+            if (++in_b == nb) {
+                in_b = 0;
+                in_row += gridDim.x;
+            }
+            if (++in_slot == S) in_slot = 0;
+        }
+        cp_async_commit();
+    };
+
+    for (int j = 0; j < S - 1; ++j) issue_next();
+    int slot_i = 0, it = 0;
+    for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++it) {
+        const int64_t rbase = row * (int64_t)C;
+        float ss = 0.0f;
+        for (int b = 0; b < nb; ++b) {
+            issue_next();
+            cp_async_wait(S - 1);  // this item has landed in this thread's slots
+            const int c = b * kAsyncThreads + tid;
+            if (c < C) {
+                const uint4* slot = ring + (size_t)slot_i * (WS + 1) * kAsyncThreads + tid;
+                float acc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+                for (int r = 0; r < WS; ++r) accumulate<T>(acc, slot[r * kAsyncThreads]);
+                xrow[c] = residual_chunk<T>(acc, slot[WS * kAsyncThreads], p.residual_out + rbase + c, ss);
+            }
+            if (++slot_i == S) slot_i = 0;
+        }
+        // the row is complete: normalise it
+        const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
+        for (int b = 0; b < nb; ++b) {
+            const int c = b * kAsyncThreads + tid;
+            if (c < C) normalise_chunk<T>(xrow[c], ld_keep(p.gamma + c), inv, p.out + rbase + c);
+        }
+    }
+    cp_async_wait(0);  // only empty groups can remain; leave with nothing in flight
+}
+
 // Writes the W partial pointers of a staging area laid out as W equal
 // partials, `stride` bytes apart (host-buffer entry point).
 __global__ void fill_pointer_array(const void** array, const char* first, int64_t stride, int W);

@@ -57,6 +57,18 @@ RmsFn rms_kernel_for(int ws, int vpt) {
 }
 
 template <typename T>
+RmsFn async_kernel_for(int ws) {
+    switch (ws) {
+        case 1: return rms_async_kernel<T, 1>;
+        case 2: return rms_async_kernel<T, 2>;
+        case 4: return rms_async_kernel<T, 4>;
+        case 8: return rms_async_kernel<T, 8>;
+        case 16: return rms_async_kernel<T, 16>;
+        default: return nullptr;
+    }
+}
+
+template <typename T>
 cudaError_t launch_flat_t(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s) {
     FlatFn fn = flat_kernel_for<T>(plan.w_spec, plan.vpt);
     if (!fn) return cudaErrorInvalidValue;
@@ -76,12 +88,14 @@ cudaError_t launch_flat_t(const FlatParams& p, const arf_plan_t& plan, cudaStrea
 
 template <typename T>
 cudaError_t launch_rms_t(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s) {
-    RmsFn fn = rms_kernel_for<T>(plan.w_spec, plan.vpt);
+    const bool streaming = plan.path == ARF_PATH_ASYNC;
+    RmsFn fn = streaming ? async_kernel_for<T>(plan.w_spec) : rms_kernel_for<T>(plan.w_spec, plan.vpt);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.grid);
     cfg.blockDim = dim3((unsigned)plan.threads);
+    cfg.dynamicSmemBytes = streaming ? async_dyn_smem(plan.w_spec, plan.stages, p.C) : 0;
     cfg.stream = s;
     unsigned n = 0;
     if (plan.cluster > 1) {
@@ -102,15 +116,22 @@ cudaError_t launch_rms_t(const RmsParams& p, const arf_plan_t& plan, cudaStream_
 }
 
 template <typename T>
-cudaError_t allow_large_clusters_t() {
+cudaError_t configure_kernels_t(bool clusters, int max_dyn_smem) {
     const int ws_list[] = {0, 1, 2, 4, 8, 16};
     const int vpt_list[] = {1, 2, 4, 8};
-    for (int ws : ws_list)
-        for (int vpt : vpt_list) {
-            cudaError_t e = cudaFuncSetAttribute(rms_kernel_for<T>(ws, vpt),
-                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return e;
-        }
+    if (clusters)
+        for (int ws : ws_list)
+            for (int vpt : vpt_list) {
+                cudaError_t e = cudaFuncSetAttribute(rms_kernel_for<T>(ws, vpt),
+                                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return e;
+            }
+    for (int ws : ws_list) {
+        RmsFn fn = async_kernel_for<T>(ws);
+        if (!fn) continue;
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
+        if (e != cudaSuccess) return e;
+    }
     return cudaSuccess;
 }
 
@@ -132,10 +153,12 @@ cudaError_t rms_max_active_clusters_t(const arf_plan_t& plan, int* n) {
 }
 
 template <typename T>
-cudaError_t rms_max_active_blocks_t(const arf_plan_t& plan, int* n) {
-    RmsFn fn = rms_kernel_for<T>(plan.w_spec, plan.vpt);
+cudaError_t rms_max_active_blocks_t(const arf_plan_t& plan, int C, int* n) {
+    const bool streaming = plan.path == ARF_PATH_ASYNC;
+    RmsFn fn = streaming ? async_kernel_for<T>(plan.w_spec) : rms_kernel_for<T>(plan.w_spec, plan.vpt);
     if (!fn) return cudaErrorInvalidValue;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fn, plan.threads, 0);
+    const size_t smem = streaming ? async_dyn_smem(plan.w_spec, plan.stages, C) : 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fn, plan.threads, smem);
 }
 
 }  // namespace arf

@@ -9,13 +9,15 @@ cudaError_t launch_flat_fp16(const FlatParams& p, const arf_plan_t& plan, cudaSt
 cudaError_t launch_rms_fp16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s) {
     return launch_rms_t<__half>(p, plan, s);
 }
-cudaError_t allow_large_clusters_fp16() { return allow_large_clusters_t<__half>(); }
+cudaError_t configure_kernels_fp16(bool clusters, int max_dyn_smem) {
+    return configure_kernels_t<__half>(clusters, max_dyn_smem);
+}
 cudaError_t rms_max_active_clusters_fp16(const arf_plan_t& plan, int* n) {
     return rms_max_active_clusters_t<__half>(plan, n);
 }
 
-cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int* n) {
-    return rms_max_active_blocks_t<__half>(plan, n);
+cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int C, int* n) {
+    return rms_max_active_blocks_t<__half>(plan, C, n);
 }
 
 }  // namespace arf

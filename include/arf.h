@@ -76,8 +76,12 @@ typedef enum arf_dtype {
 typedef enum arf_path {
     ARF_PATH_FLAT = 0,    /* kAllReduce: grid-stride over 16-byte chunks of [M,H] */
     ARF_PATH_ROW = 1,     /* kARResidualRMSNorm: one CTA owns a whole row */
-    ARF_PATH_CLUSTER = 2  /* kARResidualRMSNorm: a row split over a thread-block
+    ARF_PATH_CLUSTER = 2, /* kARResidualRMSNorm: a row split over a thread-block
                              cluster, sum of squares exchanged through DSMEM */
+    ARF_PATH_ASYNC = 3    /* kARResidualRMSNorm, W in {1,2,4,8,16}: one CTA of
+                             256 threads per SM streams its rows in column
+                             blocks of 256 chunks through a ring of `stages`
+                             asynchronous shared-memory copies (cp.async) */
 } arf_path_t;
 
 /* Limits of this build. */
@@ -89,18 +93,21 @@ typedef struct arf_device_caps {
     int num_sms;            /* streaming multiprocessors */
     int max_cluster;        /* largest usable cluster size (1, 2, 4, 8 or 16) */
     int max_threads_per_sm; /* resident threads per SM */
+    int max_smem_per_block; /* opt-in shared memory per CTA, bytes */
 } arf_device_caps_t;
 
 /* A launch plan: which kernel shape and launch configuration one call uses. */
 typedef struct arf_plan {
     int path;     /* arf_path_t */
-    int threads;  /* threads per CTA, a multiple of 32 in [32, 1024] */
+    int threads;  /* threads per CTA, a multiple of 32 in [32, 512] */
     int vpt;      /* 16-byte chunks per thread per row (row/cluster paths) or
                      chunks per thread per loop trip (flat path): 1, 2, 4 or 8 */
     int cluster;  /* CTAs per row (cluster path: 2, 4, 8 or 16; else 1) */
     int grid;     /* CTAs launched; a multiple of `cluster` */
     int w_spec;   /* rank count compiled into the kernel, or 0 for the generic
                      kernel that reads W at run time */
+    int stages;   /* async path: copies in flight per thread, in column
+                     blocks (2..8); 0 on the other paths */
 } arf_plan_t;
 
 typedef struct arf_workspace* arf_workspace_t;

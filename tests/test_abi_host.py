@@ -13,7 +13,7 @@ from all_reduce_residual_gb300 import _binding, build
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "arf.h")
 
-GB300 = arf.DeviceCaps(num_sms=152, max_cluster=16, max_threads_per_sm=2048)
+GB300 = arf.DeviceCaps(num_sms=152, max_cluster=16, max_threads_per_sm=2048, max_smem_per_block=232448)
 K3_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048)
 SHAPES = [(2, 8, 1024), (2, 128, 4096), *[(8, m, 7168) for m in K3_M], (4, 5851, 7168), (16, 585, 7168),
           (1, 1, 8), (3, 7, 8), (64, 3, 32768), (5, 1000, 1000), (17, 200, 2048)]
@@ -75,13 +75,21 @@ def test_supports_rules(pattern):
 @pytest.mark.parametrize("pattern", [arf.ARF_ALLREDUCE, arf.ARF_AR_RESIDUAL_RMSNORM])
 @pytest.mark.parametrize("W,M,H", SHAPES)
 def test_planner_plans_are_legal(pattern, W, M, H):
-    for caps in (GB300, arf.DeviceCaps(148, 8, 2048), arf.DeviceCaps(132, 1, 2048), arf.DeviceCaps(1, 1, 1024)):
+    for caps in (GB300, arf.DeviceCaps(148, 8, 2048, 232448), arf.DeviceCaps(132, 1, 2048, 101376),
+                 arf.DeviceCaps(1, 1, 1024, 49152)):
         p = arf.Plan()
         assert arf.arf_plan_for_caps(caps, pattern, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
         assert arf.arf_plan_check(caps, p, pattern, W, M, H, arf.ARF_BF16) == arf.ARF_OK, p
         assert p.grid % p.cluster == 0 and p.threads % 32 == 0
         assert p.w_spec in (0, W)
         per_sm = caps.max_threads_per_sm // p.threads
+        if p.path == arf.ARF_PATH_ASYNC:
+            # many rows, compile-time W: one streaming CTA per SM, ring of >= 3 blocks in shared memory
+            assert M >= caps.num_sms and W in (1, 2, 4, 8, 16) and p.grid == caps.num_sms
+            ring = p.stages * (W + 1) * 256 * 16 + (H // 8) * 16
+            assert 3 <= p.stages <= 8 and ring + 1024 <= caps.max_smem_per_block
+            continue
+        assert p.stages == 0
         if pattern == arf.ARF_ALLREDUCE:
             assert p.path == arf.ARF_PATH_FLAT and p.cluster == 1
             chunks = M * H // 8
@@ -106,12 +114,14 @@ def test_planner_uses_the_sm_count():
     arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 128, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and (p.threads, p.vpt, p.grid) == (448, 2, 128)
     arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 2048, 7168, arf.ARF_BF16, p)
-    assert p.path == arf.ARF_PATH_ROW and p.grid % 152 == 0
+    assert p.path == arf.ARF_PATH_ASYNC and p.grid == 152 and p.stages == 5
     arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 4, 5851, 7168, arf.ARF_BF16, p)
-    assert p.path == arf.ARF_PATH_ROW and p.vpt * (4 + 1) <= 18 and p.grid % 152 == 0
+    assert p.path == arf.ARF_PATH_ASYNC and p.stages == 8
     arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7168, arf.ARF_BF16, p)
-    assert p.path == arf.ARF_PATH_ROW and (p.threads, p.vpt) == (448, 2)  # 896 chunks > 512 threads
-    no_cluster = arf.DeviceCaps(152, 1, 2048)
+    assert p.path == arf.ARF_PATH_ASYNC and p.stages == 3
+    arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 17, 585, 7168, arf.ARF_BF16, p)
+    assert p.path == arf.ARF_PATH_ROW and (p.threads, p.vpt) == (448, 2)  # generic W: no streaming kernel
+    no_cluster = arf.DeviceCaps(152, 1, 2048, 232448)
     arf.arf_plan_for_caps(no_cluster, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 1, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and p.grid == 1
 
@@ -136,13 +146,26 @@ def test_plan_check_rejects_bad_plans():
     assert with_(path=arf.ARF_PATH_CLUSTER, cluster=32, grid=64) == arf.ARF_ERR_UNSUPPORTED
     assert with_(path=arf.ARF_PATH_CLUSTER, cluster=4, grid=6) == arf.ARF_ERR_UNSUPPORTED
     assert with_(path=arf.ARF_PATH_ROW, cluster=1, threads=32, vpt=1) == arf.ARF_ERR_UNSUPPORTED  # 896 chunks
-    small = arf.DeviceCaps(152, 4, 2048)
+    small = arf.DeviceCaps(152, 4, 2048, 232448)
     p = arf.Plan(path=arf.ARF_PATH_CLUSTER, threads=64, vpt=1, cluster=16, grid=16, w_spec=8)
     assert arf.arf_plan_check(small, p, *args) == arf.ARF_ERR_UNSUPPORTED
     flat = arf.Plan(path=arf.ARF_PATH_FLAT, threads=256, vpt=4, cluster=1, grid=10, w_spec=16)
     assert arf.arf_plan_check(GB300, flat, arf.ARF_ALLREDUCE, 16, 4, 64, arf.ARF_BF16) == arf.ARF_ERR_UNSUPPORTED
     flat.vpt = 1
     assert arf.arf_plan_check(GB300, flat, arf.ARF_ALLREDUCE, 16, 4, 64, arf.ARF_BF16) == arf.ARF_OK
+    flat.stages = 2
+    assert arf.arf_plan_check(GB300, flat, arf.ARF_ALLREDUCE, 16, 4, 64, arf.ARF_BF16) == arf.ARF_ERR_UNSUPPORTED
+    a = arf.Plan(path=arf.ARF_PATH_ASYNC, threads=256, vpt=1, cluster=1, grid=152, w_spec=16, stages=3)
+    rms16 = (arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7168, arf.ARF_FP16)
+    assert arf.arf_plan_check(GB300, a, *rms16) == arf.ARF_OK
+    a.stages = 4  # 4 x 17 x 4 KiB does not fit next to the row buffer
+    assert arf.arf_plan_check(GB300, a, *rms16) == arf.ARF_ERR_UNSUPPORTED
+    a.stages, a.threads = 3, 128
+    assert arf.arf_plan_check(GB300, a, *rms16) == arf.ARF_ERR_UNSUPPORTED
+    a.threads, a.w_spec = 256, 0
+    assert arf.arf_plan_check(GB300, a, *rms16) == arf.ARF_ERR_UNSUPPORTED
+    a.w_spec = 16
+    assert arf.arf_plan_check(GB300, a, arf.ARF_ALLREDUCE, 16, 585, 7168, arf.ARF_FP16) == arf.ARF_ERR_UNSUPPORTED
 
 
 def test_staging_bytes():

@@ -63,12 +63,21 @@ def rms_plans(ws, W, M, H, grids=("full", 1)):
                                  vpt=vpt, cluster=cs, grid=max(1, nclus) * cs, w_spec=w_spec)
                     assert arf.arf_plan_check(caps, p, RMS, W, M, H, arf.ARF_BF16) == arf.ARF_OK, p
                     plans.append(p)
+    if W in (1, 2, 4, 8, 16):  # the streaming kernel, every ring depth that fits
+        for stages in range(2, 9):
+            for g in ("full", 1, 3):
+                grid = min(M, caps.num_sms) if g == "full" else g
+                p = arf.Plan(path=arf.ARF_PATH_ASYNC, threads=256, vpt=1, cluster=1, grid=grid, w_spec=W,
+                             stages=stages)
+                if arf.arf_plan_check(caps, p, RMS, W, M, H, arf.ARF_BF16) == arf.ARF_OK:
+                    plans.append(p)
     return plans
 
 
 @pytest.mark.parametrize("W,M,H,dtype", [(3, 37, 1000, "bf16"), (8, 5, 7168, "bf16"), (16, 3, 4096, "fp16"),
                                          (1, 9, 8, "bf16"), (64, 2, 256, "fp16"), (5, 4, 32768, "bf16"),
-                                         (2, 19, 2056, "bf16")])
+                                         (2, 19, 2056, "bf16"), (4, 41, 7176, "bf16"), (16, 23, 7168, "fp16"),
+                                         (8, 13, 32768, "bf16"), (1, 300, 264, "fp16")])
 def test_every_rms_plan(ws, W, M, H, dtype):
     inp = inputs(W, M, H, dtype)
     ref = oracle_run(RMS, inp)
@@ -78,8 +87,8 @@ def test_every_rms_plan(ws, W, M, H, dtype):
     for plan in rms_plans(ws, W, M, H):
         try:
             got = gpu_run(ws, RMS, P, R, G, inp.workload.eps, plan=plan)
-        except arf.ArfError as e:  # a cluster shape this device cannot keep resident
-            assert e.status == arf.ARF_ERR_UNSUPPORTED and plan.cluster > 1, e
+        except arf.ArfError as e:  # a cluster or ring shape this device cannot keep resident
+            assert e.status == arf.ARF_ERR_UNSUPPORTED and (plan.cluster > 1 or plan.stages > 0), e
             continue
         ran += 1
         assert_parity(DT[dtype], RMS, got, ref, f"{plan}")
