@@ -36,30 +36,6 @@ arf_status_t cuda_fail(arf_workspace_t ws, cudaError_t e) {
     return ARF_ERR_CUDA;
 }
 
-// Ring depth of the streaming kernel that fits in one CTA's shared memory
-// next to a row of rounded residual_out (0 when it does not apply).
-int async_stages(const arf_device_caps_t& caps, int w_spec, int64_t H) {
-    if (w_spec == 0) return 0;
-    const int64_t C = H / 8;
-    const int64_t avail = (int64_t)caps.max_smem_per_block - arf::kAsyncStaticSmem - C * 16;
-    const int64_t per = (int64_t)(w_spec + 1) * arf::kAsyncCtaThreads * 16;
-    const int64_t st = avail > 0 ? avail / per : 0;
-    return st < 2 ? 0 : (int)(st > 8 ? 8 : st);
-}
-
-arf_plan_t async_plan(const arf_device_caps_t& caps, int w_spec, int64_t M, int stages) {
-    arf_plan_t pl = {};
-    pl.path = ARF_PATH_ASYNC;
-    pl.threads = arf::kAsyncCtaThreads;
-    pl.vpt = 1;
-    pl.cluster = 1;
-    pl.w_spec = w_spec;
-    pl.stages = stages;
-    const int64_t g = M < caps.num_sms ? M : caps.num_sms;
-    pl.grid = (int)(g > 0 ? g : 1);
-    return pl;
-}
-
 // The RMS plan for a given cluster size and chunks-per-thread count: threads
 // cover the CTA's slice in whole warps; grid = rows (clusters) up to what the
 // SMs can hold by thread count (the workspace refines this by occupancy).
@@ -226,10 +202,11 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
             while (cs < 8 && cs < caps->max_cluster && (int64_t)cs * M < 32) cs *= 2;
         }
         pl = rms_plan(*caps, w_spec, M, H, cs, vpt);
-        // Enough rows to give every SM several: stream them through the
-        // asynchronous-copy ring when at least 3 column blocks fit in flight.
-        const int st = async_stages(*caps, w_spec, H);
-        if (M >= caps->num_sms && st >= 3) pl = async_plan(*caps, w_spec, M, st);
+        // The streaming kernel (ARF_PATH_ASYNC) is not chosen: measured on
+        // GB300 it keeps fewer bytes in flight than the row kernel's register
+        // prefetch (8 warps per SM issuing per-thread copies), e.g. 107 us vs
+        // 83 us in-kernel for W=4, M=5851, H=7168. It stays available to
+        // explicit plans.
     }
     *plan_out = pl;
     return ARF_OK;
