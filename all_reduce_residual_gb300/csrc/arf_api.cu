@@ -175,16 +175,20 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
     arf_plan_t pl = {};
     if (pattern == ARF_ALLREDUCE) {
         // one pass over all chunks (no grid-stride trips); about 8 loads
-        // outstanding per thread
+        // outstanding per thread when there is enough work to fill the
+        // device several times over, else one chunk per thread (latency:
+        // as many CTAs as the work allows)
+        const int64_t nchunks = M * H / 8;
         int u = 1;
         if (w_spec > 0) u = w_spec <= 2 ? 4 : (w_spec <= 4 ? 2 : 1);
+        if (nchunks < (int64_t)caps->num_sms * caps->max_threads_per_sm * 2) u = 1;
         while (!arf::flat_unroll_compiled(w_spec, u)) u /= 2;
         pl.path = ARF_PATH_FLAT;
         pl.threads = 256;
         pl.vpt = u;
         pl.cluster = 1;
         pl.w_spec = w_spec;
-        const int64_t need = ceil_div(M * H / 8, (int64_t)pl.threads * u);
+        const int64_t need = ceil_div(nchunks, (int64_t)pl.threads * u);
         pl.grid = (int)(need < 1 ? 1 : (need > INT32_MAX ? INT32_MAX : need));
     } else {
         // One CTA per row with the fewest 16-byte chunks per thread that keep

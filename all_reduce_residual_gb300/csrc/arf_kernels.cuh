@@ -116,6 +116,15 @@ __device__ __forceinline__ uint4 ld_keep(const uint4* p) { return __ldg(p); }
 
 __device__ __forceinline__ void st_out(uint4* p, const uint4& v) { *p = v; }
 
+// Chunk k (of VPT) of this thread within a run of blockDim.x*VPT chunks:
+// every warp owns VPT*32 consecutive chunks, so each warp reads 512*VPT
+// contiguous bytes of every rank's tensor (DRAM row locality), and each warp
+// instruction still covers 32 consecutive 16-byte chunks (coalescing).
+template <int VPT>
+__device__ __forceinline__ int warp_run_chunk(int k) {
+    return ((((int)threadIdx.x >> 5) * VPT + k) << 5) + ((int)threadIdx.x & 31);
+}
+
 // acc[e] += f32(v[e]), one IEEE binary32 round-to-nearest add per element.
 template <typename T>
 __device__ __forceinline__ void accumulate(float acc[8], const uint4& v) {
@@ -185,13 +194,14 @@ __global__ void __launch_bounds__(kMaxThreads) ar_flat_kernel(FlatParams p) {
 
     const int64_t nthr = blockDim.x;
     const int64_t step = (int64_t)gridDim.x * nthr * U;
-    for (int64_t base = (int64_t)blockIdx.x * nthr * U + threadIdx.x; base < p.nchunks; base += step) {
+    // this thread's first chunk of each tile of nthr*U chunks is base + u*32
+    for (int64_t base = (int64_t)blockIdx.x * nthr * U + warp_run_chunk<U>(0); base < p.nchunks; base += step) {
         if constexpr (WS > 0) {
             // all U*W loads first, then the adds
             uint4 v[U][WS];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int64_t c = base + u * nthr;
+                const int64_t c = base + u * 32;
                 if (c < p.nchunks) {
 #pragma unroll
                     for (int r = 0; r < WS; ++r) v[u][r] = ld_once(s_ptr[r] + c);
@@ -199,7 +209,7 @@ __global__ void __launch_bounds__(kMaxThreads) ar_flat_kernel(FlatParams p) {
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int64_t c = base + u * nthr;
+                const int64_t c = base + u * 32;
                 if (c < p.nchunks) {
                     float acc[8];
 #pragma unroll
@@ -212,7 +222,7 @@ __global__ void __launch_bounds__(kMaxThreads) ar_flat_kernel(FlatParams p) {
         } else {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int64_t c = base + u * nthr;
+                const int64_t c = base + u * 32;
                 if (c < p.nchunks) {
                     float acc[8];
                     rank_sum<T, 0>(acc, s_ptr, p.W, c);
@@ -250,7 +260,7 @@ __device__ __forceinline__ void issue_row(uint4 (&L)[VPT][WS + 1], const uint4* 
                                           const uint4* residual, int64_t rbase, int c0, int c1) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-        const int c = c0 + threadIdx.x + k * blockDim.x;
+        const int c = c0 + warp_run_chunk<VPT>(k);
         if (c < c1) {
             const uint4* rp = residual + rbase + c;
             asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -336,7 +346,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
     if constexpr (Shape::kGammaRegs) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const int c = c0 + threadIdx.x + k * blockDim.x;
+            const int c = c0 + warp_run_chunk<VPT>(k);
             if (c < c1) g[k] = ld_keep(p.gamma + c);
         }
     }
@@ -352,7 +362,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
             float ss = 0.0f;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int c = c0 + threadIdx.x + k * blockDim.x;
+                const int c = c0 + warp_run_chunk<VPT>(k);
                 if (c < c1) {
                     float acc[8];
 #pragma unroll
@@ -367,7 +377,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
             const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, it) / (float)p.H + p.eps);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int c = c0 + threadIdx.x + k * blockDim.x;
+                const int c = c0 + warp_run_chunk<VPT>(k);
                 if (c < c1) {
                     uint4 gv;
                     if constexpr (Shape::kGammaRegs) gv = g[k];
@@ -384,7 +394,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
             float ss = 0.0f;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int c = c0 + threadIdx.x + k * blockDim.x;
+                const int c = c0 + warp_run_chunk<VPT>(k);
                 if (c < c1) {
                     float acc[8];
                     const uint4 rv = ld_resid(p.residual + rbase + c);
@@ -395,7 +405,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
             const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, it) / (float)p.H + p.eps);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int c = c0 + threadIdx.x + k * blockDim.x;
+                const int c = c0 + warp_run_chunk<VPT>(k);
                 if (c < c1) {
                     uint4 gv;
                     if constexpr (Shape::kGammaRegs) gv = g[k];

@@ -6,7 +6,11 @@
 One step = one pass of the whole hot path over one batch: a kAllReduce call
 and a kARResidualRMSNorm call on the workload's partials (default workload:
 Llama-3-8B-like TP2 decode, W=2, M=128, H=4096, bf16). The L2 is flushed
-(a write of twice its size) before every step, outside the timed events.
+before every step, outside the timed events: a write of twice its size, then
+a read of another buffer of twice its size. The read evicts the flush's own
+dirty lines, so their write-back to HBM is not charged to the timed kernels
+(a write-only flush adds 5-13 us of such write-backs to each call here); the
+sweep reports both.
 Metric: achieved HBM GB/s = algorithmic bytes / device time, where the
 algorithmic bytes read every partial and the residual once, gamma once and
 write each output once. Rank 0 prints one JSON line.
@@ -176,6 +180,32 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class L2Flush:
+    """Leaves the L2 holding none of the benchmark's data: write `nbytes`
+    (twice the L2), then read another `nbytes` so that the L2 ends up full
+    of clean lines (no write-back pending when the timed kernels start).
+    zero_(dirty_only=True) skips the read: the plain write flush."""
+
+    def __init__(self, nbytes, dev):
+        import torch
+
+        self.w = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(nbytes // 4, dtype=torch.int32, device=dev)
+        self.sink = torch.empty(1, dtype=torch.int64, device=dev)
+        self.nbytes = nbytes
+
+    def zero_(self, dirty_only=False):
+        import torch
+
+        self.w.zero_()
+        if not dirty_only:
+            torch.sum(self.r, dim=(0,), dtype=torch.int64, out=self.sink[0])
+
+    def describe(self):
+        mib = self.nbytes >> 20
+        return f"flushed before every step: write {mib} MiB, then read another {mib} MiB (L2 left clean)"
+
+
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
@@ -204,7 +234,7 @@ def run_arf(args):
     outs = {p: torch.empty_like(R) for p in pats}
     ro = torch.empty_like(R)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(max(2 * l2, 256 << 20), dev)
     bytes_call = {p: w.bytes_per_call(p) for p in pats}
     step_bytes = sum(bytes_call.values())
 
@@ -254,7 +284,7 @@ def run_arf(args):
         "config": {"workload": f"{w.name}: W={w.W} M={w.M} H={w.H} {w.dtype}, one {' + one '.join(pats)} call per step",
                    "W": w.W, "M": w.M, "H": w.H, "io_dtype": w.dtype, "accumulate": "f32",
                    "patterns": list(pats), "bytes_per_step": step_bytes,
-                   "l2": f"flushed before every step by writing {flush.numel() >> 20} MiB",
+                   "l2": flush.describe(),
                    "parallelism": f"replicas x{world}",
                    "plans": {p: ws.plan(p, w.W, w.M, w.H, torch.bfloat16 if w.dtype == "bf16"
                                         else torch.float16).as_dict() for p in pats}},
@@ -325,7 +355,7 @@ def e2e_leg(ws, w, inp, pats, flush, dev, K, world):
 def sweep(ws, dev, flush, peak):
     """µs/call and GB/s for every workload, pattern and (k3_tp8) M, through
     arf_run and through arf_run_ex with partials by value + PDL: cold
-    (L2 flushed before each call, mean of 50 CUDA-event timings: the event
+    (L2 flushed clean before each call, mean of 50 CUDA-event timings: the event
     clock ticks in steps of about 2 µs here, and the mean of many samples
     taken at random phases is unbiased where a median is not) and warm (a
     CUDA graph of 20 back-to-back calls, per-call time of the fastest of 5
@@ -350,12 +380,12 @@ def sweep(ws, dev, flush, peak):
                     arf.run(ws, pat, P, R, G, w.eps, out=out, residual_out=ro if pat == "rmsnorm" else None,
                             ptrs=ptrs, by_value=opt, pdl=opt)
 
-                def cold_us(opt):
+                def cold_us(opt, dirty=False):
                     for _ in range(10):
                         call(opt)
                     ts = []
                     for _ in range(50):
-                        flush.zero_()
+                        flush.zero_(dirty_only=dirty)
                         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                         a.record(stream)
                         call(opt)
@@ -386,7 +416,7 @@ def sweep(ws, dev, flush, peak):
                     del g
                     return best
 
-                us, us_opt = cold_us(False), cold_us(True)
+                us, us_opt, us_dirty = cold_us(False), cold_us(True), cold_us(False, dirty=True)
                 warm, warm_opt = warm_us(False), warm_us(True)
                 nbytes = ww.bytes_per_call(pat)
                 plan = ws.plan(pat, w.W, M, w.H, torch.bfloat16 if w.dtype == "bf16" else torch.float16)
@@ -394,6 +424,7 @@ def sweep(ws, dev, flush, peak):
                              "bytes": nbytes, "us_cold": round(us, 3), "us_warm_graph": round(warm, 3),
                              "gbs_cold": round(nbytes / us / 1e3, 1), "frac_cold": round(nbytes / us / 1e3 / peak, 4),
                              "us_cold_byvalue_pdl": round(us_opt, 3), "us_warm_graph_byvalue_pdl": round(warm_opt, 3),
+                             "us_cold_write_only_flush": round(us_dirty, 3),
                              "plan": [plan.path, plan.threads, plan.vpt, plan.cluster, plan.grid, plan.w_spec]})
             del inp, P, R, G, out, ro, ptrs
             torch.cuda.empty_cache()
