@@ -125,13 +125,37 @@ __device__ __forceinline__ int warp_run_chunk(int k) {
     return ((((int)threadIdx.x >> 5) * VPT + k) << 5) + ((int)threadIdx.x & 31);
 }
 
-// acc[e] += f32(v[e]), one IEEE binary32 round-to-nearest add per element.
+// acc[e] += f32(v[e]): the 16-bit value widened exactly, then one IEEE
+// binary32 round-to-nearest add. sm_100+ does both in one mixed-precision
+// instruction (add.rn.f32.bf16 / add.rn.f32.f16: 16-bit operand, f32
+// accumulator and result).
+template <typename T>
+struct MixedAdd;
+
+template <>
+struct MixedAdd<__nv_bfloat16> {
+    static __device__ __forceinline__ float add(float acc, unsigned short h) {
+        asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(acc) : "h"(h));
+        return acc;
+    }
+};
+
+template <>
+struct MixedAdd<__half> {
+    static __device__ __forceinline__ float add(float acc, unsigned short h) {
+        asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(acc) : "h"(h));
+        return acc;
+    }
+};
+
 template <typename T>
 __device__ __forceinline__ void accumulate(float acc[8], const uint4& v) {
-    float f[8];
-    Pack8<T>::widen(v, f);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
+    for (int j = 0; j < 4; ++j) {
+        acc[2 * j] = MixedAdd<T>::add(acc[2 * j], (unsigned short)(w[j] & 0xffffu));
+        acc[2 * j + 1] = MixedAdd<T>::add(acc[2 * j + 1], (unsigned short)(w[j] >> 16));
+    }
 }
 
 // Sum of the W partials at chunk c, in rank order, into acc (acc starts at
@@ -303,10 +327,7 @@ __device__ __forceinline__ float row_sum_squares(float ss, float (*s_warp)[kMaxT
 // store residual_out, return the rounded value, accumulate its squares.
 template <typename T>
 __device__ __forceinline__ uint4 residual_chunk(float acc[8], const uint4& rv, uint4* dst, float& ss) {
-    float r[8];
-    Pack8<T>::widen(rv, r);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], r[e]);
+    accumulate<T>(acc, rv);
     const uint4 xs = Pack8<T>::narrow(acc);
     st_out(dst, xs);
     float x[8];

@@ -444,3 +444,29 @@ def test_run_ex_rejects_null_by_value_pointer(ws):
     st = arf.arf_run_ex(ws.handle, opts, AR, 2, [R.data_ptr(), 0], None, None, 0.0, R.data_ptr(), None, 2, 64,
                         arf.ARF_BF16, torch.cuda.current_stream().cuda_stream)
     assert st == arf.ARF_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_every_code_sums_exactly(ws, dtype):
+    """All 65 536 codes (zeros of both signs, subnormals, normals, the
+    largest values, infinities, NaNs) pass through the rank sum and the
+    residual add exactly as in the oracle: widened exactly, added with one
+    binary32 round-to-nearest, rounded once to the I/O type."""
+    d = DT[dtype]
+    allc = np.arange(65536, dtype=np.uint16).reshape(2, 32768)
+    rng = np.random.default_rng(11)
+    partner = pins.nearest_codes(d, rng.standard_normal((2, 32768)) * 2.0 ** rng.integers(-30, 12, (2, 32768)))
+    cases = [[allc], [allc, partner], [partner, allc, partner[::-1].copy()]]
+    for P in cases:
+        Pd = [wl.from_codes(p, dtype).cuda() for p in P]
+        out, _ = arf.run(ws, AR, Pd)
+        ref, _ = oracle.run(oracle.ALLREDUCE, P, dtype=d)
+        torch.cuda.synchronize()
+        assert bitwise_equal(d, wl.codes(out.cpu()), ref).all(), f"W={len(P)}"
+    # every code as the residual
+    G = np.full(32768, pins.exact_codes(d, "1")[0], np.uint16)
+    Pd = [wl.from_codes(partner, dtype).cuda()]
+    out, ro = arf.run(ws, RMS, Pd, wl.from_codes(allc, dtype).cuda(), wl.from_codes(G, dtype).cuda(), 1e-6)
+    ref_out, ref_ro = oracle.run(oracle.AR_RESIDUAL_RMSNORM, [partner], allc, G, 1e-6, dtype=d)
+    torch.cuda.synchronize()
+    assert bitwise_equal(d, wl.codes(ro.cpu()), ref_ro).all()
