@@ -166,13 +166,22 @@ def run(ws: Workspace, pattern, partials, residual=None, gamma=None, eps: float 
 
 
 class HostRunner:
-    """Host-buffer calls (arf_run_host) with a device staging buffer sized
-    for one shape, allocated once by torch and reused by every call."""
+    """Calls on host (page-locked) buffers for one shape.
 
-    def __init__(self, ws: Workspace, pattern, W: int, M: int, H: int, dtype):
+    zero_copy=False: arf_run_host, with a device staging buffer allocated
+    once by torch and reused by every call (copies in, kernel, copies out).
+    zero_copy=True: arf_run on the host buffers themselves, which the kernels
+    read and write over the host link; the pointer array is a page-locked
+    host array kept per set of partials for the runner's lifetime."""
+
+    def __init__(self, ws: Workspace, pattern, W: int, M: int, H: int, dtype, zero_copy: bool = False):
         torch = _torch()
         self.ws, self.pat, self.W, self.M, self.H = ws, pattern_code(pattern), W, M, H
         self.dt = dtype
+        self.zero_copy = zero_copy
+        self._ptr_arrays = {}
+        if zero_copy:
+            return
         self.nbytes = arf_host_staging_bytes(self.pat, W, M, H, dtype_code(dtype))
         if self.nbytes == 0 and M > 0:
             raise ArfError(ARF_ERR_UNSUPPORTED, "arf_host_staging_bytes")
@@ -187,6 +196,20 @@ class HostRunner:
         torch = _torch()
         s = stream if stream is not None else torch.cuda.current_stream(self.ws.device)
         rms = self.pat == ARF_AR_RESIDUAL_RMSNORM
+        if self.zero_copy:
+            key = tuple(p.data_ptr() for p in partials)
+            ptrs = self._ptr_arrays.get(key)
+            if ptrs is None:
+                ptrs = torch.tensor(list(key), dtype=torch.int64).pin_memory()
+                self._ptr_arrays[key] = ptrs
+            st = arf_run(self.ws.handle, self.pat, self.W, ptrs.data_ptr(), residual.data_ptr() if rms else None,
+                         gamma.data_ptr() if rms else None, float(eps), out.data_ptr(),
+                         residual_out.data_ptr() if rms else None, self.M, self.H, dtype_code(self.dt),
+                         s.cuda_stream)
+            if st != ARF_OK:
+                raise ArfError(st, "arf_run (host buffers)",
+                               arf_last_cuda_error(self.ws.handle) if st == ARF_ERR_CUDA else 0)
+            return
         st = arf_run_host(self.ws.handle, self.pat, self.W, [p.data_ptr() for p in partials],
                           residual.data_ptr() if rms else None, gamma.data_ptr() if rms else None, float(eps),
                           out.data_ptr(), residual_out.data_ptr() if rms else None, self.M, self.H,

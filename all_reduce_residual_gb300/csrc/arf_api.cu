@@ -154,12 +154,19 @@ extern "C" int arf_last_cuda_error(arf_workspace_t ws) { return ws ? ws->last_er
 // capability and planning
 // ---------------------------------------------------------------------------
 
-extern "C" arf_status_t arf_supports(arf_workspace_t, arf_pattern_t pattern, int W, int64_t M, int64_t H,
+namespace {
+// Longest kARResidualRMSNorm row a cluster of `max_cluster` CTAs can hold.
+int64_t max_rms_row(int max_cluster) { return (int64_t)ARF_MAX_H_PER_CTA * (max_cluster < 1 ? 1 : max_cluster); }
+}  // namespace
+
+extern "C" arf_status_t arf_supports(arf_workspace_t ws, arf_pattern_t pattern, int W, int64_t M, int64_t H,
                                      arf_dtype_t dtype) {
     if (!valid_pattern(pattern) || !valid_dtype(dtype)) return ARF_ERR_INVALID_ARG;
     if (H <= 0 || M < 0) return ARF_ERR_INVALID_ARG;
     if (W < 1 || W > ARF_MAX_W) return ARF_ERR_UNSUPPORTED;
     if (H % 8 != 0 || H > ARF_MAX_H) return ARF_ERR_UNSUPPORTED;
+    if (pattern == ARF_AR_RESIDUAL_RMSNORM && H > max_rms_row(ws ? ws->caps.max_cluster : 16))
+        return ARF_ERR_UNSUPPORTED;
     // [M,H] indices and the chunk count stay far inside int64
     if (M > ((int64_t)1 << 40) / H) return ARF_ERR_UNSUPPORTED;
     return ARF_OK;
@@ -171,6 +178,7 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
     arf_status_t st = arf_supports(nullptr, pattern, W, M, H, dtype);
     if (st != ARF_OK) return st;
     if (caps->num_sms < 1 || caps->max_threads_per_sm < 32 || caps->max_cluster < 1) return ARF_ERR_INVALID_ARG;
+    if (pattern == ARF_AR_RESIDUAL_RMSNORM && H > max_rms_row(caps->max_cluster)) return ARF_ERR_UNSUPPORTED;
     const int w_spec = arf::w_spec_compiled(W) ? W : 0;
     arf_plan_t pl = {};
     if (pattern == ARF_ALLREDUCE) {
@@ -204,6 +212,15 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
             vpt = 1;
             cs = 2;
             while (cs < 8 && cs < caps->max_cluster && (int64_t)cs * M < 32) cs *= 2;
+        }
+        // Rows longer than one CTA holds (H > 32768): the smallest cluster
+        // that keeps a CTA's slice at <= 2048 chunks (4 per thread), or the
+        // largest the device has.
+        if (C > kMaxThreads * 8) {
+            int big = 2;
+            while (big < caps->max_cluster && big < 16 && ceil_div(C, big) > kMaxThreads * 4) big *= 2;
+            if (big > cs) cs = big;
+            vpt = 1;
         }
         pl = rms_plan(*caps, w_spec, M, H, cs, vpt);
         // The streaming kernel (ARF_PATH_ASYNC) is not chosen: measured on
@@ -304,6 +321,10 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
         (void)cudaGetLastError();
         pl = rms_plan(ws->caps, pl.w_spec, M, H, pl.cluster / 2, pl.vpt);
     }
+    // a fallback that cannot cover the row (a long row on a device that holds
+    // only smaller clusters) is refused rather than launched
+    st = arf_plan_check(&ws->caps, &pl, pattern, W, M, H, dtype);
+    if (st != ARF_OK) return st;
     if (!capturing && pl.path == ARF_PATH_ROW) {
         int b = 0;
         cudaError_t e = max_active_blocks(dtype, pl, H, &b);

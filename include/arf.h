@@ -85,8 +85,11 @@ typedef enum arf_path {
 } arf_path_t;
 
 /* Limits of this build. */
-#define ARF_MAX_W 64      /* ranks: the pages' world sizes {2,...,64}, plus 1 */
-#define ARF_MAX_H 32768   /* hidden size; H must also be a multiple of 8 */
+#define ARF_MAX_W 64        /* ranks: the pages' world sizes {2,...,64}, plus 1 */
+#define ARF_MAX_H 524288    /* hidden size; H must also be a multiple of 8 */
+#define ARF_MAX_H_PER_CTA 32768 /* kARResidualRMSNorm rows longer than this are
+                                   split over a thread-block cluster: H up to
+                                   ARF_MAX_H_PER_CTA x the cluster limit */
 
 /* What the planner needs to know about a device. */
 typedef struct arf_device_caps {
@@ -139,9 +142,11 @@ const char* arf_status_string(arf_status_t status);
 
 /* Whether (pattern, W, M, H, dtype) is handled, judged on the sizes alone in
  * the manner of the supports()/dispatch contract of tokenspeed PR #1075
- * (Summary). ws may be NULL (shape rules only). Returns ARF_OK, or the status
- * arf_run would return for these sizes: W outside [1, ARF_MAX_W], H % 8 != 0,
- * H > ARF_MAX_H -> UNSUPPORTED; H <= 0 or M < 0 or a bad enum -> INVALID_ARG. */
+ * (Summary). ws may be NULL (shape rules only; a 16-CTA cluster limit is
+ * assumed). Returns ARF_OK, or the status arf_run would return for these
+ * sizes: W outside [1, ARF_MAX_W], H % 8 != 0, H > ARF_MAX_H, or (for
+ * kARResidualRMSNorm) H > ARF_MAX_H_PER_CTA x the workspace's cluster limit
+ * -> UNSUPPORTED; H <= 0 or M < 0 or a bad enum -> INVALID_ARG. */
 arf_status_t arf_supports(arf_workspace_t ws, arf_pattern_t pattern, int W,
                           int64_t M, int64_t H, arf_dtype_t dtype);
 
@@ -184,6 +189,11 @@ arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_plan_t* pla
  *   out           [M,H] device, written
  *   residual_out  [M,H] device, written   (kARResidualRMSNorm; else ignored)
  *
+ * Any buffer, and the pointer array, may also be page-locked host memory the
+ * GPU can address (for example from cudaHostAlloc): the kernels then read and
+ * write it in place over the host link, with no staging copies (on
+ * Grace-Blackwell the NVLink-C2C link; measured about twice as fast as
+ * arf_run_host's copies for decode-size calls).
  * Inputs are never modified. residual_out == residual is allowed (in place):
  * each element is read before the same thread overwrites it. out ==
  * residual_out is rejected (INVALID_ARG); other overlaps are undefined.

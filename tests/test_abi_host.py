@@ -62,10 +62,11 @@ def test_supports_rules(pattern):
     assert S(None, pattern, 8, 2048, 7168, bf) == arf.ARF_OK
     assert S(None, pattern, 1, 0, 8, arf.ARF_FP16) == arf.ARF_OK
     assert S(None, pattern, 64, 1, 32768, bf) == arf.ARF_OK
+    assert S(None, pattern, 8, 3, 65536, bf) == arf.ARF_OK
     assert S(None, pattern, 0, 1, 8, bf) == arf.ARF_ERR_UNSUPPORTED
     assert S(None, pattern, 65, 1, 8, bf) == arf.ARF_ERR_UNSUPPORTED
     assert S(None, pattern, 2, 1, 12, bf) == arf.ARF_ERR_UNSUPPORTED      # H % 8
-    assert S(None, pattern, 2, 1, 32776, bf) == arf.ARF_ERR_UNSUPPORTED   # H > max
+    assert S(None, pattern, 2, 1, 524296, bf) == arf.ARF_ERR_UNSUPPORTED  # H > max
     assert S(None, pattern, 2, 1, 0, bf) == arf.ARF_ERR_INVALID_ARG
     assert S(None, pattern, 2, -1, 8, bf) == arf.ARF_ERR_INVALID_ARG
     assert S(None, pattern, 2, 1, 8, 7) == arf.ARF_ERR_INVALID_ARG
@@ -122,6 +123,35 @@ def test_planner_uses_the_sm_count():
     no_cluster = arf.DeviceCaps(152, 1, 2048, 232448)
     arf.arf_plan_for_caps(no_cluster, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 1, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and p.grid == 1
+
+
+@pytest.mark.parametrize("H", [32776, 65536, 131072, 262144, 524288])
+@pytest.mark.parametrize("M", [1, 7, 300])
+def test_long_rows_split_over_clusters(H, M):
+    """Rows longer than one CTA holds: kARResidualRMSNorm splits them over a
+    cluster (up to 16 CTAs); kAllReduce is flat and takes any H <= ARF_MAX_H."""
+    p = arf.Plan()
+    assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+    assert p.path == arf.ARF_PATH_CLUSTER and p.threads <= 512
+    assert p.threads * p.vpt * p.cluster >= H // 8
+    assert arf.arf_plan_check(GB300, p, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16) == arf.ARF_OK
+    assert arf.arf_plan_for_caps(GB300, arf.ARF_ALLREDUCE, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+    # a device with 4-CTA clusters holds rows up to 4 x 32768
+    small = arf.DeviceCaps(152, 4, 2048, 232448)
+    want = arf.ARF_OK if H <= 4 * 32768 else arf.ARF_ERR_UNSUPPORTED
+    assert arf.arf_plan_for_caps(small, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == want
+
+
+def test_long_row_limits():
+    S = arf.arf_supports
+    assert S(None, arf.ARF_ALLREDUCE, 2, 1, 524288, arf.ARF_BF16) == arf.ARF_OK
+    assert S(None, arf.ARF_AR_RESIDUAL_RMSNORM, 2, 1, 524288, arf.ARF_BF16) == arf.ARF_OK
+    assert S(None, arf.ARF_ALLREDUCE, 2, 1, 524296, arf.ARF_BF16) == arf.ARF_ERR_UNSUPPORTED
+    no_cluster = arf.DeviceCaps(152, 1, 2048, 232448)
+    p = arf.Plan()
+    assert arf.arf_plan_for_caps(no_cluster, arf.ARF_AR_RESIDUAL_RMSNORM, 2, 1, 32776, arf.ARF_BF16, p) == \
+        arf.ARF_ERR_UNSUPPORTED
+    assert arf.arf_plan_for_caps(no_cluster, arf.ARF_ALLREDUCE, 2, 1, 524288, arf.ARF_BF16, p) == arf.ARF_OK
 
 
 def test_plan_check_rejects_bad_plans():

@@ -1,0 +1,76 @@
+"""Seeded random cases on the GPU against the oracle: random rank counts,
+shapes (ragged ones included), dtypes, patterns, value scales, and either the
+planner's plan or a random legal plan of any kernel shape."""
+import numpy as np
+import pytest
+import torch
+
+import all_reduce_residual_gb300 as arf
+from all_reduce_residual_gb300 import workloads as wl
+from gpu_util import DT, assert_parity, gpu_run, oracle_run, to_device
+
+pytestmark = pytest.mark.gpu
+RMS, AR = arf.ARF_AR_RESIDUAL_RMSNORM, arf.ARF_ALLREDUCE
+
+
+@pytest.fixture(scope="module")
+def ws():
+    with arf.Workspace(0) as w:
+        yield w
+
+
+def random_plan(rng, ws, pattern, W, M, H, dtype):
+    """A random plan that arf_plan_check accepts (or None for the planner's)."""
+    caps = ws.caps
+    if rng.random() < 0.4:
+        return None
+    ws_choices = [0] + ([W] if W in (1, 2, 4, 8, 16) else [])
+    for _ in range(50):
+        w_spec = int(rng.choice(ws_choices))
+        if pattern == AR:
+            p = arf.Plan(path=arf.ARF_PATH_FLAT, threads=int(rng.choice([32, 64, 128, 256, 512])),
+                         vpt=int(rng.choice([1, 2, 4])), cluster=1, grid=int(rng.integers(1, 2000)), w_spec=w_spec)
+        else:
+            kind = rng.integers(0, 3)
+            C = H // 8
+            if kind == 2 and W in (1, 2, 4, 8, 16):
+                p = arf.Plan(path=arf.ARF_PATH_ASYNC, threads=256, vpt=1, cluster=1,
+                             grid=int(rng.integers(1, 200)), w_spec=W, stages=int(rng.integers(2, 9)))
+            else:
+                cs = 1 if kind == 0 else int(rng.choice([2, 4, 8, 16]))
+                vpt = int(rng.choice([1, 2, 4, 8]))
+                per = -(-(-(-C // cs)) // vpt)
+                threads = max(32, -(-per // 32) * 32)
+                p = arf.Plan(path=arf.ARF_PATH_ROW if cs == 1 else arf.ARF_PATH_CLUSTER, threads=threads, vpt=vpt,
+                             cluster=cs, grid=cs * int(rng.integers(1, 300)), w_spec=w_spec)
+        if arf.arf_plan_check(caps, p, pattern, W, M, H, arf.dtype_code(wl.TORCH_DTYPE[dtype])) == arf.ARF_OK:
+            return p
+    return None
+
+
+@pytest.mark.parametrize("case", range(60))
+def test_fuzz(ws, case):
+    rng = np.random.default_rng(1000 + case)
+    W = int(rng.choice([1, 2, 3, 4, 5, 8, 12, 16, 17, 31, 32, 64]))
+    M = int(rng.choice([0, 1, 2, 5, 16, 33, 150, 300]))
+    H = 8 * int(rng.choice([1, 3, 64, 125, 512, 896, 1000, 1025, 4096]))
+    dtype = str(rng.choice(["bf16", "fp16"]))
+    sigma = float(rng.choice([1e-3, 0.3, 1.0, 40.0]))
+    eps = float(rng.choice([0.0, 1e-6, 1e-2]))
+    pattern = int(rng.choice([AR, RMS]))
+    inp = wl.make_inputs(wl.custom(W, M, H, dtype, sigma, eps, config_id=2000 + case))
+    P, R, G = to_device(inp)
+    plan = random_plan(rng, ws, pattern, W, M, H, dtype)
+    if M == 0:
+        out, _ = arf.run(ws, pattern, P, R, G, eps, plan=plan)
+        return
+    try:
+        got = gpu_run(ws, pattern, P, R, G, eps, plan=plan)
+    except arf.ArfError as e:  # a cluster or ring shape this device cannot keep resident
+        assert plan is not None and (plan.cluster > 1 or plan.stages > 0) and e.status == arf.ARF_ERR_UNSUPPORTED
+        return
+    if eps == 0.0 and pattern == RMS:
+        # an all-zero row would give NaN in both; the seeded data has none
+        pass
+    assert_parity(DT[dtype], pattern, got, oracle_run(pattern, inp), f"case {case}: W={W} M={M} H={H} {dtype} {plan}")
+    torch.cuda.synchronize()

@@ -122,7 +122,8 @@ def test_generic_rank_counts(ws, W, pattern):
     check(ws, pattern, inputs(W, 3, 264, "bf16" if W % 2 else "fp16", sigma=0.3), what=f"W={W}")
 
 
-@pytest.mark.parametrize("M,H", [(1, 8), (1, 32768), (2500, 64), (5000, 8), (3, 7176)])
+@pytest.mark.parametrize("M,H", [(1, 8), (1, 32768), (2500, 64), (5000, 8), (3, 7176), (3, 32776), (2, 65536),
+                                 (40, 40960), (2, 262144), (1, 524288)])
 @pytest.mark.parametrize("pattern", [AR, RMS])
 def test_ragged_and_extreme_shapes(ws, M, H, pattern):
     check(ws, pattern, inputs(4, M, H), what=f"M={M} H={H}")
@@ -275,7 +276,7 @@ def test_rejected_calls_write_nothing(ws):
     assert call(W=0) == arf.ARF_ERR_UNSUPPORTED
     assert call(W=65) == arf.ARF_ERR_UNSUPPORTED
     assert call(h=12) == arf.ARF_ERR_UNSUPPORTED
-    assert call(h=32776) == arf.ARF_ERR_UNSUPPORTED
+    assert call(h=524296) == arf.ARF_ERR_UNSUPPORTED
     assert call(m=-1) == arf.ARF_ERR_INVALID_ARG
     assert call(pp=None) == arf.ARF_ERR_INVALID_ARG
     assert call(res=None) == arf.ARF_ERR_INVALID_ARG
@@ -470,3 +471,29 @@ def test_every_code_sums_exactly(ws, dtype):
     ref_out, ref_ro = oracle.run(oracle.AR_RESIDUAL_RMSNORM, [partner], allc, G, 1e-6, dtype=d)
     torch.cuda.synchronize()
     assert bitwise_equal(d, wl.codes(ro.cpu()), ref_ro).all()
+
+
+@pytest.mark.parametrize("name,M", [("small", 8), ("llama_tp2", 128), ("k3_tp8", 64), ("tp16_8mib", 32)])
+def test_zero_copy_host_buffers(ws, name, M):
+    """arf_run directly on page-locked host buffers (kernels read and write
+    host memory in place): same results as on device buffers, in place too."""
+    w = wl.WORKLOADS[name].with_m(M)
+    inp = wl.make_inputs(w)
+    d = DT[w.dtype]
+    P = [p.pin_memory() for p in inp.partials]
+    R, G = inp.residual.pin_memory(), inp.gamma.pin_memory()
+    for pat in (AR, RMS):
+        out = torch.empty_like(R).pin_memory()
+        ro = torch.empty_like(R).pin_memory()
+        runner = arf.HostRunner(ws, pat, w.W, M, w.H, P[0].dtype, zero_copy=True)
+        runner(P, R, G, w.eps, out, ro)
+        torch.cuda.synchronize()
+        got = (wl.codes(out), wl.codes(ro) if pat == RMS else None)
+        assert_parity(d, pat, got, oracle_run(pat, inp), f"{name} zero-copy")
+    # in place on host memory: residual_out is the residual buffer
+    Rin = inp.residual.clone().pin_memory()
+    out = torch.empty_like(R).pin_memory()
+    HostRunner = arf.HostRunner(ws, RMS, w.W, M, w.H, P[0].dtype, zero_copy=True)
+    HostRunner(P, Rin, G, w.eps, out, Rin)
+    torch.cuda.synchronize()
+    assert_parity(d, RMS, (wl.codes(out), wl.codes(Rin)), oracle_run(RMS, inp), f"{name} zero-copy in place")
