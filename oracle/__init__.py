@@ -91,6 +91,13 @@ class Oracle:
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
         ]
         L.arf_oracle_run.restype = ctypes.c_int
+        L.arf_oracle_run_general.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int,
+        ]
+        L.arf_oracle_run_general.restype = ctypes.c_int
         self.lib = L
         self.path = path
 
@@ -163,6 +170,50 @@ class Oracle:
         return out, residual_out
 
 
+F32 = 2  # partial dtype code for binary32 partials
+
+
+def _rows(a, name, H=None):
+    """(row stride in elements, array) of a 2-D array whose rows may be wider
+    than H (a column slice of a wider array); elements must be contiguous."""
+    if a.ndim != 2 or a.strides[1] != a.itemsize or a.strides[0] % a.itemsize:
+        raise ValueError(f"{name}: rows must be contiguous")
+    return a.strides[0] // a.itemsize
+
+
+def run_general_with(o, pattern, partials, residual=None, gamma=None, eps=0.0, dtype=BF16, out=None,
+                     residual_out=None):
+    """The general entry point: partials are uint16 codes or float32 arrays
+    of shape [M, H], possibly column slices of wider arrays (row strides are
+    read from the arrays); out / residual_out likewise (allocated contiguous
+    when None). Returns (out, residual_out)."""
+    P = list(partials)
+    M, H = P[0].shape
+    pdtype = F32 if P[0].dtype == np.float32 else dtype
+    ldp = _rows(P[0], "partials")
+    for p in P:
+        if p.shape != (M, H) or p.dtype != P[0].dtype or _rows(p, "partials") != ldp:
+            raise ValueError("partials must share shape, dtype and row stride")
+    ptrs = (ctypes.c_void_p * len(P))(*[p.ctypes.data for p in P])
+    if out is None:
+        out = np.empty((M, H), np.uint16)
+    r_ptr = g_ptr = ro_ptr = None
+    ldr = ldro = H
+    if pattern == AR_RESIDUAL_RMSNORM:
+        if residual_out is None:
+            residual_out = np.empty((M, H), np.uint16)
+        ldr, ldro = _rows(residual, "residual"), _rows(residual_out, "residual_out")
+        G = _u16(gamma).reshape(H)
+        r_ptr, g_ptr, ro_ptr = residual.ctypes.data, G.ctypes.data, residual_out.ctypes.data
+    rc = o.lib.arf_oracle_run_general(pattern, len(P), ptrs, pdtype, ldp, r_ptr, ldr, g_ptr, float(eps),
+                                      out.ctypes.data, _rows(out, "out"), ro_ptr, ldro, M, H, dtype)
+    if rc != 0:
+        raise ValueError(f"arf_oracle_run_general rejected its arguments (rc={rc})")
+    return out, residual_out
+
+
+Oracle.run_general = run_general_with
+
 _default = None
 
 
@@ -192,3 +243,7 @@ def inv_rms(dtype, x_row, eps):
 
 def run(pattern, partials, residual=None, gamma=None, eps=0.0, dtype=BF16, residual_out=None):
     return default().run(pattern, partials, residual, gamma, eps, dtype, residual_out)
+
+
+def run_general(pattern, partials, residual=None, gamma=None, eps=0.0, dtype=BF16, out=None, residual_out=None):
+    return default().run_general(pattern, partials, residual, gamma, eps, dtype, out, residual_out)

@@ -159,50 +159,71 @@ double arf_oracle_inv_rms(int dtype, const uint16_t* x, int64_t H, float eps,
     return 1.0 / sqrt(ss / (double)H + (double)eps);
 }
 
-int arf_oracle_run(int pattern, int W, const void* const* partials,
-                   const void* residual, const void* gamma, float eps,
-                   void* out, void* residual_out, int64_t M, int64_t H,
-                   int dtype)
+/* Value of partial element i of rank r: 16-bit codes of the I/O dtype, or
+ * binary32 as stored (pdtype 2). */
+static float partial_at(const void* p, int pdtype, int dtype, int64_t i)
+{
+    if (pdtype == 2) return ((const float*)p)[i];
+    return arf_oracle_widen(dtype, ((const uint16_t*)p)[i]);
+}
+
+int arf_oracle_run_general(int pattern, int W, const void* const* partials, int pdtype, int64_t ld_partials,
+                           const void* residual, int64_t ld_residual, const void* gamma, float eps,
+                           void* out, int64_t ld_out, void* residual_out, int64_t ld_residual_out,
+                           int64_t M, int64_t H, int dtype)
 {
     if (pattern != 0 && pattern != 1) return 1;
     if (dtype != 0 && dtype != 1) return 1;
+    if (pdtype != dtype && pdtype != 2) return 1;
     if (W < 1 || M < 0 || H < 1) return 1;
+    if (ld_partials < H || ld_out < H) return 1;
     if (partials == NULL || out == NULL) return 1;
     for (int r = 0; r < W; ++r)
         if (partials[r] == NULL) return 1;
-    if (pattern == 1 && (residual == NULL || gamma == NULL || residual_out == NULL))
-        return 1;
+    if (pattern == 1) {
+        if (residual == NULL || gamma == NULL || residual_out == NULL) return 1;
+        if (ld_residual < H || ld_residual_out < H) return 1;
+    }
 
-    const uint16_t* const* P = (const uint16_t* const*)partials;
     const uint16_t* R = (const uint16_t*)residual;
     const uint16_t* G = (const uint16_t*)gamma;
     uint16_t* O = (uint16_t*)out;
     uint16_t* RO = (uint16_t*)residual_out;
 
     for (int64_t m = 0; m < M; ++m) {
-        const int64_t base = m * H;
+        const int64_t pb = m * ld_partials, ob = m * ld_out;
+        const int64_t rb = m * ld_residual, rob = m * ld_residual_out;
 
         /* Cross-rank sum, binary32, ranks in the order given. */
         for (int64_t i = 0; i < H; ++i) {
             float acc = 0.0f;
-            for (int r = 0; r < W; ++r) acc = acc + arf_oracle_widen(dtype, P[r][base + i]);
+            for (int r = 0; r < W; ++r) acc = acc + partial_at(partials[r], pdtype, dtype, pb + i);
             if (pattern == 0) {
-                O[base + i] = arf_oracle_narrow_f32(dtype, acc);
+                O[ob + i] = arf_oracle_narrow_f32(dtype, acc);
             } else {
                 /* Residual add on the unrounded sum: one rounding in total. */
-                float t = acc + arf_oracle_widen(dtype, R[base + i]);
-                RO[base + i] = arf_oracle_narrow_f32(dtype, t);
+                float t = acc + arf_oracle_widen(dtype, R[rb + i]);
+                RO[rob + i] = arf_oracle_narrow_f32(dtype, t);
             }
         }
         if (pattern == 0) continue;
 
         /* RMSNorm of the stored residual_out row. */
-        double inv = arf_oracle_inv_rms(dtype, RO + base, H, eps, NULL);
+        double inv = arf_oracle_inv_rms(dtype, RO + rob, H, eps, NULL);
         for (int64_t i = 0; i < H; ++i) {
-            double x = (double)arf_oracle_widen(dtype, RO[base + i]);
+            double x = (double)arf_oracle_widen(dtype, RO[rob + i]);
             double g = (double)arf_oracle_widen(dtype, G[i]);
-            O[base + i] = arf_oracle_narrow_f64(dtype, x * inv * g);
+            O[ob + i] = arf_oracle_narrow_f64(dtype, x * inv * g);
         }
     }
     return 0;
+}
+
+int arf_oracle_run(int pattern, int W, const void* const* partials,
+                   const void* residual, const void* gamma, float eps,
+                   void* out, void* residual_out, int64_t M, int64_t H,
+                   int dtype)
+{
+    return arf_oracle_run_general(pattern, W, partials, dtype, H, residual, H, gamma, eps, out, H,
+                                  residual_out, H, M, H, dtype);
 }

@@ -39,6 +39,15 @@ void arf_oracle_narrow_f64_n(int dtype, const double* in, uint16_t* out, int64_t
 double arf_oracle_inv_rms(int dtype, const uint16_t* x, int64_t H, float eps,
                           double* ss_out);
 
+/* The epilogue with general layouts: every [M,H] tensor has its own row
+ * stride (in elements, >= H), and the partials may be binary32 (pdtype 2)
+ * instead of the I/O dtype (pdtype == dtype). binary32 partials enter the
+ * binary32 rank-order sum as they are. Same return convention as below. */
+int arf_oracle_run_general(int pattern, int W, const void* const* partials, int pdtype, int64_t ld_partials,
+                           const void* residual, int64_t ld_residual, const void* gamma, float eps,
+                           void* out, int64_t ld_out, void* residual_out, int64_t ld_residual_out,
+                           int64_t M, int64_t H, int dtype);
+
 /* The epilogue on host buffers.
  *   partials: host array of W host pointers, each to an [M,H] tensor.
  *   kAllReduce writes out only; residual, gamma, residual_out may be NULL.

@@ -277,7 +277,7 @@ def check_exact_tiny(o, trials=150, seed=3):
         dtype = BF16 if t % 2 == 0 else FP16
         W = int(rng.choice([1, 2, 3, 5, 8]))
         M = int(rng.integers(1, 4))
-        H = int(rng.choice([8, 16, 24]))
+        H = int(rng.choice([1, 3, 8, 13, 16, 24]))
         sigma = float(rng.choice([0.01, 0.5, 3.0, 100.0]))
         eps32 = np.float32(rng.choice([1e-6, 1e-5, 0.1]))
         P = [_draw(rng, dtype, (M, H), sigma) for _ in range(W)]
@@ -392,12 +392,84 @@ def check_invariants(o, names=tuple(SMALL_M)):
         assert not out_z.any() and not ro_z.any(), f"{name} inv7 zero row"
 
 
+# ---------------------------------------------------------------------------
+# General layouts: row strides and binary32 partials
+# ---------------------------------------------------------------------------
+
+
+def _widen_rows(a, H, pad, fill):
+    """a [M,H] array embedded in a wider [M,H+pad] array filled with `fill`;
+    returns the [M,H] column view."""
+    M = a.shape[0]
+    big = np.full((M, H + pad), fill, dtype=a.dtype)
+    big[:, :H] = a
+    return big[:, :H], big
+
+
+def check_strided(o, trials=12, seed=5):
+    """Rows embedded in wider buffers (garbage in the padding) give the
+    contiguous results, and the padding of the outputs is left untouched."""
+    rng = np.random.default_rng(seed)
+    for t in range(trials):
+        dtype = BF16 if t % 2 == 0 else FP16
+        W, M, H = int(rng.integers(1, 6)), int(rng.integers(1, 5)), int(rng.choice([1, 5, 8, 24, 40]))
+        P = [_draw(rng, dtype, (M, H), 2.0) for _ in range(W)]
+        R = _draw(rng, dtype, (M, H), 1.0)
+        G = nearest_codes(dtype, 0.5 + rng.random(H))
+        for pat in (ALLREDUCE, RMSNORM):
+            want = o.run(pat, P, R, G, 1e-6, dtype=dtype)
+            pads = [int(x) for x in rng.integers(1, 9, size=4)]
+            junk = np.uint16(0x7F81 if dtype == BF16 else 0x7C01)  # NaN codes: any read of them shows
+            Ps, bigs = [], []
+            for p in P:
+                v, b = _widen_rows(p, H, pads[0], junk)
+                Ps.append(v)
+                bigs.append(b)
+            # one shared row stride for all partials
+            Ps = [b[:, :H] for b in bigs]
+            Rv, _ = _widen_rows(R, H, pads[1], junk)
+            Ov, Ob = _widen_rows(np.zeros((M, H), np.uint16), H, pads[2], np.uint16(0x1234))
+            ROv, ROb = _widen_rows(np.zeros((M, H), np.uint16), H, pads[3], np.uint16(0x1234))
+            out, ro = o.run_general(pat, Ps, Rv, G, 1e-6, dtype=dtype, out=Ov, residual_out=ROv)
+            assert_codes_equal(dtype, out, want[0], f"strided trial {t} out")
+            assert (Ob[:, H:] == 0x1234).all(), "strided out: padding written"
+            if pat == RMSNORM:
+                assert_codes_equal(dtype, ro, want[1], f"strided trial {t} residual_out")
+                assert (ROb[:, H:] == 0x1234).all(), "strided residual_out: padding written"
+
+
+def check_f32_partials(o, trials=40, seed=6):
+    """binary32 partials: the rank-order sum of numpy float32 values, then the
+    residual add, one rounding; out by exact rationals. Odd H included."""
+    rng = np.random.default_rng(seed)
+    for t in range(trials):
+        dtype = BF16 if t % 2 == 0 else FP16
+        W, M = int(rng.integers(1, 7)), int(rng.integers(1, 4))
+        H = int(rng.choice([1, 3, 7, 8, 13, 24]))
+        top = 10.0 if dtype == FP16 else 20.0
+        P32 = [(rng.standard_normal((M, H)) * 2.0 ** rng.uniform(-6, top)).astype(np.float32) for _ in range(W)]
+        if t % 4 == 1 and W >= 3:  # cancellation: exact only in array order
+            P32[1] = -P32[0]
+        R = _draw(rng, dtype, (M, H), 1.0)
+        G = nearest_codes(dtype, 0.5 + rng.random(H))
+        eps32 = np.float32(1e-6)
+        out, _ = o.run_general(ALLREDUCE, P32, dtype=dtype)
+        assert_codes_equal(dtype, out, nearest_codes(dtype, ref_sum_f32(P32).astype(np.float64)),
+                           f"f32 trial {t} allreduce")
+        out, ro = o.run_general(RMSNORM, P32, R, G, float(eps32), dtype=dtype)
+        want_ro = nearest_codes(dtype, ref_sum_f32(P32, lib_decode(dtype, R)).astype(np.float64))
+        assert_codes_equal(dtype, ro, want_ro, f"f32 trial {t} residual_out")
+        assert_codes_equal(dtype, out, ref_rmsnorm_exact(dtype, want_ro, G, eps32), f"f32 trial {t} out")
+
+
 def run_battery(o, quick=False):
     """Every pin, in an order that fails fast on the cheap ones."""
     check_worked_rows(o)
     check_inv_rms_r2(o)
     check_one_rounding(o)
     check_exact_tiny(o, trials=40 if quick else 150)
+    check_strided(o, trials=6 if quick else 12)
+    check_f32_partials(o, trials=16 if quick else 40)
     check_widen(o)
     check_roundtrip(o)
     check_narrow_f32(o, n=100_000 if quick else 1_000_000)

@@ -16,27 +16,30 @@ MUTANTS = {
     "eps_outside_root": ("1.0 / sqrt(ss / (double)H + (double)eps)", "1.0 / (sqrt(ss / (double)H) + (double)eps)"),
     "no_sqrt": ("1.0 / sqrt(ss / (double)H + (double)eps)", "1.0 / (ss / (double)H + (double)eps)"),
     "round_sum_before_residual": (
-        "float t = acc + arf_oracle_widen(dtype, R[base + i]);",
-        "float t = arf_oracle_widen(dtype, arf_oracle_narrow_f32(dtype, acc)) + arf_oracle_widen(dtype, R[base + i]);"),
+        "float t = acc + arf_oracle_widen(dtype, R[rb + i]);",
+        "float t = arf_oracle_widen(dtype, arf_oracle_narrow_f32(dtype, acc)) + arf_oracle_widen(dtype, R[rb + i]);"),
     "low_precision_running_sum": (
-        "acc = acc + arf_oracle_widen(dtype, P[r][base + i]);",
-        "acc = arf_oracle_widen(dtype, arf_oracle_narrow_f32(dtype, acc + arf_oracle_widen(dtype, P[r][base + i])));"),
+        "acc = acc + partial_at(partials[r], pdtype, dtype, pb + i);",
+        "acc = arf_oracle_widen(dtype, arf_oracle_narrow_f32(dtype, acc + partial_at(partials[r], pdtype, dtype, pb + i)));"),
     "reversed_rank_order": ("for (int r = 0; r < W; ++r) acc", "for (int r = W - 1; r >= 0; --r) acc"),
     "dropped_last_rank": ("for (int r = 0; r < W; ++r) acc", "for (int r = 0; r < W - (W > 1); ++r) acc"),
     "residual_sign": ("float t = acc + arf_oracle_widen", "float t = acc - arf_oracle_widen"),
     "gamma_reversed": ("G[i]", "G[H - 1 - i]"),
+    "residual_row_stride_ignored": ("const int64_t rb = m * ld_residual", "const int64_t rb = m * H"),
+    "partial_row_stride_ignored": ("const int64_t pb = m * ld_partials", "const int64_t pb = m * H"),
+    "f32_partials_read_as_16_bit": ("if (pdtype == 2) return ((const float*)p)[i];", ""),
     "gamma_dropped": ("x * inv * g", "x * inv"),
     "x_misread_in_norm": (
-        "double x = (double)arf_oracle_widen(dtype, RO[base + i]);",
-        "double x = (double)arf_oracle_widen(dtype, RO[base + i]) * (1.0 + 1e-3 * (i == 0));"),
+        "double x = (double)arf_oracle_widen(dtype, RO[rob + i]);",
+        "double x = (double)arf_oracle_widen(dtype, RO[rob + i]) * (1.0 + 1e-3 * (i == 0));"),
     "ties_away_from_zero": ("(rem == 0.5 && fmod(kf, 2.0) != 0.0)", "(rem == 0.5)"),
     "truncating_narrow": ("if (rem > 0.5 || (rem == 0.5 && fmod(kf, 2.0) != 0.0)) kf += 1.0;", ""),
     "overflow_one_binade_early": ("if (E > f->emax) return sign | inf;", "if (E >= f->emax) return sign | inf;"),
     "f16_subnormal_scale": ("v = ldexp((double)man, -24);", "v = ldexp((double)man, -25);"),
     "f16_normal_bias": ("(int)ex - 25", "(int)ex - 24"),
     "double_rounding_out": (
-        "O[base + i] = arf_oracle_narrow_f64(dtype, x * inv * g);",
-        "O[base + i] = arf_oracle_narrow_f32(dtype, (float)(x * inv * g));"),
+        "O[ob + i] = arf_oracle_narrow_f64(dtype, x * inv * g);",
+        "O[ob + i] = arf_oracle_narrow_f32(dtype, (float)(x * inv * g));"),
     "subnormal_quantum_unclamped": ("if (E < f->emin) E = f->emin;", ""),
     "nan_becomes_inf": ("if (isnan(v)) return sign | f->qnan;", ""),
 }

@@ -31,6 +31,14 @@ def test_exact_tiny_bruteforce(orc):
     pins.check_exact_tiny(orc)
 
 
+def test_strided_rows(orc):
+    pins.check_strided(orc)
+
+
+def test_f32_partials_bruteforce(orc):
+    pins.check_f32_partials(orc)
+
+
 def test_widen_exhaustive(orc):
     pins.check_widen(orc)
 
