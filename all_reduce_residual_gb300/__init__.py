@@ -11,7 +11,7 @@ import ctypes
 
 from ._binding import (  # noqa: F401  (re-exported C-ABI names)
     ARF_AR_RESIDUAL_RMSNORM, ARF_ALLREDUCE, ARF_BF16, ARF_ERR_CUDA, ARF_ERR_DEVICE_MISMATCH,
-    ARF_ERR_INVALID_ARG, ARF_ERR_UNSUPPORTED, ARF_FP16, ARF_MAX_H, ARF_MAX_W, ARF_OK, ARF_PATH_ASYNC, ARF_PATH_CLUSTER,
+    ARF_ERR_INVALID_ARG, ARF_ERR_UNSUPPORTED, ARF_FP16, ARF_MAX_H, ARF_MAX_W, ARF_OK, ARF_PATH_ASYNC, ARF_PATH_CLUSTER, ARF_PATH_ELEM,
     ARF_PATH_FLAT, ARF_PATH_ROW, ARF_STATIC_STAGING_BYTES, ArfError, DeviceCaps, Plan, RunOpts,
     arf_host_staging_bytes, arf_last_cuda_error, arf_plan_check, arf_plan_for_caps, arf_run, arf_run_ex,
     arf_run_host, arf_run_host_static, arf_run_planned, arf_status_string, arf_supports,
@@ -93,14 +93,21 @@ def pointer_array(tensors, device=None):
 
 
 def _check_operand(t, name, shape, dtype, device):
+    """Returns the row stride in elements ([M,H] tensors may be row-strided
+    views whose elements are contiguous within a row)."""
     if t.dtype != dtype:
         raise ValueError(f"{name}: dtype {t.dtype} != {dtype}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
     if t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if len(shape) == 1 or shape[0] <= 1:
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        return shape[-1]
+    if t.stride(1) != 1 or t.stride(0) < shape[1]:
+        raise ValueError(f"{name}: rows must be contiguous with a row stride >= H")
+    return t.stride(0)
 
 
 def run(ws: Workspace, pattern, partials, residual=None, gamma=None, eps: float = 0.0, out=None,
@@ -122,28 +129,39 @@ def run(ws: Workspace, pattern, partials, residual=None, gamma=None, eps: float 
     if W == 0:
         raise ValueError("at least one partial is required")
     M, H = P[0].shape
-    dev, dt = P[0].device, P[0].dtype
-    for i, p in enumerate(P):
-        _check_operand(p, f"partials[{i}]", (M, H), dt, dev)
+    dev, pdt = P[0].device, P[0].dtype
+    f32p = pdt == torch.float32
     rms = pat == ARF_AR_RESIDUAL_RMSNORM
+    # the I/O dtype: the partials' own, or (binary32 partials) that of the other tensors
+    dt = pdt if not f32p else (residual.dtype if rms and residual is not None else
+                               (out.dtype if out is not None else torch.bfloat16))
+    ldp = None
+    for i, p in enumerate(P):
+        ld = _check_operand(p, f"partials[{i}]", (M, H), pdt, dev)
+        if ldp is not None and ld != ldp:
+            raise ValueError("all partials must have the same row stride")
+        ldp = ld
     if out is None:
         out = torch.empty((M, H), dtype=dt, device=dev)
-    _check_operand(out, "out", (M, H), dt, dev)
+    ldo = _check_operand(out, "out", (M, H), dt, dev)
     r_ptr = g_ptr = ro_ptr = None
+    ldr = ldro = H
     if rms:
         if residual is None or gamma is None:
             raise ValueError("kARResidualRMSNorm needs residual and gamma")
-        _check_operand(residual, "residual", (M, H), dt, dev)
+        ldr = _check_operand(residual, "residual", (M, H), dt, dev)
         _check_operand(gamma, "gamma", (H,), dt, dev)
         if residual_out is None:
             residual_out = torch.empty((M, H), dtype=dt, device=dev)
-        _check_operand(residual_out, "residual_out", (M, H), dt, dev)
+        ldro = _check_operand(residual_out, "residual_out", (M, H), dt, dev)
         r_ptr, g_ptr, ro_ptr = residual.data_ptr(), gamma.data_ptr(), residual_out.data_ptr()
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     tail = (r_ptr, g_ptr, float(eps), out.data_ptr(), ro_ptr, M, H, dtype_code(dt), s.cuda_stream)
-    if by_value or pdl:
+    general = f32p or (ldp, ldr, ldo, ldro) != (H, H, H, H)
+    if by_value or pdl or general:
         opts = RunOpts(plan=ctypes.pointer(plan) if plan is not None else None, partials_by_value=int(by_value),
-                       pdl=int(pdl))
+                       pdl=int(pdl), ld_partials=ldp, ld_residual=ldr, ld_out=ldo, ld_residual_out=ldro,
+                       partials_f32=int(f32p))
         if by_value:
             parts = [p.data_ptr() for p in P]
         else:

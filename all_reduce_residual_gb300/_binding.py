@@ -31,6 +31,7 @@ ARF_PATH_FLAT = 0
 ARF_PATH_ROW = 1
 ARF_PATH_CLUSTER = 2
 ARF_PATH_ASYNC = 3
+ARF_PATH_ELEM = 4
 ARF_MAX_W = 64
 ARF_MAX_H = 32768
 ARF_STATIC_STAGING_BYTES = 16 << 20
@@ -61,7 +62,9 @@ class Plan(ctypes.Structure):
 
 
 class RunOpts(ctypes.Structure):
-    _fields_ = [("plan", ctypes.POINTER(Plan)), ("partials_by_value", ctypes.c_int), ("pdl", ctypes.c_int)]
+    _fields_ = [("plan", ctypes.POINTER(Plan)), ("partials_by_value", ctypes.c_int), ("pdl", ctypes.c_int),
+                ("ld_partials", ctypes.c_int64), ("ld_residual", ctypes.c_int64), ("ld_out", ctypes.c_int64),
+                ("ld_residual_out", ctypes.c_int64), ("partials_f32", ctypes.c_int)]
 
 
 _c = ctypes

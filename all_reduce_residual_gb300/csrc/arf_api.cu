@@ -157,6 +157,31 @@ extern "C" int arf_last_cuda_error(arf_workspace_t ws) { return ws ? ws->last_er
 namespace {
 // Longest kARResidualRMSNorm row a cluster of `max_cluster` CTAs can hold.
 int64_t max_rms_row(int max_cluster) { return (int64_t)ARF_MAX_H_PER_CTA * (max_cluster < 1 ? 1 : max_cluster); }
+
+// The elementwise kernels' plan: kAllReduce tiles of 256 elements, up to a
+// device-full of CTAs; kARResidualRMSNorm one CTA per row, up to 512 threads.
+arf_plan_t elem_plan(const arf_device_caps_t& caps, arf_pattern_t pattern, int64_t M, int64_t H) {
+    arf_plan_t pl = {};
+    pl.path = ARF_PATH_ELEM;
+    pl.vpt = 1;
+    pl.cluster = 1;
+    if (pattern == ARF_ALLREDUCE) {
+        pl.threads = 256;
+        const int64_t tiles = ceil_div(H, 256) * M;
+        const int64_t cap = (int64_t)caps.num_sms * (caps.max_threads_per_sm / 256 > 0 ? caps.max_threads_per_sm / 256 : 1);
+        const int64_t g = tiles < cap ? tiles : cap;
+        pl.grid = (int)(g > 0 ? g : 1);
+    } else {
+        int64_t t = ceil_div(H, 32) * 32;
+        if (t > kMaxThreads) t = kMaxThreads;
+        pl.threads = (int)t;
+        const int per_sm = caps.max_threads_per_sm / pl.threads > 0 ? caps.max_threads_per_sm / pl.threads : 1;
+        const int64_t cap = (int64_t)caps.num_sms * per_sm;
+        const int64_t g = M < cap ? M : cap;
+        pl.grid = (int)(g > 0 ? g : 1);
+    }
+    return pl;
+}
 }  // namespace
 
 extern "C" arf_status_t arf_supports(arf_workspace_t ws, arf_pattern_t pattern, int W, int64_t M, int64_t H,
@@ -164,9 +189,8 @@ extern "C" arf_status_t arf_supports(arf_workspace_t ws, arf_pattern_t pattern, 
     if (!valid_pattern(pattern) || !valid_dtype(dtype)) return ARF_ERR_INVALID_ARG;
     if (H <= 0 || M < 0) return ARF_ERR_INVALID_ARG;
     if (W < 1 || W > ARF_MAX_W) return ARF_ERR_UNSUPPORTED;
-    if (H % 8 != 0 || H > ARF_MAX_H) return ARF_ERR_UNSUPPORTED;
-    if (pattern == ARF_AR_RESIDUAL_RMSNORM && H > max_rms_row(ws ? ws->caps.max_cluster : 16))
-        return ARF_ERR_UNSUPPORTED;
+    if (H > ARF_MAX_H) return ARF_ERR_UNSUPPORTED;
+    (void)ws;
     // [M,H] indices and the chunk count stay far inside int64
     if (M > ((int64_t)1 << 40) / H) return ARF_ERR_UNSUPPORTED;
     return ARF_OK;
@@ -178,10 +202,13 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
     arf_status_t st = arf_supports(nullptr, pattern, W, M, H, dtype);
     if (st != ARF_OK) return st;
     if (caps->num_sms < 1 || caps->max_threads_per_sm < 32 || caps->max_cluster < 1) return ARF_ERR_INVALID_ARG;
-    if (pattern == ARF_AR_RESIDUAL_RMSNORM && H > max_rms_row(caps->max_cluster)) return ARF_ERR_UNSUPPORTED;
     const int w_spec = arf::w_spec_compiled(W) ? W : 0;
     arf_plan_t pl = {};
-    if (pattern == ARF_ALLREDUCE) {
+    if (H % 8 != 0 || (pattern == ARF_AR_RESIDUAL_RMSNORM && H > max_rms_row(caps->max_cluster))) {
+        // no 16-byte chunking possible, or a row longer than the device's
+        // clusters hold: the elementwise kernels
+        pl = elem_plan(*caps, pattern, M, H);
+    } else if (pattern == ARF_ALLREDUCE) {
         // one pass over all chunks (no grid-stride trips); about 8 loads
         // outstanding per thread when there is enough work to fill the
         // device several times over, else one chunk per thread (latency:
@@ -242,6 +269,11 @@ extern "C" arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_
     if (!arf::w_spec_compiled(pl->w_spec)) return ARF_ERR_UNSUPPORTED;
     if (pl->threads < 32 || pl->threads > kMaxThreads || pl->threads % 32 != 0) return ARF_ERR_UNSUPPORTED;
     if (pl->cluster < 1 || pl->grid < 1 || pl->grid % pl->cluster != 0) return ARF_ERR_UNSUPPORTED;
+    if (pl->path == ARF_PATH_ELEM) {
+        if (pl->cluster != 1 || pl->vpt != 1 || pl->stages != 0 || pl->w_spec != 0) return ARF_ERR_UNSUPPORTED;
+        return ARF_OK;
+    }
+    if (H % 8 != 0) return ARF_ERR_UNSUPPORTED;  // the 16-byte kernels need whole chunks
     if (pl->path == ARF_PATH_ASYNC) {
         if (pattern != ARF_AR_RESIDUAL_RMSNORM || pl->w_spec == 0 || pl->w_spec != W) return ARF_ERR_UNSUPPORTED;
         if (pl->threads != arf::kAsyncCtaThreads || pl->cluster != 1 || pl->vpt != 1) return ARF_ERR_UNSUPPORTED;
@@ -273,8 +305,9 @@ extern "C" arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_
 
 namespace {
 
-cudaError_t max_active_clusters(arf_dtype_t dt, const arf_plan_t& pl, int* n) {
-    return dt == ARF_BF16 ? arf::rms_max_active_clusters_bf16(pl, n) : arf::rms_max_active_clusters_fp16(pl, n);
+cudaError_t max_active_clusters(arf_dtype_t dt, const arf_plan_t& pl, int* n, bool f32p = false) {
+    return dt == ARF_BF16 ? arf::rms_max_active_clusters_bf16(pl, n, f32p)
+                          : arf::rms_max_active_clusters_fp16(pl, n, f32p);
 }
 
 cudaError_t max_active_blocks(arf_dtype_t dt, const arf_plan_t& pl, int64_t H, int* n) {
@@ -345,21 +378,42 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
     return ARF_OK;
 }
 
-// Everything arf_run checks before it launches (sizes already supported).
-arf_status_t check_call(arf_workspace_t ws, arf_pattern_t pattern, const void* const* partials,
-                        const void* residual, const void* gamma, float eps, const void* out,
-                        const void* residual_out) {
+// Row strides in elements and the partial type of one call.
+struct Layout {
+    int64_t ldp, ldr, ldo, ldro;
+    bool f32p;
+    bool vec_ok;  // the 16-byte kernels can take it
+};
+
+bool odd(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) != 0; }
+
+// Everything arf_run checks before it launches (sizes already supported),
+// and whether the 16-byte kernels can take the layout.
+arf_status_t check_call(arf_pattern_t pattern, const arf_run_opts_t* opts, bool by_value,
+                        const void* const* partials, const void* residual, const void* gamma, float eps,
+                        const void* out, const void* residual_out, int64_t H, Layout* ly) {
     if (!partials || !out) return ARF_ERR_INVALID_ARG;
     const bool rms = pattern == ARF_AR_RESIDUAL_RMSNORM;
+    ly->ldp = opts && opts->ld_partials ? opts->ld_partials : H;
+    ly->ldr = opts && opts->ld_residual ? opts->ld_residual : H;
+    ly->ldo = opts && opts->ld_out ? opts->ld_out : H;
+    ly->ldro = opts && opts->ld_residual_out ? opts->ld_residual_out : H;
+    ly->f32p = opts && opts->partials_f32;
+    if (ly->ldp < H || ly->ldo < H) return ARF_ERR_INVALID_ARG;
     if (rms) {
         if (!residual || !gamma || !residual_out) return ARF_ERR_INVALID_ARG;
         if (!std::isfinite(eps) || eps < 0.0f) return ARF_ERR_INVALID_ARG;
         if (out == residual_out) return ARF_ERR_INVALID_ARG;
-        if (!aligned16(residual) || !aligned16(gamma) || !aligned16(residual_out)) return ARF_ERR_UNSUPPORTED;
+        if (ly->ldr < H || ly->ldro < H) return ARF_ERR_INVALID_ARG;
+        if (residual == residual_out && ly->ldr != ly->ldro) return ARF_ERR_INVALID_ARG;
+        if (odd(residual) || odd(gamma) || odd(residual_out)) return ARF_ERR_UNSUPPORTED;
     }
-    if (!aligned16(out)) return ARF_ERR_UNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(partials) & 7u) != 0) return ARF_ERR_UNSUPPORTED;
-    (void)ws;
+    if (odd(out)) return ARF_ERR_UNSUPPORTED;
+    if (!by_value && (reinterpret_cast<uintptr_t>(partials) & 7u) != 0) return ARF_ERR_UNSUPPORTED;
+    bool v = H % 8 == 0 && ly->ldp % 8 == 0 && ly->ldo % 8 == 0 && aligned16(out);
+    if (rms) v = v && ly->ldr % 8 == 0 && ly->ldro % 8 == 0 && aligned16(residual) && aligned16(gamma) &&
+                 aligned16(residual_out);
+    ly->vec_ok = v;
     return ARF_OK;
 }
 
@@ -397,18 +451,50 @@ void fill_common(arf::LaunchCommon& lc, const void* const* partials, int W, bool
 arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t pattern, int W,
                     const void* const* partials, bool by_value, bool pdl, const void* residual, const void* gamma,
                     float eps, void* out, void* residual_out, int64_t M, int64_t H, arf_dtype_t dtype,
-                    cudaStream_t stream) {
+                    const Layout& L, cudaStream_t stream) {
     cudaError_t e;
+    const bool bf = dtype == ARF_BF16;
+    if (pl.path == ARF_PATH_ELEM) {
+        arf::ElemParams p = {};
+        fill_common(p.lc, partials, W, by_value, pdl);
+        p.residual = static_cast<const unsigned short*>(residual);
+        p.gamma = static_cast<const unsigned short*>(gamma);
+        p.out = static_cast<unsigned short*>(out);
+        p.residual_out = static_cast<unsigned short*>(residual_out);
+        p.M = M;
+        p.ldp = L.ldp;
+        p.ldr = L.ldr;
+        p.ldo = L.ldo;
+        p.ldro = L.ldro;
+        p.H = (int)H;
+        p.W = W;
+        p.eps = eps;
+        const bool rms = pattern == ARF_AR_RESIDUAL_RMSNORM;
+        e = bf ? arf::launch_elem_bf16(p, pl, rms, stream, L.f32p) : arf::launch_elem_fp16(p, pl, rms, stream, L.f32p);
+        if (e != cudaSuccess) return cuda_fail(ws, e);
+        return ARF_OK;
+    }
+    // 16-byte vectors: 16-bit tensors have 8 elements per vector, binary32 partials 4
+    arf::RowLayout rl;
+    rl.ldp = L.f32p ? L.ldp / 4 : L.ldp / 8;
+    rl.ldr = L.ldr / 8;
+    rl.ldo = L.ldo / 8;
+    rl.ldro = L.ldro / 8;
     if (pattern == ARF_ALLREDUCE) {
         arf::FlatParams p = {};
         fill_common(p.lc, partials, W, by_value, pdl);
+        p.ly = rl;
         p.out = static_cast<uint4*>(out);
         p.nchunks = M * H / 8;
+        p.M = M;
+        p.C = (int)(H / 8);
+        p.strided = (L.ldp != H || L.ldo != H) ? 1 : 0;
         p.W = W;
-        e = dtype == ARF_BF16 ? arf::launch_flat_bf16(p, pl, stream) : arf::launch_flat_fp16(p, pl, stream);
+        e = bf ? arf::launch_flat_bf16(p, pl, stream, L.f32p) : arf::launch_flat_fp16(p, pl, stream, L.f32p);
     } else {
         arf::RmsParams p = {};
         fill_common(p.lc, partials, W, by_value, pdl);
+        p.ly = rl;
         p.residual = static_cast<const uint4*>(residual);
         p.gamma = static_cast<const uint4*>(gamma);
         p.out = static_cast<uint4*>(out);
@@ -421,7 +507,7 @@ arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t patt
         p.slice = (int)ceil_div(p.C, pl.cluster);
         p.stages = pl.stages;
         p.eps = eps;
-        e = dtype == ARF_BF16 ? arf::launch_rms_bf16(p, pl, stream) : arf::launch_rms_fp16(p, pl, stream);
+        e = bf ? arf::launch_rms_bf16(p, pl, stream, L.f32p) : arf::launch_rms_fp16(p, pl, stream, L.f32p);
     }
     if (e != cudaSuccess) return cuda_fail(ws, e);
     return ARF_OK;
@@ -441,8 +527,15 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
         if (st != ARF_OK) return st;
     }
     if (M == 0) return ARF_OK;
-    st = check_call(ws, pattern, partials, residual, gamma, eps, out, residual_out);
+    Layout L;
+    st = check_call(pattern, opts, by_value, partials, residual, gamma, eps, out, residual_out, H, &L);
     if (st != ARF_OK) return st;
+    if (forced && forced->path != ARF_PATH_ELEM) {
+        // an explicit 16-byte plan needs a layout those kernels take; binary32
+        // partials exist only in the run-time-W instances of the row/flat kernels
+        if (!L.vec_ok) return ARF_ERR_UNSUPPORTED;
+        if (L.f32p && (forced->w_spec != 0 || forced->path == ARF_PATH_ASYNC)) return ARF_ERR_UNSUPPORTED;
+    }
     if (by_value) {
         for (int r = 0; r < W; ++r)
             if (!partials[r]) return ARF_ERR_INVALID_ARG;
@@ -457,7 +550,7 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
         if (pl.path == ARF_PATH_CLUSTER && !capturing) {
             // a cluster shape must fit the device: no launch that cannot start
             int n = 0;
-            cudaError_t e = max_active_clusters(dtype, pl, &n);
+            cudaError_t e = max_active_clusters(dtype, pl, &n, L.f32p);
             if (e != cudaSuccess) return cuda_fail(ws, e);
             if (n < 1) return ARF_ERR_UNSUPPORTED;
         }
@@ -470,9 +563,23 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
     } else {
         st = device_plan(ws, pattern, W, M, H, dtype, &pl, capturing);
         if (st != ARF_OK) return st;
+        if (pl.path != ARF_PATH_ELEM) {
+            if (!L.vec_ok) {
+                pl = elem_plan(ws->caps, pattern, M, H);  // strides or alignment the vectors cannot take
+            } else if (L.f32p) {
+                pl.w_spec = 0;  // binary32 partials: the run-time W instances
+                if (pl.path == ARF_PATH_CLUSTER && !capturing) {
+                    int n = 0;
+                    if (max_active_clusters(dtype, pl, &n, true) != cudaSuccess || n < 1) {
+                        (void)cudaGetLastError();
+                        pl = elem_plan(ws->caps, pattern, M, H);
+                    }
+                }
+            }
+        }
     }
     return launch(ws, pl, pattern, W, partials, by_value, pdl, residual, gamma, eps, out, residual_out, M, H, dtype,
-                  stream);
+                  L, stream);
 }
 
 }  // namespace

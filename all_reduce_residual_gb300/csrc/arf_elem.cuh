@@ -1,0 +1,96 @@
+// arf_elem.cuh: elementwise kernels for layouts the 16-byte kernels cannot
+// take: H not a multiple of 8, row strides not a multiple of 8 elements, or
+// residual / gamma / outputs not 16-byte aligned (2-byte alignment suffices;
+// binary32 partials need 4). One element per thread per step, the same
+// arithmetic as the vector kernels: binary32 rank-order sum with one
+// round-to-nearest add per rank, the residual added to the unrounded sum,
+// one rounding, the statistic of the stored residual_out.
+#pragma once
+
+#include "arf_kernels.cuh"
+
+namespace arf {
+
+template <typename T>
+__device__ __forceinline__ float widen1(unsigned short h);
+template <>
+__device__ __forceinline__ float widen1<__nv_bfloat16>(unsigned short h) {
+    return __uint_as_float((uint32_t)h << 16);
+}
+template <>
+__device__ __forceinline__ float widen1<__half>(unsigned short h) {
+    return __half2float(__ushort_as_half(h));
+}
+
+template <typename T>
+__device__ __forceinline__ unsigned short narrow1(float f);
+template <>
+__device__ __forceinline__ unsigned short narrow1<__nv_bfloat16>(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+template <>
+__device__ __forceinline__ unsigned short narrow1<__half>(float f) {
+    return __half_as_ushort(__float2half_rn(f));
+}
+
+// Rank-order binary32 sum of element i of every partial (acc from +0.0f).
+template <typename T, bool F32P>
+__device__ __forceinline__ float elem_rank_sum(const uint4* const* s_ptr, int W, int64_t i) {
+    float acc = 0.0f;
+    if constexpr (F32P) {
+        for (int r = 0; r < W; ++r) acc = __fadd_rn(acc, reinterpret_cast<const float*>(s_ptr[r])[i]);
+    } else {
+        for (int r = 0; r < W; ++r)
+            acc = MixedAdd<T>::add(acc, reinterpret_cast<const unsigned short*>(s_ptr[r])[i]);
+    }
+    return acc;
+}
+
+// kAllReduce: tiles of blockDim.x elements, never crossing a row.
+template <typename T, bool F32P>
+__global__ void __launch_bounds__(kMaxThreads) ar_elem_kernel(ElemParams p) {
+    __shared__ const uint4* s_ptr[ARF_MAX_W];
+    prologue(s_ptr, p.lc, p.W);
+    __syncthreads();
+    const int64_t per_row = (p.H + blockDim.x - 1) / blockDim.x;
+    const int64_t ntiles = per_row * p.M;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const int64_t row = t / per_row;
+        const int64_t e = (t - row * per_row) * blockDim.x + threadIdx.x;
+        if (e < p.H) {
+            const float acc = elem_rank_sum<T, F32P>(s_ptr, p.W, row * p.ldp + e);
+            p.out[row * p.ldo + e] = narrow1<T>(acc);
+        }
+    }
+}
+
+// kARResidualRMSNorm: one CTA per row (rows grid-stride). The rounded
+// residual_out goes to memory in the first pass and is read back in the
+// second by the thread that wrote it.
+template <typename T, bool F32P>
+__global__ void __launch_bounds__(kMaxThreads) rms_elem_kernel(ElemParams p) {
+    __shared__ const uint4* s_ptr[ARF_MAX_W];
+    __shared__ float s_warp[2][kMaxThreads / 32];
+    prologue(s_ptr, p.lc, p.W);
+    __syncthreads();
+    int it = 0;
+    for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++it) {
+        float ss = 0.0f;
+        for (int64_t e = threadIdx.x; e < p.H; e += blockDim.x) {
+            float acc = elem_rank_sum<T, F32P>(s_ptr, p.W, row * p.ldp + e);
+            acc = MixedAdd<T>::add(acc, p.residual[row * p.ldr + e]);
+            const unsigned short xs = narrow1<T>(acc);
+            p.residual_out[row * p.ldro + e] = xs;
+            const float x = widen1<T>(xs);
+            ss = fmaf(x, x, ss);
+        }
+        const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
+        for (int64_t e = threadIdx.x; e < p.H; e += blockDim.x) {
+            const float x = widen1<T>(p.residual_out[row * p.ldro + e]);
+            const float g = widen1<T>(p.gamma[e]);
+            p.out[row * p.ldo + e] = narrow1<T>(__fmul_rn(__fmul_rn(x, inv), g));
+        }
+    }
+}
+
+}  // namespace arf

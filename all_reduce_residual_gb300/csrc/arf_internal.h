@@ -30,15 +30,30 @@ struct LaunchCommon {
     int pdl;                        // 1: launched as a programmatic dependent
 };
 
+// Row layout shared by both kernels. A chunk is 8 elements; strides are in
+// 16-byte vectors. 16-bit partials: chunk c of row m is vector m*ldp + c;
+// binary32 partials (f32p): vectors m*ldp + 2c and m*ldp + 2c + 1.
+struct RowLayout {
+    int64_t ldp;   // partials row stride (vectors)
+    int64_t ldr;   // residual row stride (vectors)
+    int64_t ldo;   // out row stride (vectors)
+    int64_t ldro;  // residual_out row stride (vectors)
+};
+
 struct FlatParams {
     LaunchCommon lc;
+    RowLayout ly;
     uint4* out;
-    int64_t nchunks;              // M*H/8
+    int64_t nchunks;              // M*C
+    int64_t M;
+    int C;                        // chunks per row, H/8
+    int strided;                  // 0: rows contiguous (a flat range of chunks)
     int W;
 };
 
 struct RmsParams {
     LaunchCommon lc;
+    RowLayout ly;
     const uint4* residual;
     const uint4* gamma;
     uint4* out;
@@ -53,12 +68,28 @@ struct RmsParams {
     float eps;
 };
 
+// Elementwise kernels (arf_elem.cuh): any H, 2-byte alignment.
+struct ElemParams {
+    LaunchCommon lc;
+    const unsigned short* residual;
+    const unsigned short* gamma;
+    unsigned short* out;
+    unsigned short* residual_out;
+    int64_t M;
+    int64_t ldp, ldr, ldo, ldro;  // row strides, elements
+    int H;
+    int W;
+    float eps;
+};
+
 // Launchers, one per I/O type (arf_launch_bf16.cu / arf_launch_fp16.cu).
-// They assume a plan that passed arf_plan_check.
-cudaError_t launch_flat_bf16(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s);
-cudaError_t launch_flat_fp16(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s);
-cudaError_t launch_rms_bf16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s);
-cudaError_t launch_rms_fp16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s);
+// They assume a plan that passed arf_plan_check. f32p: binary32 partials.
+cudaError_t launch_flat_bf16(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p);
+cudaError_t launch_flat_fp16(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p);
+cudaError_t launch_rms_bf16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p);
+cudaError_t launch_rms_fp16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p);
+cudaError_t launch_elem_bf16(const ElemParams& p, const arf_plan_t& plan, bool rms, cudaStream_t s, bool f32p);
+cudaError_t launch_elem_fp16(const ElemParams& p, const arf_plan_t& plan, bool rms, cudaStream_t s, bool f32p);
 
 // Per-device kernel attributes, set once at workspace creation: 16-CTA
 // clusters for the cluster kernels (when the device has clusters) and
@@ -77,12 +108,12 @@ constexpr size_t async_dyn_smem(int W, int stages, int C) {
 
 // How many clusters of plan.cluster CTAs of plan.threads threads the RMS
 // kernel instance of `plan` can keep resident at once (0 = cannot launch).
-cudaError_t rms_max_active_clusters_bf16(const arf_plan_t& plan, int* n);
-cudaError_t rms_max_active_clusters_fp16(const arf_plan_t& plan, int* n);
+cudaError_t rms_max_active_clusters_bf16(const arf_plan_t& plan, int* n, bool f32p = false);
+cudaError_t rms_max_active_clusters_fp16(const arf_plan_t& plan, int* n, bool f32p = false);
 // How many CTAs of the RMS kernel instance of `plan` (rows of C chunks) one
 // SM can hold.
-cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int C, int* n);
-cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int C, int* n);
+cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int C, int* n, bool f32p = false);
+cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int C, int* n, bool f32p = false);
 
 // Record a CUDA error as the workspace's last one (arf_last_cuda_error).
 void note_cuda_error(arf_workspace_t ws, cudaError_t e);

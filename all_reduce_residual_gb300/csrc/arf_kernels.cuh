@@ -158,15 +158,37 @@ __device__ __forceinline__ void accumulate(float acc[8], const uint4& v) {
     }
 }
 
-// Sum of the W partials at chunk c, in rank order, into acc (acc starts at
-// +0.0f). WS > 0: W == WS is known at compile time and every load is issued
-// before the first add. WS == 0: W is read at run time and handled in groups
-// of 8 predicated loads.
-template <typename T, int WS>
+// acc[e] += binary32 partial values held as two 16-byte vectors (8 floats).
+__device__ __forceinline__ void accumulate_f32(float acc[8], const uint4& a, const uint4& b) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], __uint_as_float(w[e]));
+}
+
+// Sum of the W partials at one chunk, in rank order, into acc (acc starts at
+// +0.0f); c is the chunk's vector index in every partial. WS > 0: W == WS is
+// known at compile time and every load is issued before the first add.
+// WS == 0: W is read at run time and handled in groups of 8 predicated loads.
+// F32P: binary32 partials, two vectors per chunk (c and c + 1), run-time W.
+template <typename T, int WS, bool F32P = false>
 __device__ __forceinline__ void rank_sum(float acc[8], const uint4* const* s_ptr, int W, int64_t c) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-    if constexpr (WS > 0) {
+    if constexpr (F32P) {
+        static_assert(WS == 0, "binary32 partials use the run-time rank count");
+        for (int r0 = 0; r0 < W; r0 += 4) {
+            uint4 v[4][2];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (r0 + j < W) {
+                    v[j][0] = ld_once(s_ptr[r0 + j] + c);
+                    v[j][1] = ld_once(s_ptr[r0 + j] + c + 1);
+                }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (r0 + j < W) accumulate_f32(acc, v[j][0], v[j][1]);
+        }
+    } else if constexpr (WS > 0) {
         uint4 v[WS];
 #pragma unroll
         for (int r = 0; r < WS; ++r) v[r] = ld_once(s_ptr[r] + c);
@@ -208,51 +230,69 @@ __device__ __forceinline__ void prologue(const uint4** s_ptr, const LaunchCommon
 }
 
 // ---------------------------------------------------------------------------
-// kAllReduce: out = rn(sum_r P_r), flat over all M*H/8 chunks.
+// kAllReduce: out = rn(sum_r P_r). Rows contiguous: one flat range of M*C
+// chunks in tiles of nthr*U chunks. Strided rows: tiles never cross a row
+// (tiles_per_row tiles per row; one division per tile).
 // ---------------------------------------------------------------------------
-template <typename T, int WS, int U>
+template <typename T, int WS, int U, bool F32P>
+__device__ __forceinline__ void flat_tile(const FlatParams& p, const uint4* const* s_ptr, int64_t row, int64_t col0,
+                                          int64_t col_end) {
+    // chunk col of row `row`: partial vector row*ldp + col (x2 for binary32),
+    // output vector row*ldo + col
+    const int64_t pbase = row * p.ly.ldp, obase = row * p.ly.ldo;
+    if constexpr (WS > 0 && !F32P) {
+        uint4 v[U][WS];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t c = col0 + u * 32;
+            if (c < col_end) {
+#pragma unroll
+                for (int r = 0; r < WS; ++r) v[u][r] = ld_once(s_ptr[r] + pbase + c);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t c = col0 + u * 32;
+            if (c < col_end) {
+                float acc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+                for (int r = 0; r < WS; ++r) accumulate<T>(acc, v[u][r]);
+                st_out(p.out + obase + c, Pack8<T>::narrow(acc));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t c = col0 + u * 32;
+            if (c < col_end) {
+                float acc[8];
+                rank_sum<T, 0, F32P>(acc, s_ptr, p.W, pbase + (F32P ? 2 * c : c));
+                st_out(p.out + obase + c, Pack8<T>::narrow(acc));
+            }
+        }
+    }
+}
+
+template <typename T, int WS, int U, bool F32P = false>
 __global__ void __launch_bounds__(kMaxThreads) ar_flat_kernel(FlatParams p) {
     __shared__ const uint4* s_ptr[ARF_MAX_W];
     prologue(s_ptr, p.lc, p.W);
     __syncthreads();
 
-    const int64_t nthr = blockDim.x;
-    const int64_t step = (int64_t)gridDim.x * nthr * U;
-    // this thread's first chunk of each tile of nthr*U chunks is base + u*32
-    for (int64_t base = (int64_t)blockIdx.x * nthr * U + warp_run_chunk<U>(0); base < p.nchunks; base += step) {
-        if constexpr (WS > 0) {
-            // all U*W loads first, then the adds
-            uint4 v[U][WS];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t c = base + u * 32;
-                if (c < p.nchunks) {
-#pragma unroll
-                    for (int r = 0; r < WS; ++r) v[u][r] = ld_once(s_ptr[r] + c);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t c = base + u * 32;
-                if (c < p.nchunks) {
-                    float acc[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-#pragma unroll
-                    for (int r = 0; r < WS; ++r) accumulate<T>(acc, v[u][r]);
-                    st_out(p.out + c, Pack8<T>::narrow(acc));
-                }
-            }
-        } else {
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t c = base + u * 32;
-                if (c < p.nchunks) {
-                    float acc[8];
-                    rank_sum<T, 0>(acc, s_ptr, p.W, c);
-                    st_out(p.out + c, Pack8<T>::narrow(acc));
-                }
-            }
+    const int64_t tile = (int64_t)blockDim.x * U;
+    if (!p.strided) {
+        // the whole [M, C] range as one row (ldp = C or 2C, ldo = C)
+        for (int64_t t0 = (int64_t)blockIdx.x * tile; t0 < p.nchunks; t0 += (int64_t)gridDim.x * tile)
+            flat_tile<T, WS, U, F32P>(p, s_ptr, 0, t0 + warp_run_chunk<U>(0), p.nchunks);
+    } else {
+        const int64_t tiles_per_row = (p.C + tile - 1) / tile;
+        const int64_t ntiles = tiles_per_row * p.M;
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            const int64_t row = t / tiles_per_row;
+            const int64_t col0 = (t - row * tiles_per_row) * tile;
+            flat_tile<T, WS, U, F32P>(p, s_ptr, row, col0 + warp_run_chunk<U>(0), p.C);
         }
     }
 }
@@ -281,7 +321,7 @@ struct RmsShape {
 // the reduction barrier), which is the point of prefetching.
 template <int WS, int VPT>
 __device__ __forceinline__ void issue_row(uint4 (&L)[VPT][WS + 1], const uint4* const* s_ptr,
-                                          const uint4* residual, int64_t rbase, int c0, int c1) {
+                                          const uint4* residual, int64_t pbase, int64_t rbase, int c0, int c1) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int c = c0 + warp_run_chunk<VPT>(k);
@@ -292,7 +332,7 @@ __device__ __forceinline__ void issue_row(uint4 (&L)[VPT][WS + 1], const uint4* 
                          : "l"(rp));
 #pragma unroll
             for (int r = 0; r < WS; ++r) {
-                const uint4* pp = s_ptr[r] + rbase + c;
+                const uint4* pp = s_ptr[r] + pbase + c;
                 asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                              : "=r"(L[k][r].x), "=r"(L[k][r].y), "=r"(L[k][r].z), "=r"(L[k][r].w)
                              : "l"(pp));
@@ -347,9 +387,10 @@ __device__ __forceinline__ void normalise_chunk(const uint4& xs, const uint4& gv
     st_out(dst, Pack8<T>::narrow(y));
 }
 
-template <typename T, int WS, int VPT>
+template <typename T, int WS, int VPT, bool F32P = false>
 __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
     using Shape = RmsShape<WS, VPT>;
+    static_assert(!F32P || WS == 0, "binary32 partials use the run-time rank count");
     __shared__ const uint4* s_ptr[ARF_MAX_W];
     __shared__ float s_warp[2][kMaxThreads / 32];  // per-warp partial sums, by row parity
     __shared__ float s_cta[2];                     // this CTA's partial, read by its peers
@@ -376,9 +417,9 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
     if constexpr (Shape::kPrefetch) {
         uint4 L[VPT][WS + 1];
         int64_t row = cluster_id;
-        if (row < p.M) issue_row<WS, VPT>(L, s_ptr, p.residual, row * (int64_t)p.C, c0, c1);
+        if (row < p.M) issue_row<WS, VPT>(L, s_ptr, p.residual, row * p.ly.ldp, row * p.ly.ldr, c0, c1);
         for (int it = 0; row < p.M; row += nclusters, ++it) {
-            const int64_t rbase = row * (int64_t)p.C;
+            const int64_t ob = row * p.ly.ldo, rob = row * p.ly.ldro;
             uint4 xs[VPT];
             float ss = 0.0f;
 #pragma unroll
@@ -390,11 +431,11 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
                     for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll
                     for (int r = 0; r < WS; ++r) accumulate<T>(acc, L[k][r]);
-                    xs[k] = residual_chunk<T>(acc, L[k][WS], p.residual_out + rbase + c, ss);
+                    xs[k] = residual_chunk<T>(acc, L[k][WS], p.residual_out + rob + c, ss);
                 }
             }
             const int64_t next = row + nclusters;
-            if (next < p.M) issue_row<WS, VPT>(L, s_ptr, p.residual, next * (int64_t)p.C, c0, c1);
+            if (next < p.M) issue_row<WS, VPT>(L, s_ptr, p.residual, next * p.ly.ldp, next * p.ly.ldr, c0, c1);
             const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, it) / (float)p.H + p.eps);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
@@ -403,14 +444,14 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
                     uint4 gv;
                     if constexpr (Shape::kGammaRegs) gv = g[k];
                     else gv = ld_keep(p.gamma + c);
-                    normalise_chunk<T>(xs[k], gv, inv, p.out + rbase + c);
+                    normalise_chunk<T>(xs[k], gv, inv, p.out + ob + c);
                 }
             }
         }
     } else {
         int it = 0;
         for (int64_t row = cluster_id; row < p.M; row += nclusters, ++it) {
-            const int64_t rbase = row * (int64_t)p.C;
+            const int64_t pb = row * p.ly.ldp, rb = row * p.ly.ldr, ob = row * p.ly.ldo, rob = row * p.ly.ldro;
             uint4 xs[VPT];
             float ss = 0.0f;
 #pragma unroll
@@ -418,9 +459,9 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
                 const int c = c0 + warp_run_chunk<VPT>(k);
                 if (c < c1) {
                     float acc[8];
-                    const uint4 rv = ld_resid(p.residual + rbase + c);
-                    rank_sum<T, WS>(acc, s_ptr, p.W, rbase + c);
-                    xs[k] = residual_chunk<T>(acc, rv, p.residual_out + rbase + c, ss);
+                    const uint4 rv = ld_resid(p.residual + rb + c);
+                    rank_sum<T, WS, F32P>(acc, s_ptr, p.W, pb + (F32P ? 2 * (int64_t)c : (int64_t)c));
+                    xs[k] = residual_chunk<T>(acc, rv, p.residual_out + rob + c, ss);
                 }
             }
             const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, it) / (float)p.H + p.eps);
@@ -431,7 +472,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
                     uint4 gv;
                     if constexpr (Shape::kGammaRegs) gv = g[k];
                     else gv = ld_keep(p.gamma + c);
-                    normalise_chunk<T>(xs[k], gv, inv, p.out + rbase + c);
+                    normalise_chunk<T>(xs[k], gv, inv, p.out + ob + c);
                 }
             }
         }
@@ -507,11 +548,11 @@ __global__ void __launch_bounds__(kAsyncThreads, 1) rms_async_kernel(RmsParams p
         if (in_row < p.M) {
             const int c = in_b * kAsyncThreads + tid;
             if (c < C) {
-                const int64_t off = in_row * (int64_t)C + c;
+                const int64_t poff = in_row * p.ly.ldp + c, roff = in_row * p.ly.ldr + c;
                 const uint32_t slot = ring_addr + (uint32_t)in_slot * kSlotStride + (uint32_t)tid * 16u;
 #pragma unroll
-                for (int r = 0; r < WS; ++r) cp_async16(slot + r * kRankStride, s_ptr[r] + off);
-                cp_async16(slot + WS * kRankStride, p.residual + off);
+                for (int r = 0; r < WS; ++r) cp_async16(slot + r * kRankStride, s_ptr[r] + poff);
+                cp_async16(slot + WS * kRankStride, p.residual + roff);
             }
             if (++in_b == nb) {
                 in_b = 0;
@@ -525,7 +566,7 @@ __global__ void __launch_bounds__(kAsyncThreads, 1) rms_async_kernel(RmsParams p
     for (int j = 0; j < S - 1; ++j) issue_next();
     int slot_i = 0, it = 0;
     for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++it) {
-        const int64_t rbase = row * (int64_t)C;
+        const int64_t ob = row * p.ly.ldo, rob = row * p.ly.ldro;
         float ss = 0.0f;
         for (int b = 0; b < nb; ++b) {
             issue_next();
@@ -538,7 +579,7 @@ __global__ void __launch_bounds__(kAsyncThreads, 1) rms_async_kernel(RmsParams p
                 for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll
                 for (int r = 0; r < WS; ++r) accumulate<T>(acc, slot[r * kAsyncThreads]);
-                xrow[c] = residual_chunk<T>(acc, slot[WS * kAsyncThreads], p.residual_out + rbase + c, ss);
+                xrow[c] = residual_chunk<T>(acc, slot[WS * kAsyncThreads], p.residual_out + rob + c, ss);
             }
             if (++slot_i == S) slot_i = 0;
         }
@@ -546,7 +587,7 @@ __global__ void __launch_bounds__(kAsyncThreads, 1) rms_async_kernel(RmsParams p
         const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
         for (int b = 0; b < nb; ++b) {
             const int c = b * kAsyncThreads + tid;
-            if (c < C) normalise_chunk<T>(xrow[c], ld_keep(p.gamma + c), inv, p.out + rbase + c);
+            if (c < C) normalise_chunk<T>(xrow[c], ld_keep(p.gamma + c), inv, p.out + ob + c);
         }
     }
     cp_async_wait(0);  // only empty groups can remain; leave with nothing in flight

@@ -2,12 +2,13 @@
 // arf_launch_bf16.cu and arf_launch_fp16.cu, which instantiate it once each.
 #pragma once
 
-#include "arf_kernels.cuh"
+#include "arf_elem.cuh"
 
 namespace arf {
 
 using FlatFn = void (*)(FlatParams);
 using RmsFn = void (*)(RmsParams);
+using ElemFn = void (*)(ElemParams);
 
 template <typename T, int WS>
 FlatFn flat_by_unroll(int u) {
@@ -20,7 +21,16 @@ FlatFn flat_by_unroll(int u) {
 }
 
 template <typename T>
-FlatFn flat_kernel_for(int ws, int u) {
+FlatFn flat_kernel_for(int ws, int u, bool f32p = false) {
+    if (f32p) {  // binary32 partials: run-time rank count only
+        if (ws != 0) return nullptr;
+        switch (u) {
+            case 1: return ar_flat_kernel<T, 0, 1, true>;
+            case 2: return ar_flat_kernel<T, 0, 2, true>;
+            case 4: return ar_flat_kernel<T, 0, 4, true>;
+            default: return nullptr;
+        }
+    }
     switch (ws) {
         case 0: return flat_by_unroll<T, 0>(u);
         case 1: return flat_by_unroll<T, 1>(u);
@@ -44,7 +54,17 @@ RmsFn rms_by_vpt(int vpt) {
 }
 
 template <typename T>
-RmsFn rms_kernel_for(int ws, int vpt) {
+RmsFn rms_kernel_for(int ws, int vpt, bool f32p = false) {
+    if (f32p) {  // binary32 partials: run-time rank count only
+        if (ws != 0) return nullptr;
+        switch (vpt) {
+            case 1: return rms_kernel<T, 0, 1, true>;
+            case 2: return rms_kernel<T, 0, 2, true>;
+            case 4: return rms_kernel<T, 0, 4, true>;
+            case 8: return rms_kernel<T, 0, 8, true>;
+            default: return nullptr;
+        }
+    }
     switch (ws) {
         case 0: return rms_by_vpt<T, 0>(vpt);
         case 1: return rms_by_vpt<T, 1>(vpt);
@@ -69,8 +89,8 @@ RmsFn async_kernel_for(int ws) {
 }
 
 template <typename T>
-cudaError_t launch_flat_t(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s) {
-    FlatFn fn = flat_kernel_for<T>(plan.w_spec, plan.vpt);
+cudaError_t launch_flat_t(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p) {
+    FlatFn fn = flat_kernel_for<T>(plan.w_spec, plan.vpt, f32p);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
@@ -87,9 +107,10 @@ cudaError_t launch_flat_t(const FlatParams& p, const arf_plan_t& plan, cudaStrea
 }
 
 template <typename T>
-cudaError_t launch_rms_t(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s) {
+cudaError_t launch_rms_t(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p) {
     const bool streaming = plan.path == ARF_PATH_ASYNC;
-    RmsFn fn = streaming ? async_kernel_for<T>(plan.w_spec) : rms_kernel_for<T>(plan.w_spec, plan.vpt);
+    if (streaming && f32p) return cudaErrorInvalidValue;
+    RmsFn fn = streaming ? async_kernel_for<T>(plan.w_spec) : rms_kernel_for<T>(plan.w_spec, plan.vpt, f32p);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = {};
@@ -116,16 +137,36 @@ cudaError_t launch_rms_t(const RmsParams& p, const arf_plan_t& plan, cudaStream_
 }
 
 template <typename T>
+cudaError_t launch_elem_t(const ElemParams& p, const arf_plan_t& plan, bool rms, cudaStream_t s, bool f32p) {
+    ElemFn fn = rms ? (f32p ? rms_elem_kernel<T, true> : rms_elem_kernel<T, false>)
+                    : (f32p ? ar_elem_kernel<T, true> : ar_elem_kernel<T, false>);
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.grid);
+    cfg.blockDim = dim3((unsigned)plan.threads);
+    cfg.stream = s;
+    if (p.lc.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+template <typename T>
 cudaError_t configure_kernels_t(bool clusters, int max_dyn_smem) {
     const int ws_list[] = {0, 1, 2, 4, 8, 16};
     const int vpt_list[] = {1, 2, 4, 8};
     if (clusters)
         for (int ws : ws_list)
-            for (int vpt : vpt_list) {
-                cudaError_t e = cudaFuncSetAttribute(rms_kernel_for<T>(ws, vpt),
-                                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-                if (e != cudaSuccess) return e;
-            }
+            for (int vpt : vpt_list)
+                for (int f32p = 0; f32p < 2; ++f32p) {
+                    RmsFn fn = rms_kernel_for<T>(ws, vpt, f32p != 0);
+                    if (!fn) continue;
+                    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                    if (e != cudaSuccess) return e;
+                }
     for (int ws : ws_list) {
         RmsFn fn = async_kernel_for<T>(ws);
         if (!fn) continue;
@@ -136,8 +177,8 @@ cudaError_t configure_kernels_t(bool clusters, int max_dyn_smem) {
 }
 
 template <typename T>
-cudaError_t rms_max_active_clusters_t(const arf_plan_t& plan, int* n) {
-    RmsFn fn = rms_kernel_for<T>(plan.w_spec, plan.vpt);
+cudaError_t rms_max_active_clusters_t(const arf_plan_t& plan, int* n, bool f32p) {
+    RmsFn fn = rms_kernel_for<T>(plan.w_spec, plan.vpt, f32p);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
@@ -153,9 +194,9 @@ cudaError_t rms_max_active_clusters_t(const arf_plan_t& plan, int* n) {
 }
 
 template <typename T>
-cudaError_t rms_max_active_blocks_t(const arf_plan_t& plan, int C, int* n) {
+cudaError_t rms_max_active_blocks_t(const arf_plan_t& plan, int C, int* n, bool f32p) {
     const bool streaming = plan.path == ARF_PATH_ASYNC;
-    RmsFn fn = streaming ? async_kernel_for<T>(plan.w_spec) : rms_kernel_for<T>(plan.w_spec, plan.vpt);
+    RmsFn fn = streaming ? async_kernel_for<T>(plan.w_spec) : rms_kernel_for<T>(plan.w_spec, plan.vpt, f32p);
     if (!fn) return cudaErrorInvalidValue;
     const size_t smem = streaming ? async_dyn_smem(plan.w_spec, plan.stages, C) : 0;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fn, plan.threads, smem);

@@ -3,21 +3,24 @@
 
 namespace arf {
 
-cudaError_t launch_flat_bf16(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s) {
-    return launch_flat_t<__nv_bfloat16>(p, plan, s);
+cudaError_t launch_flat_bf16(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p) {
+    return launch_flat_t<__nv_bfloat16>(p, plan, s, f32p);
 }
-cudaError_t launch_rms_bf16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s) {
-    return launch_rms_t<__nv_bfloat16>(p, plan, s);
+cudaError_t launch_rms_bf16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p) {
+    return launch_rms_t<__nv_bfloat16>(p, plan, s, f32p);
+}
+cudaError_t launch_elem_bf16(const ElemParams& p, const arf_plan_t& plan, bool rms, cudaStream_t s, bool f32p) {
+    return launch_elem_t<__nv_bfloat16>(p, plan, rms, s, f32p);
 }
 cudaError_t configure_kernels_bf16(bool clusters, int max_dyn_smem) {
     return configure_kernels_t<__nv_bfloat16>(clusters, max_dyn_smem);
 }
-cudaError_t rms_max_active_clusters_bf16(const arf_plan_t& plan, int* n) {
-    return rms_max_active_clusters_t<__nv_bfloat16>(plan, n);
+cudaError_t rms_max_active_clusters_bf16(const arf_plan_t& plan, int* n, bool f32p) {
+    return rms_max_active_clusters_t<__nv_bfloat16>(plan, n, f32p);
 }
 
-cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int C, int* n) {
-    return rms_max_active_blocks_t<__nv_bfloat16>(plan, C, n);
+cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int C, int* n, bool f32p) {
+    return rms_max_active_blocks_t<__nv_bfloat16>(plan, C, n, f32p);
 }
 
 }  // namespace arf

@@ -78,18 +78,23 @@ typedef enum arf_path {
     ARF_PATH_ROW = 1,     /* kARResidualRMSNorm: one CTA owns a whole row */
     ARF_PATH_CLUSTER = 2, /* kARResidualRMSNorm: a row split over a thread-block
                              cluster, sum of squares exchanged through DSMEM */
-    ARF_PATH_ASYNC = 3    /* kARResidualRMSNorm, W in {1,2,4,8,16}: one CTA of
+    ARF_PATH_ASYNC = 3,   /* kARResidualRMSNorm, W in {1,2,4,8,16}: one CTA of
                              256 threads per SM streams its rows in column
                              blocks of 256 chunks through a ring of `stages`
                              asynchronous shared-memory copies (cp.async) */
+    ARF_PATH_ELEM = 4     /* either pattern, any layout: one element per thread
+                             per step (H not a multiple of 8, row strides not a
+                             multiple of 8, tensors only 2-byte aligned) */
 } arf_path_t;
 
 /* Limits of this build. */
 #define ARF_MAX_W 64        /* ranks: the pages' world sizes {2,...,64}, plus 1 */
-#define ARF_MAX_H 524288    /* hidden size; H must also be a multiple of 8 */
+#define ARF_MAX_H 524288    /* hidden size */
 #define ARF_MAX_H_PER_CTA 32768 /* kARResidualRMSNorm rows longer than this are
-                                   split over a thread-block cluster: H up to
-                                   ARF_MAX_H_PER_CTA x the cluster limit */
+                                   split over a thread-block cluster (H up to
+                                   ARF_MAX_H_PER_CTA x the cluster limit); longer
+                                   still, or H not a multiple of 8, take the
+                                   elementwise path */
 
 /* What the planner needs to know about a device. */
 typedef struct arf_device_caps {
@@ -142,11 +147,11 @@ const char* arf_status_string(arf_status_t status);
 
 /* Whether (pattern, W, M, H, dtype) is handled, judged on the sizes alone in
  * the manner of the supports()/dispatch contract of tokenspeed PR #1075
- * (Summary). ws may be NULL (shape rules only; a 16-CTA cluster limit is
- * assumed). Returns ARF_OK, or the status arf_run would return for these
- * sizes: W outside [1, ARF_MAX_W], H % 8 != 0, H > ARF_MAX_H, or (for
- * kARResidualRMSNorm) H > ARF_MAX_H_PER_CTA x the workspace's cluster limit
- * -> UNSUPPORTED; H <= 0 or M < 0 or a bad enum -> INVALID_ARG. */
+ * (Summary). ws may be NULL (shape rules only). Returns ARF_OK, or the status
+ * arf_run would return for these sizes: W outside [1, ARF_MAX_W] or
+ * H > ARF_MAX_H -> UNSUPPORTED; H <= 0 or M < 0 or a bad enum -> INVALID_ARG.
+ * Sizes the 16-byte kernels cannot take (H % 8 != 0, kARResidualRMSNorm rows
+ * longer than the device's clusters hold) run on the elementwise path. */
 arf_status_t arf_supports(arf_workspace_t ws, arf_pattern_t pattern, int W,
                           int64_t M, int64_t H, arf_dtype_t dtype);
 
@@ -199,9 +204,11 @@ arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_plan_t* pla
  * residual_out is rejected (INVALID_ARG); other overlaps are undefined.
  * M == 0 returns ARF_OK and launches nothing.
  * Errors: see arf_supports; NULL required pointer, non-finite or negative eps
- * -> INVALID_ARG; residual, gamma, out or residual_out not 16-byte aligned ->
- * UNSUPPORTED; current device or stream device != workspace device ->
- * DEVICE_MISMATCH; launch failure -> CUDA (code in arf_last_cuda_error). */
+ * -> INVALID_ARG; residual, gamma, out or residual_out at an odd address ->
+ * UNSUPPORTED (2-byte aligned but not 16-byte aligned: the elementwise path;
+ * partial pointers must be 16-byte aligned when H % 8 == 0, 2-byte otherwise);
+ * current device or stream device != workspace device -> DEVICE_MISMATCH;
+ * launch failure -> CUDA (code in arf_last_cuda_error). */
 arf_status_t arf_run(arf_workspace_t ws, arf_pattern_t pattern, int W,
                      const void* const* partials_dev,
                      const void* residual, const void* gamma, float eps,
@@ -240,11 +247,22 @@ typedef struct arf_run_opts {
                                 (griddepcontrol.wait) for it to complete before
                                 it touches any memory, so results are the same;
                                 what overlaps is launch latency. */
+    int64_t ld_partials;     /* row strides in elements (0 = H, contiguous): of */
+    int64_t ld_residual;     /* every partial, the residual, out and            */
+    int64_t ld_out;          /* residual_out. Each must be >= H. Strides that   */
+    int64_t ld_residual_out; /* are multiples of 8 keep the 16-byte kernels.    */
+    int partials_f32;        /* 1: the partials are binary32 [M,H] tensors (the
+                                I/O dtype still applies to residual, gamma and
+                                the outputs); they enter the binary32 rank-order
+                                sum exactly; 4-byte alignment required */
 } arf_run_opts_t;
 
 /* arf_run with per-call options (NULL opts = arf_run). Same semantics,
  * results contract and errors; with partials_by_value, `partials` must point
- * to W readable host pointers (INVALID_ARG if any is NULL). */
+ * to W readable host pointers (INVALID_ARG if any is NULL); a stride below H,
+ * or residual_out == residual with different strides -> INVALID_ARG. Layouts
+ * the 16-byte kernels cannot take (strides not multiples of 8, tensors only
+ * 2-byte aligned) run on the elementwise path; odd addresses -> UNSUPPORTED. */
 arf_status_t arf_run_ex(arf_workspace_t ws, const arf_run_opts_t* opts,
                         arf_pattern_t pattern, int W, const void* const* partials,
                         const void* residual, const void* gamma, float eps,

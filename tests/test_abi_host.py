@@ -16,7 +16,8 @@ HEADER = os.path.join(ROOT, "include", "arf.h")
 GB300 = arf.DeviceCaps(num_sms=152, max_cluster=16, max_threads_per_sm=2048, max_smem_per_block=232448)
 K3_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048)
 SHAPES = [(2, 8, 1024), (2, 128, 4096), *[(8, m, 7168) for m in K3_M], (4, 5851, 7168), (16, 585, 7168),
-          (1, 1, 8), (3, 7, 8), (64, 3, 32768), (5, 1000, 1000), (17, 200, 2048)]
+          (1, 1, 8), (3, 7, 8), (64, 3, 32768), (5, 1000, 1000), (17, 200, 2048),
+          (3, 7, 13), (2, 5, 1001), (8, 300, 7170), (1, 2, 1)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -65,7 +66,8 @@ def test_supports_rules(pattern):
     assert S(None, pattern, 8, 3, 65536, bf) == arf.ARF_OK
     assert S(None, pattern, 0, 1, 8, bf) == arf.ARF_ERR_UNSUPPORTED
     assert S(None, pattern, 65, 1, 8, bf) == arf.ARF_ERR_UNSUPPORTED
-    assert S(None, pattern, 2, 1, 12, bf) == arf.ARF_ERR_UNSUPPORTED      # H % 8
+    assert S(None, pattern, 2, 1, 12, bf) == arf.ARF_OK                   # H % 8 != 0: elementwise path
+    assert S(None, pattern, 2, 1, 1, bf) == arf.ARF_OK
     assert S(None, pattern, 2, 1, 524296, bf) == arf.ARF_ERR_UNSUPPORTED  # H > max
     assert S(None, pattern, 2, 1, 0, bf) == arf.ARF_ERR_INVALID_ARG
     assert S(None, pattern, 2, -1, 8, bf) == arf.ARF_ERR_INVALID_ARG
@@ -84,6 +86,9 @@ def test_planner_plans_are_legal(pattern, W, M, H):
         assert p.grid % p.cluster == 0 and p.threads % 32 == 0
         assert p.w_spec in (0, W)
         per_sm = caps.max_threads_per_sm // p.threads
+        if H % 8:
+            assert p.path == arf.ARF_PATH_ELEM and p.w_spec == 0 and p.cluster == 1 and p.stages == 0
+            continue
         if p.path == arf.ARF_PATH_ASYNC:
             # many rows, compile-time W: one streaming CTA per SM, ring of >= 3 blocks in shared memory
             assert M >= caps.num_sms and W in (1, 2, 4, 8, 16) and p.grid == caps.num_sms
@@ -136,10 +141,11 @@ def test_long_rows_split_over_clusters(H, M):
     assert p.threads * p.vpt * p.cluster >= H // 8
     assert arf.arf_plan_check(GB300, p, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16) == arf.ARF_OK
     assert arf.arf_plan_for_caps(GB300, arf.ARF_ALLREDUCE, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
-    # a device with 4-CTA clusters holds rows up to 4 x 32768
+    # a device with 4-CTA clusters holds rows up to 4 x 32768; longer rows
+    # take the elementwise kernel
     small = arf.DeviceCaps(152, 4, 2048, 232448)
-    want = arf.ARF_OK if H <= 4 * 32768 else arf.ARF_ERR_UNSUPPORTED
-    assert arf.arf_plan_for_caps(small, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == want
+    assert arf.arf_plan_for_caps(small, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+    assert p.path == (arf.ARF_PATH_CLUSTER if H <= 4 * 32768 else arf.ARF_PATH_ELEM)
 
 
 def test_long_row_limits():
@@ -149,8 +155,8 @@ def test_long_row_limits():
     assert S(None, arf.ARF_ALLREDUCE, 2, 1, 524296, arf.ARF_BF16) == arf.ARF_ERR_UNSUPPORTED
     no_cluster = arf.DeviceCaps(152, 1, 2048, 232448)
     p = arf.Plan()
-    assert arf.arf_plan_for_caps(no_cluster, arf.ARF_AR_RESIDUAL_RMSNORM, 2, 1, 32776, arf.ARF_BF16, p) == \
-        arf.ARF_ERR_UNSUPPORTED
+    assert arf.arf_plan_for_caps(no_cluster, arf.ARF_AR_RESIDUAL_RMSNORM, 2, 1, 32776, arf.ARF_BF16, p) == arf.ARF_OK
+    assert p.path == arf.ARF_PATH_ELEM and p.threads == 512
     assert arf.arf_plan_for_caps(no_cluster, arf.ARF_ALLREDUCE, 2, 1, 524288, arf.ARF_BF16, p) == arf.ARF_OK
 
 
@@ -174,6 +180,14 @@ def test_plan_check_rejects_bad_plans():
     assert with_(path=arf.ARF_PATH_CLUSTER, cluster=32, grid=64) == arf.ARF_ERR_UNSUPPORTED
     assert with_(path=arf.ARF_PATH_CLUSTER, cluster=4, grid=6) == arf.ARF_ERR_UNSUPPORTED
     assert with_(path=arf.ARF_PATH_ROW, cluster=1, threads=32, vpt=1) == arf.ARF_ERR_UNSUPPORTED  # 896 chunks
+    elem = arf.Plan(path=arf.ARF_PATH_ELEM, threads=256, vpt=1, cluster=1, grid=9, w_spec=0)
+    assert arf.arf_plan_check(GB300, elem, *args) == arf.ARF_OK
+    assert arf.arf_plan_check(GB300, elem, arf.ARF_AR_RESIDUAL_RMSNORM, 3, 5, 13, arf.ARF_BF16) == arf.ARF_OK
+    elem.w_spec = 8
+    assert arf.arf_plan_check(GB300, elem, *args) == arf.ARF_ERR_UNSUPPORTED
+    row13 = arf.Plan(path=arf.ARF_PATH_ROW, threads=32, vpt=1, cluster=1, grid=5, w_spec=3)
+    assert arf.arf_plan_check(GB300, row13, arf.ARF_AR_RESIDUAL_RMSNORM, 3, 5, 13, arf.ARF_BF16) == \
+        arf.ARF_ERR_UNSUPPORTED  # 16-byte kernels need H % 8 == 0
     small = arf.DeviceCaps(152, 4, 2048, 232448)
     p = arf.Plan(path=arf.ARF_PATH_CLUSTER, threads=64, vpt=1, cluster=16, grid=16, w_spec=8)
     assert arf.arf_plan_check(small, p, *args) == arf.ARF_ERR_UNSUPPORTED

@@ -1,0 +1,161 @@
+"""General layouts on the GPU against the oracle's general entry point:
+H not a multiple of 8 (elementwise kernels), row strides (16-byte kernels
+when they are multiples of 8 elements, elementwise otherwise), tensors only
+2-byte aligned, binary32 partials, and explicit elementwise plans."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import all_reduce_residual_gb300 as arf
+import oracle
+import pins
+from all_reduce_residual_gb300 import workloads as wl
+from gpu_util import DT, assert_parity
+
+pytestmark = pytest.mark.gpu
+RMS, AR = arf.ARF_AR_RESIDUAL_RMSNORM, arf.ARF_ALLREDUCE
+OPAT = {AR: oracle.ALLREDUCE, RMS: oracle.AR_RESIDUAL_RMSNORM}
+
+
+@pytest.fixture(scope="module")
+def ws():
+    with arf.Workspace(0) as w:
+        yield w
+
+
+def codes_of(rng, d, shape, sigma):
+    return pins.nearest_codes(d, rng.standard_normal(shape) * sigma)
+
+
+def embed(a, pad, fill, dtype):
+    """A CUDA [M,H] view with row stride H+pad of a wider buffer (padding = fill)."""
+    M, H = a.shape
+    big = np.full((M, H + pad), fill, dtype=a.dtype)
+    big[:, :H] = a
+    if a.dtype == np.float32:
+        t = torch.from_numpy(big).cuda()
+    else:
+        t = wl.from_codes(big, dtype).cuda()
+    return t[:, :H], t
+
+
+def host_codes(t):
+    return wl.codes(t.cpu().contiguous())
+
+
+def run_case(ws, pattern, dtype, W, M, H, pads=(0, 0, 0, 0), f32p=False, plan=None, seed=0):
+    d = DT[dtype]
+    rng = np.random.default_rng(seed)
+    if f32p:
+        P = [(rng.standard_normal((M, H)) * 2.0 ** rng.uniform(-4, 6)).astype(np.float32) for _ in range(W)]
+    else:
+        P = [codes_of(rng, d, (M, H), 1.5) for _ in range(W)]
+    R = codes_of(rng, d, (M, H), 1.0)
+    G = pins.nearest_codes(d, 0.5 + rng.random(H))
+    junk = np.float32(np.nan) if f32p else np.uint16(0x7FC1)
+    Pd, Pbig = zip(*[embed(p, pads[0], junk, dtype) for p in P])
+    # all partials share one row stride
+    Rd, _ = embed(R, pads[1], np.uint16(0x7FC1), dtype)
+    Od, Ob = embed(np.zeros((M, H), np.uint16), pads[2], np.uint16(0x1234), dtype)
+    ROd, ROb = embed(np.zeros((M, H), np.uint16), pads[3], np.uint16(0x1234), dtype)
+    Gd = wl.from_codes(G, dtype).cuda()
+    rms = pattern == RMS
+    arf.run(ws, pattern, list(Pd), Rd if rms else None, Gd if rms else None, 1e-6, out=Od,
+            residual_out=ROd if rms else None, plan=plan)
+    torch.cuda.synchronize()
+    ref = oracle.run_general(OPAT[pattern], P, R if rms else None, G if rms else None, 1e-6, dtype=d)
+    got = (host_codes(Od), host_codes(ROd) if rms else None)
+    assert_parity(d, pattern, got, ref, f"{dtype} W={W} M={M} H={H} pads={pads} f32p={f32p} plan={plan}")
+    # the outputs' row padding is untouched
+    for big in (Ob,) + ((ROb,) if rms else ()):
+        pad = host_codes(big)[:, H:]
+        assert (pad == 0x1234).all(), "wrote outside the rows"
+
+
+@pytest.mark.parametrize("H", [1, 3, 7, 13, 1001, 4099, 7170])
+@pytest.mark.parametrize("W", [1, 2, 3, 8])
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_h_not_multiple_of_8(ws, pattern, W, H):
+    run_case(ws, pattern, "bf16" if H % 2 else "fp16", W, 5, H, seed=H + W)
+
+
+@pytest.mark.parametrize("pads", [(8, 16, 24, 8), (3, 1, 5, 7), (0, 0, 8, 0), (8, 8, 8, 8), (0, 2, 0, 1)])
+@pytest.mark.parametrize("H", [64, 4096, 7168])
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_row_strides(ws, pattern, H, pads):
+    run_case(ws, pattern, "bf16", 4, 37, H, pads=pads, seed=H)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 8, 17])
+@pytest.mark.parametrize("M,H", [(1, 8), (37, 4096), (300, 7168), (5, 13), (2, 65536)])
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_f32_partials(ws, pattern, W, M, H):
+    run_case(ws, pattern, "bf16" if W % 2 else "fp16", W, M, H, f32p=True, seed=W * 7 + M)
+
+
+def test_f32_partials_strided(ws):
+    for pattern in (AR, RMS):
+        run_case(ws, pattern, "bf16", 3, 20, 1024, pads=(8, 8, 16, 8), f32p=True, seed=3)
+        run_case(ws, pattern, "fp16", 3, 20, 1000, pads=(3, 5, 1, 2), f32p=True, seed=4)
+
+
+@pytest.mark.parametrize("M,H", [(3, 8), (40, 7168), (2, 65536)])
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_explicit_elementwise_plans(ws, pattern, M, H):
+    for threads in (32, 256, 512):
+        for grid in (1, 7, 300):
+            plan = arf.Plan(path=arf.ARF_PATH_ELEM, threads=threads, vpt=1, cluster=1, grid=grid, w_spec=0)
+            run_case(ws, pattern, "fp16", 3, M, H, plan=plan, seed=threads + grid)
+
+
+def test_two_byte_aligned_tensors(ws):
+    """out / residual / gamma / residual_out at 2-byte (not 16-byte) offsets:
+    the elementwise kernels; an odd address is refused."""
+    M, H, W = 9, 256, 3
+    rng = np.random.default_rng(9)
+    P = [codes_of(rng, oracle.BF16, (M, H), 1.0) for _ in range(W)]
+    R = codes_of(rng, oracle.BF16, (M, H), 1.0)
+    G = pins.nearest_codes(oracle.BF16, 0.5 + rng.random(H))
+    Pd = [wl.from_codes(p, "bf16").cuda() for p in P]
+    buf = torch.zeros(4 * M * H + 64, dtype=torch.int16, device="cuda")
+    Rd = buf[1:1 + M * H].view(torch.bfloat16).view(M, H)
+    Rd.copy_(wl.from_codes(R, "bf16").cuda())
+    Gd = buf[M * H + 3:M * H + 3 + H].view(torch.bfloat16)
+    Gd.copy_(wl.from_codes(G, "bf16").cuda())
+    Od = buf[2 * M * H + 5:3 * M * H + 5].view(torch.bfloat16).view(M, H)
+    ROd = buf[3 * M * H + 7:4 * M * H + 7].view(torch.bfloat16).view(M, H)
+    arf.run(ws, RMS, Pd, Rd, Gd, 1e-6, out=Od, residual_out=ROd)
+    torch.cuda.synchronize()
+    ref = oracle.run(oracle.AR_RESIDUAL_RMSNORM, P, R, G, 1e-6, dtype=oracle.BF16)
+    assert_parity(oracle.BF16, RMS, (host_codes(Od), host_codes(ROd)), ref)
+    ptrs = arf.pointer_array(Pd)
+    st = arf.arf_run(ws.handle, RMS, W, ptrs.data_ptr(), Rd.data_ptr(), Gd.data_ptr(), 1e-6, Od.data_ptr() + 1,
+                     ROd.data_ptr(), M, H, arf.ARF_BF16, torch.cuda.current_stream().cuda_stream)
+    assert st == arf.ARF_ERR_UNSUPPORTED
+
+
+def test_layout_argument_errors(ws):
+    M, H = 4, 64
+    P = [torch.zeros((M, H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    R = torch.zeros((M, H), dtype=torch.bfloat16, device="cuda")
+    G = torch.ones((H,), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(R)
+    ptrs = arf.pointer_array(P)
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call(**kw):
+        o = arf.RunOpts(plan=None, partials_by_value=0, pdl=0, **kw)
+        return arf.arf_run_ex(ws.handle, o, RMS, 2, ptrs.data_ptr(), R.data_ptr(), G.data_ptr(), 1e-6,
+                              out.data_ptr(), R.data_ptr(), M, H, arf.ARF_BF16, s)
+
+    assert call(ld_partials=32) == arf.ARF_ERR_INVALID_ARG          # stride below H
+    assert call(ld_residual=72, ld_residual_out=80) == arf.ARF_ERR_INVALID_ARG  # in place, strides differ
+    assert call() == arf.ARF_OK                                      # in place, equal strides
+    plan = arf.Plan(path=arf.ARF_PATH_ROW, threads=32, vpt=2, cluster=1, grid=4, w_spec=2)
+    o = arf.RunOpts(plan=ctypes.pointer(plan), partials_by_value=0, pdl=0, partials_f32=1)
+    # an explicit run-time-W plan is needed for binary32 partials
+    assert arf.arf_run_ex(ws.handle, o, RMS, 2, ptrs.data_ptr(), R.data_ptr(), G.data_ptr(), 1e-6,
+                          out.data_ptr(), R.data_ptr(), M, H, arf.ARF_BF16, s) == arf.ARF_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
