@@ -275,7 +275,8 @@ def test_rejected_calls_write_nothing(ws):
 
     assert call(W=0) == arf.ARF_ERR_UNSUPPORTED
     assert call(W=65) == arf.ARF_ERR_UNSUPPORTED
-    assert call(h=12) == arf.ARF_ERR_UNSUPPORTED
+    assert call(h=0) == arf.ARF_ERR_INVALID_ARG
+    assert call(h=-8) == arf.ARF_ERR_INVALID_ARG
     assert call(h=524296) == arf.ARF_ERR_UNSUPPORTED
     assert call(m=-1) == arf.ARF_ERR_INVALID_ARG
     assert call(pp=None) == arf.ARF_ERR_INVALID_ARG
@@ -287,9 +288,9 @@ def test_rejected_calls_write_nothing(ws):
     assert call(eps=float("inf")) == arf.ARF_ERR_INVALID_ARG
     assert call(eps=-1e-6) == arf.ARF_ERR_INVALID_ARG
     assert call(rr=o) == arf.ARF_ERR_INVALID_ARG                 # out == residual_out
-    assert call(oo=o + 2) == arf.ARF_ERR_UNSUPPORTED             # misaligned out
-    assert call(rr=r + 8) == arf.ARF_ERR_UNSUPPORTED             # misaligned residual_out
-    assert call(res=R.data_ptr() + 2) == arf.ARF_ERR_UNSUPPORTED
+    assert call(oo=o + 1) == arf.ARF_ERR_UNSUPPORTED             # odd address (2-byte offsets run elementwise)
+    assert call(rr=r + 9) == arf.ARF_ERR_UNSUPPORTED             # odd residual_out
+    assert call(res=R.data_ptr() + 3) == arf.ARF_ERR_UNSUPPORTED
     assert call(pattern=7) == arf.ARF_ERR_INVALID_ARG
     assert call(dt=5) == arf.ARF_ERR_INVALID_ARG
     bad = arf.Plan(path=arf.ARF_PATH_ROW, threads=48, vpt=1, cluster=1, grid=1, w_spec=2)  # not whole warps
