@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401  (re-exported C-ABI names)
     ARF_ERR_INVALID_ARG, ARF_ERR_UNSUPPORTED, ARF_FP16, ARF_MAX_H, ARF_MAX_W, ARF_OK, ARF_PATH_ASYNC, ARF_PATH_CLUSTER, ARF_PATH_ELEM,
     ARF_PATH_FLAT, ARF_PATH_ROW, ARF_STATIC_STAGING_BYTES, ArfError, DeviceCaps, Plan, RunOpts,
     arf_host_staging_bytes, arf_last_cuda_error, arf_plan_check, arf_plan_for_caps, arf_run, arf_run_ex,
+    arf_workspace_autotune,
     arf_run_host, arf_run_host_static, arf_run_planned, arf_status_string, arf_supports,
     arf_workspace_caps, arf_workspace_create, arf_workspace_destroy, arf_workspace_plan, load,
 )
@@ -64,6 +65,28 @@ class Workspace:
         if st != ARF_OK:
             raise ArfError(st, "arf_workspace_plan")
         return p
+
+    def autotune(self, pattern, partials, residual=None, gamma=None, eps: float = 0.0, out=None,
+                 residual_out=None, reps: int = 20, ptrs=None):
+        """arf_workspace_autotune on CUDA tensors (contiguous 16-bit layout);
+        returns (plan, microseconds per call). Later calls of the shape use it."""
+        torch = _torch()
+        pat = pattern_code(pattern)
+        P = list(partials)
+        M, H = P[0].shape
+        dev, dt = P[0].device, P[0].dtype
+        rms = pat == ARF_AR_RESIDUAL_RMSNORM
+        out = out if out is not None else torch.empty((M, H), dtype=dt, device=dev)
+        ro = residual_out if residual_out is not None else (torch.empty((M, H), dtype=dt, device=dev) if rms else None)
+        ptrs = ptrs if ptrs is not None else pointer_array(P, dev)
+        plan, us = Plan(), ctypes.c_float()
+        st = arf_workspace_autotune(self.handle, pat, len(P), ptrs.data_ptr(), residual.data_ptr() if rms else None,
+                                    gamma.data_ptr() if rms else None, float(eps), out.data_ptr(),
+                                    ro.data_ptr() if rms else None, M, H, dtype_code(dt), reps,
+                                    torch.cuda.current_stream(dev).cuda_stream, plan, us)
+        if st != ARF_OK:
+            raise ArfError(st, "arf_workspace_autotune", arf_last_cuda_error(self.handle) if st == ARF_ERR_CUDA else 0)
+        return plan, us.value
 
     def close(self):
         if self.handle:

@@ -88,6 +88,8 @@ _SIGNATURES = {
                                    _vp, _i64, _i64, _c.c_int, _vp]),
     "arf_run_ex": (_c.c_int, [_vp, _c.POINTER(RunOpts), _c.c_int, _c.c_int, _vp, _vp, _vp, _c.c_float, _vp, _vp,
                               _i64, _i64, _c.c_int, _vp]),
+    "arf_workspace_autotune": (_c.c_int, [_vp, _c.c_int, _c.c_int, _vp, _vp, _vp, _c.c_float, _vp, _vp, _i64, _i64,
+                                          _c.c_int, _c.c_int, _vp, _c.POINTER(Plan), _c.POINTER(_c.c_float)]),
     "arf_host_staging_bytes": (_c.c_size_t, [_c.c_int, _c.c_int, _i64, _i64, _c.c_int]),
     "arf_run_host": (_c.c_int, [_vp, _c.c_int, _c.c_int, _c.POINTER(_vp), _vp, _vp, _c.c_float, _vp, _vp, _i64,
                                 _i64, _c.c_int, _vp, _c.c_size_t, _vp]),
@@ -191,6 +193,14 @@ def arf_run_ex(ws, opts, pattern, W, partials, residual, gamma, eps, out, residu
         partials = ctypes.cast((ctypes.c_void_p * W)(*partials), ctypes.c_void_p)
     return load().arf_run_ex(ws, ctypes.byref(opts) if opts is not None else None, pattern, W, partials, residual,
                              gamma, eps, out, residual_out, M, H, dtype, stream)
+
+
+def arf_workspace_autotune(ws, pattern, W, partials_dev, residual, gamma, eps, out, residual_out, M, H, dtype, reps,
+                           stream, plan_out=None, us_out=None) -> int:
+    """plan_out: a Plan or None; us_out: a ctypes.c_float or None."""
+    return load().arf_workspace_autotune(ws, pattern, W, partials_dev, residual, gamma, eps, out, residual_out, M, H,
+                                         dtype, reps, stream, ctypes.byref(plan_out) if plan_out is not None else None,
+                                         ctypes.byref(us_out) if us_out is not None else None)
 
 
 def arf_host_staging_bytes(pattern, W, M, H, dtype) -> int:

@@ -5,7 +5,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <climits>
+#include <cstring>
 #include <map>
+#include <vector>
 #include <mutex>
 #include <new>
 #include <tuple>
@@ -583,6 +585,126 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
 }
 
 }  // namespace
+
+namespace {
+
+// Candidate plans around the planner's: every compiled shape near it that
+// arf_plan_check accepts on this device.
+std::vector<arf_plan_t> tune_candidates(const arf_device_caps_t& caps, const arf_plan_t& base,
+                                        arf_pattern_t pattern, int W, int64_t M, int64_t H, arf_dtype_t dtype) {
+    std::vector<arf_plan_t> out;
+    auto add = [&](const arf_plan_t& p) {
+        if (arf_plan_check(&caps, &p, pattern, W, M, H, dtype) != ARF_OK) return;
+        for (const auto& q : out)
+            if (std::memcmp(&q, &p, sizeof p) == 0) return;
+        out.push_back(p);
+    };
+    add(base);
+    if (base.path == ARF_PATH_ELEM) {
+        for (int t : {64, 128, 256, 512}) {
+            arf_plan_t p = base;
+            p.threads = t;
+            add(p);
+        }
+        return out;
+    }
+    const int w_specs[2] = {base.w_spec, 0};
+    if (pattern == ARF_ALLREDUCE) {
+        const int64_t nchunks = M * H / 8;
+        for (int ws : w_specs)
+            for (int t : {128, 256, 512})
+                for (int u : {1, 2, 4}) {
+                    arf_plan_t p = base;
+                    p.w_spec = ws;
+                    p.threads = t;
+                    p.vpt = u;
+                    const int64_t need = ceil_div(nchunks, (int64_t)t * u);
+                    p.grid = (int)(need < 1 ? 1 : (need > INT32_MAX ? INT32_MAX : need));
+                    add(p);
+                }
+        return out;
+    }
+    for (int ws : w_specs)
+        for (int cs : {1, 2, 4, 8, 16}) {
+            if (cs > caps.max_cluster) continue;
+            for (int vpt : {1, 2, 4, 8}) {
+                arf_plan_t p = rms_plan(caps, ws, M, H, cs, vpt);
+                if (p.vpt != vpt) continue;  // rms_plan raised it: covered by a larger vpt
+                add(p);
+            }
+        }
+    return out;
+}
+
+}  // namespace
+
+extern "C" arf_status_t arf_workspace_autotune(arf_workspace_t ws, arf_pattern_t pattern, int W,
+                                               const void* const* partials_dev, const void* residual,
+                                               const void* gamma, float eps, void* out, void* residual_out,
+                                               int64_t M, int64_t H, arf_dtype_t dtype, int reps, void* stream,
+                                               arf_plan_t* plan_out, float* us_out) {
+    if (!ws) return ARF_ERR_INVALID_ARG;
+    arf_status_t st = arf_supports(ws, pattern, W, M, H, dtype);
+    if (st != ARF_OK) return st;
+    if (reps <= 0) reps = 20;
+    arf_plan_t base;
+    st = device_plan(ws, pattern, W, M, H, dtype, &base);
+    if (st != ARF_OK) return st;
+    if (M == 0) {
+        if (plan_out) *plan_out = base;
+        if (us_out) *us_out = 0.0f;
+        return ARF_OK;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    cudaError_t e = cudaEventCreate(&e0);
+    if (e == cudaSuccess) e = cudaEventCreate(&e1);
+    if (e != cudaSuccess) {
+        if (e0) cudaEventDestroy(e0);
+        return cuda_fail(ws, e);
+    }
+    arf_plan_t best = base;
+    float best_us = -1.0f;
+    for (const arf_plan_t& cand : tune_candidates(ws->caps, base, pattern, W, M, H, dtype)) {
+        arf_run_opts_t o = {};
+        o.plan = &cand;
+        // warm-up; a plan this device cannot hold (UNSUPPORTED) is skipped
+        st = run_impl(ws, &o, pattern, W, partials_dev, residual, gamma, eps, out, residual_out, M, H, dtype, stream);
+        if (st == ARF_ERR_UNSUPPORTED) continue;
+        if (st != ARF_OK) break;
+        st = run_impl(ws, &o, pattern, W, partials_dev, residual, gamma, eps, out, residual_out, M, H, dtype, stream);
+        if (st != ARF_OK) break;
+        e = cudaEventRecord(e0, s);
+        for (int i = 0; i < reps && e == cudaSuccess && st == ARF_OK; ++i)
+            st = run_impl(ws, &o, pattern, W, partials_dev, residual, gamma, eps, out, residual_out, M, H, dtype,
+                          stream);
+        if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+        if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+        float ms = 0.0f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+        if (e != cudaSuccess || st != ARF_OK) break;
+        const float us = ms * 1000.0f / (float)reps;
+        if (best_us < 0.0f || us < best_us) {
+            best_us = us;
+            best = cand;
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (e != cudaSuccess) return cuda_fail(ws, e);
+    if (st != ARF_OK && st != ARF_ERR_UNSUPPORTED) return st;
+    {
+        std::lock_guard<std::mutex> lk(ws->mu);
+        ws->plans[std::make_tuple((int)pattern, W, M, H, (int)dtype)] = best;
+    }
+    if (ws->log)
+        std::fprintf(stderr, "[arf] autotune %s W=%d M=%lld H=%lld: path=%s threads=%d vpt=%d cluster=%d grid=%d "
+                     "w_spec=%d, %.3f us/call\n", pattern_name(pattern), W, (long long)M, (long long)H,
+                     path_name(best.path), best.threads, best.vpt, best.cluster, best.grid, best.w_spec, best_us);
+    if (plan_out) *plan_out = best;
+    if (us_out) *us_out = best_us;
+    return ARF_OK;
+}
 
 extern "C" arf_status_t arf_workspace_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64_t M, int64_t H,
                                            arf_dtype_t dtype, arf_plan_t* plan_out) {

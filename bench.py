@@ -365,7 +365,8 @@ def _e2e(ws, w, inp, pats, flush, dev, K, world, zero_copy):
 
 def sweep(ws, dev, flush, peak):
     """µs/call and GB/s for every workload, pattern and (k3_tp8) M, through
-    arf_run and through arf_run_ex with partials by value + PDL: cold
+    arf_run (planner's plan; and the plan arf_workspace_autotune picks, in a
+    workspace of its own) and through arf_run_ex with partials by value + PDL: cold
     (L2 flushed clean before each call, mean of 50 CUDA-event timings: the event
     clock ticks in steps of about 2 µs here, and the mean of many samples
     taken at random phases is unbiased where a median is not) and warm (a
@@ -378,6 +379,7 @@ def sweep(ws, dev, flush, peak):
 
     rows = []
     stream = torch.cuda.current_stream(dev)
+    ws_tuned = arf.Workspace(dev.index if dev.index is not None else 0)  # autotuned plans live here
     for name, w in wl.WORKLOADS.items():
         Ms = wl.K3_M_SWEEP if name == "k3_tp8" else (w.M,)
         for M in Ms:
@@ -387,8 +389,11 @@ def sweep(ws, dev, flush, peak):
             ptrs = arf.pointer_array(P, dev)
             out, ro = torch.empty_like(R), torch.empty_like(R)
             for pat in w.patterns:
-                def call(opt=False):
-                    arf.run(ws, pat, P, R, G, w.eps, out=out, residual_out=ro if pat == "rmsnorm" else None,
+                tuned_plan, tuned_us = ws_tuned.autotune(pat, P, R, G, w.eps, out=out,
+                                                         residual_out=ro if pat == "rmsnorm" else None, ptrs=ptrs)
+
+                def call(opt=False, wsx=None):
+                    arf.run(wsx or ws, pat, P, R, G, w.eps, out=out, residual_out=ro if pat == "rmsnorm" else None,
                             ptrs=ptrs, by_value=opt, pdl=opt)
 
                 def cold_us(opt, dirty=False):
@@ -405,14 +410,14 @@ def sweep(ws, dev, flush, peak):
                         ts.append(a.elapsed_time(b) * 1e3)
                     return statistics.mean(ts)
 
-                def warm_us(opt):
+                def warm_us(opt, wsx=None):
                     g = torch.cuda.CUDAGraph()
                     s = torch.cuda.Stream(dev)
                     s.wait_stream(stream)
                     with torch.cuda.stream(s):
                         with torch.cuda.graph(g, stream=s):
                             for _ in range(20):
-                                call(opt)
+                                call(opt, wsx)
                     stream.wait_stream(s)
                     torch.cuda.synchronize()
                     best = None
@@ -428,7 +433,7 @@ def sweep(ws, dev, flush, peak):
                     return best
 
                 us, us_opt, us_dirty = cold_us(False), cold_us(True), cold_us(False, dirty=True)
-                warm, warm_opt = warm_us(False), warm_us(True)
+                warm, warm_opt, warm_tuned = warm_us(False), warm_us(True), warm_us(False, ws_tuned)
                 nbytes = ww.bytes_per_call(pat)
                 plan = ws.plan(pat, w.W, M, w.H, torch.bfloat16 if w.dtype == "bf16" else torch.float16)
                 rows.append({"workload": name, "W": w.W, "M": M, "H": w.H, "dtype": w.dtype, "pattern": pat,
@@ -436,9 +441,13 @@ def sweep(ws, dev, flush, peak):
                              "gbs_cold": round(nbytes / us / 1e3, 1), "frac_cold": round(nbytes / us / 1e3 / peak, 4),
                              "us_cold_byvalue_pdl": round(us_opt, 3), "us_warm_graph_byvalue_pdl": round(warm_opt, 3),
                              "us_cold_write_only_flush": round(us_dirty, 3),
+                             "us_warm_graph_autotuned": round(warm_tuned, 3),
+                             "autotuned_plan": [tuned_plan.path, tuned_plan.threads, tuned_plan.vpt, tuned_plan.cluster,
+                                                tuned_plan.grid, tuned_plan.w_spec],
                              "plan": [plan.path, plan.threads, plan.vpt, plan.cluster, plan.grid, plan.w_spec]})
             del inp, P, R, G, out, ro, ptrs
             torch.cuda.empty_cache()
+    ws_tuned.close()
     return rows
 
 

@@ -215,6 +215,24 @@ arf_status_t arf_run(arf_workspace_t ws, arf_pattern_t pattern, int W,
                      void* out, void* residual_out,
                      int64_t M, int64_t H, arf_dtype_t dtype, void* stream);
 
+/* Measure candidate launch plans for these sizes on the caller's buffers and
+ * keep the fastest in the workspace: later arf_run calls of the same
+ * (pattern, W, M, H, dtype) use it. Candidates: the planner's plan and its
+ * neighbours (threads, chunks per thread, cluster size, compiled or run-time
+ * rank count) that pass arf_plan_check and fit the device. Each runs `reps`
+ * times (<= 0: 20) back to back on `stream`, timed with CUDA events after two
+ * warm-up calls; the call synchronises the stream, so it cannot be captured.
+ * Buffers and arguments are those of an arf_run call; the outputs are
+ * overwritten (with the values arf_run would write). The chosen plan is
+ * returned in plan_out and its mean time per call in us_out (either may be
+ * NULL). Errors: as arf_run. */
+arf_status_t arf_workspace_autotune(arf_workspace_t ws, arf_pattern_t pattern, int W,
+                                    const void* const* partials_dev,
+                                    const void* residual, const void* gamma, float eps,
+                                    void* out, void* residual_out,
+                                    int64_t M, int64_t H, arf_dtype_t dtype, int reps,
+                                    void* stream, arf_plan_t* plan_out, float* us_out);
+
 /* arf_run with an explicit launch plan instead of the planner's (tuning
  * sweeps and tests of every kernel shape). The plan must pass
  * arf_plan_check for the workspace's caps, and a cluster plan must be one the

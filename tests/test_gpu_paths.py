@@ -498,3 +498,22 @@ def test_zero_copy_host_buffers(ws, name, M):
     HostRunner(P, Rin, G, w.eps, out, Rin)
     torch.cuda.synchronize()
     assert_parity(d, RMS, (wl.codes(out), wl.codes(Rin)), oracle_run(RMS, inp), f"{name} zero-copy in place")
+
+
+@pytest.mark.parametrize("W,M,H,dtype", [(2, 128, 4096, "bf16"), (8, 1, 7168, "bf16"), (3, 37, 1000, "fp16"),
+                                         (4, 300, 7168, "bf16"), (2, 5, 13, "bf16")])
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_autotune_memoises_a_legal_plan(pattern, W, M, H, dtype):
+    """arf_workspace_autotune picks one of the candidate plans, later calls of
+    the shape use it, and results still match the oracle."""
+    with arf.Workspace(0) as ws:
+        inp = inputs(W, M, H, dtype)
+        P, R, G = to_device(inp)
+        plan, us = ws.autotune(pattern, P, R, G, inp.workload.eps, reps=5)
+        assert us > 0
+        caps = ws.caps
+        assert arf.arf_plan_check(caps, plan, pattern, W, M, H, DT[dtype]) == arf.ARF_OK
+        memo = ws.plan(pattern, W, M, H, wl.TORCH_DTYPE[dtype])
+        assert memo.as_dict() == plan.as_dict()
+        got = gpu_run(ws, pattern, P, R, G, inp.workload.eps)
+        assert_parity(DT[dtype], pattern, got, oracle_run(pattern, inp), f"autotuned {plan}")
