@@ -32,8 +32,10 @@ ARF_PATH_ROW = 1
 ARF_PATH_CLUSTER = 2
 ARF_PATH_ASYNC = 3
 ARF_PATH_ELEM = 4
+ARF_PATH_BULK = 5
 ARF_MAX_W = 64
-ARF_MAX_H = 32768
+ARF_MAX_H = 524288
+ARF_MAX_H_PER_CTA = 32768
 ARF_STATIC_STAGING_BYTES = 16 << 20
 
 STATUS_NAMES = {0: "ARF_OK", 1: "ARF_ERR_INVALID_ARG", 2: "ARF_ERR_UNSUPPORTED", 3: "ARF_ERR_CUDA",
@@ -64,7 +66,8 @@ class Plan(ctypes.Structure):
 class RunOpts(ctypes.Structure):
     _fields_ = [("plan", ctypes.POINTER(Plan)), ("partials_by_value", ctypes.c_int), ("pdl", ctypes.c_int),
                 ("ld_partials", ctypes.c_int64), ("ld_residual", ctypes.c_int64), ("ld_out", ctypes.c_int64),
-                ("ld_residual_out", ctypes.c_int64), ("partials_f32", ctypes.c_int)]
+                ("ld_residual_out", ctypes.c_int64), ("partials_f32", ctypes.c_int),
+                ("wait_limit_cycles", ctypes.c_int64), ("hold_first_copy", ctypes.c_int)]
 
 
 _c = ctypes
@@ -76,6 +79,7 @@ _SIGNATURES = {
     "arf_workspace_destroy": (_c.c_int, [_vp]),
     "arf_workspace_caps": (_c.c_int, [_vp, _c.POINTER(DeviceCaps)]),
     "arf_last_cuda_error": (_c.c_int, [_vp]),
+    "arf_workspace_wait_timeouts": (_c.c_int, [_vp, _c.POINTER(_c.c_uint)]),
     "arf_supports": (_c.c_int, [_vp, _c.c_int, _c.c_int, _i64, _i64, _c.c_int]),
     "arf_plan_for_caps": (_c.c_int, [_c.POINTER(DeviceCaps), _c.c_int, _c.c_int, _i64, _i64, _c.c_int,
                                      _c.POINTER(Plan)]),
@@ -155,6 +159,11 @@ def arf_workspace_caps(ws, caps_out: DeviceCaps) -> int:
 
 def arf_last_cuda_error(ws) -> int:
     return load().arf_last_cuda_error(ws)
+
+
+def arf_workspace_wait_timeouts(ws, count_out) -> int:
+    """count_out: a ctypes.c_uint."""
+    return load().arf_workspace_wait_timeouts(ws, ctypes.byref(count_out))
 
 
 def arf_supports(ws, pattern: int, W: int, M: int, H: int, dtype: int) -> int:

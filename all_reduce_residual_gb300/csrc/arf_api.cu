@@ -22,11 +22,13 @@ struct arf_workspace {
     std::mutex mu;
     std::map<std::tuple<int, int, int64_t, int64_t, int>, arf_plan_t> plans;
     std::atomic<int> last_err{0};
+    unsigned int* wait_timeouts = nullptr;  // device counter of the bulk kernel's given-up waits
 };
 
 namespace {
 
 using arf::kMaxThreads;
+constexpr int kBulkMaxRanks = 12;  // the planner's bulk-path limit
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool valid_pattern(int p) { return p == ARF_ALLREDUCE || p == ARF_AR_RESIDUAL_RMSNORM; }
@@ -60,9 +62,58 @@ arf_plan_t rms_plan(const arf_device_caps_t& caps, int w_spec, int64_t M, int64_
     return pl;
 }
 
+// One CTA per row with the fewest chunks per thread that keep it at <= 512
+// threads (rows of up to 8 x 512 chunks).
+arf_plan_t row_plan(const arf_device_caps_t& caps, int w_spec, int64_t M, int64_t H) {
+    int vpt = 1;
+    while (vpt < 8 && ceil_div(H / 8, vpt) > kMaxThreads) vpt *= 2;
+    return rms_plan(caps, w_spec, M, H, 1, vpt);
+}
+
+// The bulk-copy plan (ARF_PATH_BULK) for rows of H elements and W ranks:
+// column blocks of up to 512 chunks; two CTAs per SM with 2 ring slots each
+// when that fits (measured: a third slot, which costs the second CTA or
+// shares the SM's memory, was slower, e.g. W = 3: 29.4 vs 30.7 us), else one
+// CTA per SM with up to 4 slots; narrower blocks if not even 2 slots fit.
+// False if nothing fits.
+bool bulk_plan(const arf_device_caps_t& caps, int w_spec, int W, int64_t M, int64_t H, arf_plan_t* out) {
+    const int64_t C = H / 8;
+    const int64_t per_sm = (int64_t)caps.max_smem_per_block + 1024;  // the SM's shared memory
+    const int64_t fixed = C * 16 + arf::kBulkStaticSmem;             // row buffer + static
+    for (int B = (int)(C < kMaxThreads ? ceil_div(C, 32) * 32 : kMaxThreads); B >= 64; B /= 2) {
+        const int64_t slot = (int64_t)(W + 1) * B * 16;
+        for (int per = 2; per >= 1; --per) {
+            const int64_t budget = per == 2 ? per_sm / 2 - 1024 : caps.max_smem_per_block;
+            const int64_t s = (budget - fixed) / slot;
+            if (s < 2) continue;
+            arf_plan_t pl = {};
+            pl.path = ARF_PATH_BULK;
+            pl.threads = B;
+            pl.vpt = 1;
+            pl.cluster = 1;
+            pl.w_spec = w_spec;
+            const int64_t cap = per == 2 ? 2 : 4;
+            pl.stages = (int)(s < cap ? s : cap);
+            const int64_t g = (int64_t)caps.num_sms * per;
+            pl.grid = (int)(M < g ? (M > 0 ? M : 1) : g);
+            *out = pl;
+            return true;
+        }
+    }
+    return false;
+}
+
 const char* pattern_name(int p) { return p == ARF_ALLREDUCE ? "kAllReduce" : "kARResidualRMSNorm"; }
 const char* path_name(int p) {
-    return p == ARF_PATH_FLAT ? "flat" : p == ARF_PATH_ROW ? "row" : p == ARF_PATH_CLUSTER ? "cluster" : "async";
+    switch (p) {
+        case ARF_PATH_FLAT: return "flat";
+        case ARF_PATH_ROW: return "row";
+        case ARF_PATH_CLUSTER: return "cluster";
+        case ARF_PATH_ASYNC: return "async";
+        case ARF_PATH_ELEM: return "elem";
+        case ARF_PATH_BULK: return "bulk";
+        default: return "?";
+    }
 }
 
 }  // namespace
@@ -101,7 +152,10 @@ extern "C" arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out
         e = arf::configure_kernels_bf16(cl != 0, dyn);
         if (e == cudaSuccess) e = arf::configure_kernels_fp16(cl != 0, dyn);
     }
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&ws->wait_timeouts), 256);
+    if (e == cudaSuccess) e = cudaMemset(ws->wait_timeouts, 0, 256);
     if (e != cudaSuccess) {
+        if (ws->wait_timeouts) (void)cudaFree(ws->wait_timeouts);
         delete ws;
         (void)cudaGetLastError();
         return ARF_ERR_CUDA;
@@ -140,7 +194,31 @@ extern "C" arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out
 }
 
 extern "C" arf_status_t arf_workspace_destroy(arf_workspace_t ws) {
+    if (ws && ws->wait_timeouts) {
+        int cur = -1;
+        const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != ws->device &&
+                              cudaSetDevice(ws->device) == cudaSuccess;
+        (void)cudaFree(ws->wait_timeouts);
+        if (switched) (void)cudaSetDevice(cur);
+        (void)cudaGetLastError();
+    }
     delete ws;
+    return ARF_OK;
+}
+
+extern "C" arf_status_t arf_workspace_wait_timeouts(arf_workspace_t ws, unsigned int* count_out) {
+    if (!ws || !count_out) return ARF_ERR_INVALID_ARG;
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e == cudaSuccess && cur != ws->device) e = cudaSetDevice(ws->device);
+    unsigned int n = 0;
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&n, ws->wait_timeouts, sizeof n, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && n != 0) e = cudaMemset(ws->wait_timeouts, 0, sizeof n);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (cur >= 0 && cur != ws->device) (void)cudaSetDevice(cur);
+    if (e != cudaSuccess) return cuda_fail(ws, e);
+    *count_out = n;
     return ARF_OK;
 }
 
@@ -211,17 +289,18 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
         // clusters hold: the elementwise kernels
         pl = elem_plan(*caps, pattern, M, H);
     } else if (pattern == ARF_ALLREDUCE) {
-        // one pass over all chunks (no grid-stride trips); about 8 loads
-        // outstanding per thread when there is enough work to fill the
-        // device several times over, else one chunk per thread (latency:
-        // as many CTAs as the work allows)
+        // One pass over all chunks (no grid-stride trips). Bandwidth sizes:
+        // 256-thread CTAs with about 8 loads outstanding per thread. Sizes
+        // below two device-fulls of chunks (latency-bound): 128-thread CTAs
+        // with 2 chunks per thread (4 for W <= 2), the fastest shape in
+        // measured sweeps of decode-size calls on GB300.
         const int64_t nchunks = M * H / 8;
+        const bool small = nchunks < (int64_t)caps->num_sms * caps->max_threads_per_sm * 2;
         int u = 1;
-        if (w_spec > 0) u = w_spec <= 2 ? 4 : (w_spec <= 4 ? 2 : 1);
-        if (nchunks < (int64_t)caps->num_sms * caps->max_threads_per_sm * 2) u = 1;
+        if (w_spec > 0) u = w_spec <= 2 ? 4 : (w_spec <= 4 || small ? 2 : 1);
         while (!arf::flat_unroll_compiled(w_spec, u)) u /= 2;
         pl.path = ARF_PATH_FLAT;
-        pl.threads = 256;
+        pl.threads = small ? 128 : 256;
         pl.vpt = u;
         pl.cluster = 1;
         pl.w_spec = w_spec;
@@ -252,6 +331,18 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
             vpt = 1;
         }
         pl = rms_plan(*caps, w_spec, M, H, cs, vpt);
+        // One CTA per row without the register prefetch (rank count not
+        // compiled in, or too many vectors per thread): the bulk-copy ring
+        // keeps the loads in flight instead, for up to 12 ranks (wider ring
+        // slots leave too little shared memory for two of them). Measured on
+        // GB300 (fraction of the copy peak, row kernel -> bulk): W = 3, M =
+        // 2000: 0.49 -> 0.88; W = 5: 0.61 -> 0.85; W = 12: 0.61 -> 0.73;
+        // W = 4, H = 32768: 0.65 -> 0.81. With the prefetch the row kernel
+        // stays ahead (W = 4, M = 1989: 1.03 vs 0.93).
+        if (pl.path == ARF_PATH_ROW && !arf::rms_prefetches(pl.w_spec, pl.vpt) && W <= kBulkMaxRanks) {
+            arf_plan_t b;
+            if (bulk_plan(*caps, w_spec, W, M, H, &b)) pl = b;
+        }
         // The streaming kernel (ARF_PATH_ASYNC) is not chosen: measured on
         // GB300 it keeps fewer bytes in flight than the row kernel's register
         // prefetch (8 warps per SM issuing per-thread copies), e.g. 107 us vs
@@ -284,6 +375,13 @@ extern "C" arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_
         if (need > (size_t)caps->max_smem_per_block) return ARF_ERR_UNSUPPORTED;
         return ARF_OK;
     }
+    if (pl->path == ARF_PATH_BULK) {
+        if (pattern != ARF_AR_RESIDUAL_RMSNORM || pl->cluster != 1 || pl->vpt != 1) return ARF_ERR_UNSUPPORTED;
+        if (pl->stages < 2 || pl->stages > arf::kBulkMaxStages) return ARF_ERR_UNSUPPORTED;
+        const size_t need = arf::bulk_dyn_smem(W, pl->stages, pl->threads, (int)(H / 8)) + arf::kBulkStaticSmem;
+        if (need > (size_t)caps->max_smem_per_block) return ARF_ERR_UNSUPPORTED;
+        return ARF_OK;
+    }
     if (pl->stages != 0) return ARF_ERR_UNSUPPORTED;
     if (pattern == ARF_ALLREDUCE) {
         if (pl->path != ARF_PATH_FLAT || pl->cluster != 1) return ARF_ERR_UNSUPPORTED;
@@ -312,9 +410,9 @@ cudaError_t max_active_clusters(arf_dtype_t dt, const arf_plan_t& pl, int* n, bo
                           : arf::rms_max_active_clusters_fp16(pl, n, f32p);
 }
 
-cudaError_t max_active_blocks(arf_dtype_t dt, const arf_plan_t& pl, int64_t H, int* n) {
+cudaError_t max_active_blocks(arf_dtype_t dt, const arf_plan_t& pl, int64_t H, int W, int* n) {
     const int C = (int)(H / 8);
-    return dt == ARF_BF16 ? arf::rms_max_active_blocks_bf16(pl, C, n) : arf::rms_max_active_blocks_fp16(pl, C, n);
+    return dt == ARF_BF16 ? arf::rms_max_active_blocks_bf16(pl, C, W, n) : arf::rms_max_active_blocks_fp16(pl, C, W, n);
 }
 
 // The planner's plan, with the cluster size lowered until the cluster kernel
@@ -337,12 +435,21 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
     if (st != ARF_OK) return st;
     if (!capturing && pl.path == ARF_PATH_ASYNC) {
         int b = 0;
-        cudaError_t e = max_active_blocks(dtype, pl, H, &b);
+        cudaError_t e = max_active_blocks(dtype, pl, H, W, &b);
         if (e != cudaSuccess || b < 1) {  // the ring does not fit: one CTA per row instead
             (void)cudaGetLastError();
-            int vpt = 1;
-            while (vpt < 8 && ceil_div(H / 8, vpt) > kMaxThreads) vpt *= 2;
-            pl = rms_plan(ws->caps, pl.w_spec, M, H, 1, vpt);
+            pl = row_plan(ws->caps, pl.w_spec, M, H);
+        }
+    }
+    if (!capturing && pl.path == ARF_PATH_BULK) {
+        int b = 0;
+        cudaError_t e = max_active_blocks(dtype, pl, H, W, &b);
+        if (e == cudaSuccess && b > 0) {
+            const int64_t cap = (int64_t)ws->caps.num_sms * b;
+            if (cap < pl.grid) pl.grid = (int)cap;
+        } else {  // the ring does not fit after all: one CTA per row
+            (void)cudaGetLastError();
+            pl = row_plan(ws->caps, pl.w_spec, M, H);
         }
     }
     while (!capturing && pl.path == ARF_PATH_CLUSTER) {
@@ -362,7 +469,7 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
     if (st != ARF_OK) return st;
     if (!capturing && pl.path == ARF_PATH_ROW) {
         int b = 0;
-        cudaError_t e = max_active_blocks(dtype, pl, H, &b);
+        cudaError_t e = max_active_blocks(dtype, pl, H, W, &b);
         if (e == cudaSuccess && b > 0) {
             const int64_t cap = (int64_t)ws->caps.num_sms * b;
             if (cap < pl.grid) pl.grid = (int)cap;
@@ -453,7 +560,7 @@ void fill_common(arf::LaunchCommon& lc, const void* const* partials, int W, bool
 arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t pattern, int W,
                     const void* const* partials, bool by_value, bool pdl, const void* residual, const void* gamma,
                     float eps, void* out, void* residual_out, int64_t M, int64_t H, arf_dtype_t dtype,
-                    const Layout& L, cudaStream_t stream) {
+                    const Layout& L, cudaStream_t stream, const arf_run_opts_t* opts) {
     cudaError_t e;
     const bool bf = dtype == ARF_BF16;
     if (pl.path == ARF_PATH_ELEM) {
@@ -509,6 +616,9 @@ arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t patt
         p.slice = (int)ceil_div(p.C, pl.cluster);
         p.stages = pl.stages;
         p.eps = eps;
+        p.status = ws->wait_timeouts;
+        p.spin_limit = opts && opts->wait_limit_cycles > 0 ? (long long)opts->wait_limit_cycles : arf::kBulkSpinLimit;
+        p.hold_first = opts && opts->hold_first_copy ? 1 : 0;
         e = bf ? arf::launch_rms_bf16(p, pl, stream, L.f32p) : arf::launch_rms_fp16(p, pl, stream, L.f32p);
     }
     if (e != cudaSuccess) return cuda_fail(ws, e);
@@ -536,7 +646,8 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
         // an explicit 16-byte plan needs a layout those kernels take; binary32
         // partials exist only in the run-time-W instances of the row/flat kernels
         if (!L.vec_ok) return ARF_ERR_UNSUPPORTED;
-        if (L.f32p && (forced->w_spec != 0 || forced->path == ARF_PATH_ASYNC)) return ARF_ERR_UNSUPPORTED;
+        if (L.f32p && (forced->w_spec != 0 || forced->path == ARF_PATH_ASYNC || forced->path == ARF_PATH_BULK))
+            return ARF_ERR_UNSUPPORTED;
     }
     if (by_value) {
         for (int r = 0; r < W; ++r)
@@ -556,9 +667,9 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
             if (e != cudaSuccess) return cuda_fail(ws, e);
             if (n < 1) return ARF_ERR_UNSUPPORTED;
         }
-        if (pl.path == ARF_PATH_ASYNC && !capturing) {
+        if ((pl.path == ARF_PATH_ASYNC || pl.path == ARF_PATH_BULK) && !capturing) {
             int b = 0;
-            cudaError_t e = max_active_blocks(dtype, pl, H, &b);
+            cudaError_t e = max_active_blocks(dtype, pl, H, W, &b);
             if (e != cudaSuccess) return cuda_fail(ws, e);
             if (b < 1) return ARF_ERR_UNSUPPORTED;
         }
@@ -569,7 +680,10 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
             if (!L.vec_ok) {
                 pl = elem_plan(ws->caps, pattern, M, H);  // strides or alignment the vectors cannot take
             } else if (L.f32p) {
-                pl.w_spec = 0;  // binary32 partials: the run-time W instances
+                // binary32 partials: the run-time W instances of the row and
+                // flat kernels (the bulk ring holds 16-bit rows)
+                if (pl.path == ARF_PATH_BULK) pl = row_plan(ws->caps, 0, M, H);
+                pl.w_spec = 0;
                 if (pl.path == ARF_PATH_CLUSTER && !capturing) {
                     int n = 0;
                     if (max_active_clusters(dtype, pl, &n, true) != cudaSuccess || n < 1) {
@@ -581,7 +695,7 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
         }
     }
     return launch(ws, pl, pattern, W, partials, by_value, pdl, residual, gamma, eps, out, residual_out, M, H, dtype,
-                  L, stream);
+                  L, stream, opts);
 }
 
 }  // namespace
@@ -633,6 +747,22 @@ std::vector<arf_plan_t> tune_candidates(const arf_device_caps_t& caps, const arf
                 add(p);
             }
         }
+    // the bulk-copy ring: block widths, depths, one or two CTAs per SM
+    for (int ws : w_specs)
+        for (int t : {128, 256, 512})
+            for (int s : {2, 3, 4})
+                for (int per : {1, 2}) {
+                    arf_plan_t p = {};
+                    p.path = ARF_PATH_BULK;
+                    p.threads = t;
+                    p.vpt = 1;
+                    p.cluster = 1;
+                    p.w_spec = ws;
+                    p.stages = s;
+                    const int64_t g = (int64_t)caps.num_sms * per;
+                    p.grid = (int)(M < g ? (M > 0 ? M : 1) : g);
+                    add(p);
+                }
     return out;
 }
 

@@ -21,6 +21,10 @@ constexpr bool flat_unroll_compiled(int ws, int u) {
 }
 // Chunks per thread compiled for the RMS kernel.
 constexpr bool rms_vpt_compiled(int vpt) { return vpt == 1 || vpt == 2 || vpt == 4 || vpt == 8; }
+// Whether the row/cluster RMS kernel instance (ws, vpt) holds a whole row of
+// loads per thread in registers and issues the next row's before the row
+// barrier: the rank count compiled in and VPT*(W+1) <= 18 vectors.
+constexpr bool rms_prefetches(int ws, int vpt) { return ws > 0 && vpt * (ws + 1) <= 18; }
 
 // How a kernel finds the W partial pointers and when it may start.
 struct LaunchCommon {
@@ -64,8 +68,12 @@ struct RmsParams {
     int W;
     int cs;     // CTAs per row (cluster size), 1 = no cluster
     int slice;  // chunks per CTA: ceil(C / cs)
-    int stages; // streaming path: copy groups in flight per thread
+    int stages; // streaming / bulk paths: work items in flight
     float eps;
+    // bulk path (ARF_PATH_BULK) only
+    unsigned int* status;  // device counter: CTAs whose wait gave up
+    long long spin_limit;  // SM cycles a wait may take before giving up
+    int hold_first;        // testing the bounded waits: never issue item 0
 };
 
 // Elementwise kernels (arf_elem.cuh): any H, 2-byte alignment.
@@ -106,14 +114,25 @@ constexpr size_t async_dyn_smem(int W, int stages, int C) {
     return (size_t)stages * (size_t)(W + 1) * kAsyncCtaThreads * 16u + (size_t)C * 16u;
 }
 
+// The bulk-copy kernel (arf_bulk.cuh): at most this many ring slots; its
+// static shared memory; its dynamic shared memory for W ranks, `stages`
+// slots of `threads` chunks per rank and rows of C chunks.
+constexpr int kBulkMaxStages = 16;
+constexpr int kBulkStaticSmem = 1024;  // upper bound, for the planner
+constexpr size_t bulk_dyn_smem(int W, int stages, int threads, int C) {
+    return (size_t)stages * (size_t)(W + 1) * (size_t)threads * 16u + (size_t)C * 16u;
+}
+// Default wait limit of the bulk kernel: 2^31 SM cycles, about a second.
+constexpr long long kBulkSpinLimit = 1ll << 31;
+
 // How many clusters of plan.cluster CTAs of plan.threads threads the RMS
 // kernel instance of `plan` can keep resident at once (0 = cannot launch).
 cudaError_t rms_max_active_clusters_bf16(const arf_plan_t& plan, int* n, bool f32p = false);
 cudaError_t rms_max_active_clusters_fp16(const arf_plan_t& plan, int* n, bool f32p = false);
-// How many CTAs of the RMS kernel instance of `plan` (rows of C chunks) one
-// SM can hold.
-cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int C, int* n, bool f32p = false);
-cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int C, int* n, bool f32p = false);
+// How many CTAs of the RMS kernel instance of `plan` (rows of C chunks, W
+// ranks) one SM can hold.
+cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int C, int W, int* n, bool f32p = false);
+cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int C, int W, int* n, bool f32p = false);
 
 // Record a CUDA error as the workspace's last one (arf_last_cuda_error).
 void note_cuda_error(arf_workspace_t ws, cudaError_t e);

@@ -67,14 +67,20 @@ struct Pack8<__nv_bfloat16> {
 
 template <>
 struct Pack8<__half> {
+    // -0.0f + h with the sm_100 mixed-precision add: h is exactly
+    // representable in binary32, so the sum is h itself (+0 stays +0, -0
+    // stays -0); one FMA-pipe instruction instead of a conversion.
+    static __device__ __forceinline__ float widen1(unsigned short h) {
+        float f = -0.0f;
+        asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(f) : "h"(h));
+        return f;
+    }
     static __device__ __forceinline__ void widen(const uint4& v, float f[8]) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
-            float2 t = __half22float2(h);
-            f[2 * j] = t.x;
-            f[2 * j + 1] = t.y;
+            f[2 * j] = widen1((unsigned short)(w[j] & 0xffffu));
+            f[2 * j + 1] = widen1((unsigned short)(w[j] >> 16));
         }
     }
     static __device__ __forceinline__ uint4 narrow(const float f[8]) {
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(kMaxThreads) ar_flat_kernel(FlatParams p) {
 // ---------------------------------------------------------------------------
 template <int WS, int VPT>
 struct RmsShape {
-    static constexpr bool kPrefetch = WS > 0 && VPT * (WS + 1) <= 18;
+    static constexpr bool kPrefetch = rms_prefetches(WS, VPT);
     static constexpr bool kGammaRegs = VPT <= 2;  // else gamma is re-read from L1 per row
 };
 

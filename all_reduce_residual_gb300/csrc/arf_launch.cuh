@@ -2,6 +2,7 @@
 // arf_launch_bf16.cu and arf_launch_fp16.cu, which instantiate it once each.
 #pragma once
 
+#include "arf_bulk.cuh"
 #include "arf_elem.cuh"
 
 namespace arf {
@@ -89,6 +90,34 @@ RmsFn async_kernel_for(int ws) {
 }
 
 template <typename T>
+RmsFn bulk_kernel_for(int ws) {
+    switch (ws) {
+        case 0: return rms_bulk_kernel<T, 0>;
+        case 1: return rms_bulk_kernel<T, 1>;
+        case 2: return rms_bulk_kernel<T, 2>;
+        case 4: return rms_bulk_kernel<T, 4>;
+        case 8: return rms_bulk_kernel<T, 8>;
+        case 16: return rms_bulk_kernel<T, 16>;
+        default: return nullptr;
+    }
+}
+
+// The RMS kernel of a plan and its dynamic shared memory (rows of C chunks,
+// W ranks).
+template <typename T>
+RmsFn rms_fn_for(const arf_plan_t& plan, bool f32p) {
+    if (plan.path == ARF_PATH_ASYNC) return f32p ? nullptr : async_kernel_for<T>(plan.w_spec);
+    if (plan.path == ARF_PATH_BULK) return f32p ? nullptr : bulk_kernel_for<T>(plan.w_spec);
+    return rms_kernel_for<T>(plan.w_spec, plan.vpt, f32p);
+}
+
+inline size_t rms_dyn_smem(const arf_plan_t& plan, int C, int W) {
+    if (plan.path == ARF_PATH_ASYNC) return async_dyn_smem(plan.w_spec, plan.stages, C);
+    if (plan.path == ARF_PATH_BULK) return bulk_dyn_smem(W, plan.stages, plan.threads, C);
+    return 0;
+}
+
+template <typename T>
 cudaError_t launch_flat_t(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p) {
     FlatFn fn = flat_kernel_for<T>(plan.w_spec, plan.vpt, f32p);
     if (!fn) return cudaErrorInvalidValue;
@@ -108,15 +137,13 @@ cudaError_t launch_flat_t(const FlatParams& p, const arf_plan_t& plan, cudaStrea
 
 template <typename T>
 cudaError_t launch_rms_t(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p) {
-    const bool streaming = plan.path == ARF_PATH_ASYNC;
-    if (streaming && f32p) return cudaErrorInvalidValue;
-    RmsFn fn = streaming ? async_kernel_for<T>(plan.w_spec) : rms_kernel_for<T>(plan.w_spec, plan.vpt, f32p);
+    RmsFn fn = rms_fn_for<T>(plan, f32p);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.grid);
     cfg.blockDim = dim3((unsigned)plan.threads);
-    cfg.dynamicSmemBytes = streaming ? async_dyn_smem(plan.w_spec, plan.stages, p.C) : 0;
+    cfg.dynamicSmemBytes = rms_dyn_smem(plan, p.C, p.W);
     cfg.stream = s;
     unsigned n = 0;
     if (plan.cluster > 1) {
@@ -168,10 +195,11 @@ cudaError_t configure_kernels_t(bool clusters, int max_dyn_smem) {
                     if (e != cudaSuccess) return e;
                 }
     for (int ws : ws_list) {
-        RmsFn fn = async_kernel_for<T>(ws);
-        if (!fn) continue;
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
-        if (e != cudaSuccess) return e;
+        for (RmsFn fn : {async_kernel_for<T>(ws), bulk_kernel_for<T>(ws)}) {
+            if (!fn) continue;
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
+            if (e != cudaSuccess) return e;
+        }
     }
     return cudaSuccess;
 }
@@ -194,12 +222,10 @@ cudaError_t rms_max_active_clusters_t(const arf_plan_t& plan, int* n, bool f32p)
 }
 
 template <typename T>
-cudaError_t rms_max_active_blocks_t(const arf_plan_t& plan, int C, int* n, bool f32p) {
-    const bool streaming = plan.path == ARF_PATH_ASYNC;
-    RmsFn fn = streaming ? async_kernel_for<T>(plan.w_spec) : rms_kernel_for<T>(plan.w_spec, plan.vpt, f32p);
+cudaError_t rms_max_active_blocks_t(const arf_plan_t& plan, int C, int W, int* n, bool f32p) {
+    RmsFn fn = rms_fn_for<T>(plan, f32p);
     if (!fn) return cudaErrorInvalidValue;
-    const size_t smem = streaming ? async_dyn_smem(plan.w_spec, plan.stages, C) : 0;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fn, plan.threads, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fn, plan.threads, rms_dyn_smem(plan, C, W));
 }
 
 }  // namespace arf

@@ -19,8 +19,8 @@ cudaError_t rms_max_active_clusters_bf16(const arf_plan_t& plan, int* n, bool f3
     return rms_max_active_clusters_t<__nv_bfloat16>(plan, n, f32p);
 }
 
-cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int C, int* n, bool f32p) {
-    return rms_max_active_blocks_t<__nv_bfloat16>(plan, C, n, f32p);
+cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int C, int W, int* n, bool f32p) {
+    return rms_max_active_blocks_t<__nv_bfloat16>(plan, C, W, n, f32p);
 }
 
 }  // namespace arf

@@ -82,9 +82,16 @@ typedef enum arf_path {
                              256 threads per SM streams its rows in column
                              blocks of 256 chunks through a ring of `stages`
                              asynchronous shared-memory copies (cp.async) */
-    ARF_PATH_ELEM = 4     /* either pattern, any layout: one element per thread
+    ARF_PATH_ELEM = 4,    /* either pattern, any layout: one element per thread
                              per step (H not a multiple of 8, row strides not a
                              multiple of 8, tensors only 2-byte aligned) */
+    ARF_PATH_BULK = 5     /* kARResidualRMSNorm, 16-bit partials: each CTA
+                             walks its rows in column blocks of `threads`
+                             chunks; one thread keeps `stages` blocks in
+                             flight as TMA bulk copies (cp.async.bulk) into a
+                             shared-memory ring, completed on mbarriers by byte
+                             count. Its waits are bounded: see
+                             arf_workspace_wait_timeouts. */
 } arf_path_t;
 
 /* Limits of this build. */
@@ -115,7 +122,8 @@ typedef struct arf_plan {
     int w_spec;   /* rank count compiled into the kernel, or 0 for the generic
                      kernel that reads W at run time */
     int stages;   /* async path: copies in flight per thread, in column
-                     blocks (2..8); 0 on the other paths */
+                     blocks (2..8); bulk path: ring slots, in column blocks
+                     (2..16); 0 on the other paths */
 } arf_plan_t;
 
 typedef struct arf_workspace* arf_workspace_t;
@@ -139,6 +147,17 @@ arf_status_t arf_workspace_caps(arf_workspace_t ws, arf_device_caps_t* caps_out)
 
 /* The cudaError_t of the workspace's last ARF_ERR_CUDA (0 if none). */
 int arf_last_cuda_error(arf_workspace_t ws);
+
+/* Every wait of the bulk kernel (ARF_PATH_BULK) on its shared-memory ring is
+ * bounded (about a second by default, arf_run_opts_t.wait_limit_cycles): a
+ * CTA whose copies have not landed by then stops, waits (bounded again) for
+ * the copies it issued, adds 1 to a counter in the workspace's device memory
+ * and returns, so the context stays usable; that call's outputs are then
+ * incomplete. This waits for all work on the workspace's device
+ * (cudaDeviceSynchronize), reads the counter into *count_out and resets it
+ * to 0. Not during stream capture.
+ * Errors: NULL argument -> INVALID_ARG; a CUDA failure -> CUDA. */
+arf_status_t arf_workspace_wait_timeouts(arf_workspace_t ws, unsigned int* count_out);
 
 /* Static text for a status code (never NULL). */
 const char* arf_status_string(arf_status_t status);
@@ -273,6 +292,13 @@ typedef struct arf_run_opts {
                                 I/O dtype still applies to residual, gamma and
                                 the outputs); they enter the binary32 rank-order
                                 sum exactly; 4-byte alignment required */
+    int64_t wait_limit_cycles; /* bulk path: SM cycles a wait on a ring slot
+                                  may take before the CTA gives up (0 = the
+                                  default, 2^31, about a second) */
+    int hold_first_copy;     /* bulk path, for testing the bounded waits only:
+                                1 = every CTA leaves its first ring slot
+                                unfilled, so its first wait runs out; the call
+                                then produces no complete output */
 } arf_run_opts_t;
 
 /* arf_run with per-call options (NULL opts = arf_run). Same semantics,

@@ -50,6 +50,29 @@ def test_binding_covers_every_declared_symbol():
         assert callable(getattr(arf, n)), n
 
 
+def header_constants():
+    """Every `#define ARF_...` integer and every enumerator `ARF_... = n` of arf.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, expr in re.findall(r"#define\s+(ARF_\w+)\s+\(?([0-9u <]+)\)?\s*$", text, flags=re.M):
+        out[name] = eval(expr.replace("u", ""))  # integer literals and shifts only
+    for name, val in re.findall(r"\b(ARF_\w+)\s*=\s*(\d+)", text):
+        out[name] = int(val)
+    return out
+
+
+def test_binding_constants_match_the_header():
+    consts = header_constants()
+    for name in ("ARF_MAX_W", "ARF_MAX_H", "ARF_MAX_H_PER_CTA", "ARF_STATIC_STAGING_BYTES", "ARF_PATH_BULK",
+                 "ARF_PATH_ELEM", "ARF_ERR_DEVICE_MISMATCH"):
+        assert name in consts, name
+    mismatched = {n: (v, getattr(_binding, n)) for n, v in consts.items()
+                  if hasattr(_binding, n) and getattr(_binding, n) != v}
+    assert not mismatched, f"binding constant differs from arf.h: {mismatched}"
+    missing = [n for n in consts if n.startswith(("ARF_PATH_", "ARF_MAX_")) and not hasattr(_binding, n)]
+    assert not missing, missing
+
+
 def test_status_strings():
     for s in range(5):
         assert arf.arf_status_string(s)
@@ -94,6 +117,23 @@ def test_planner_plans_are_legal(pattern, W, M, H):
             assert M >= caps.num_sms and W in (1, 2, 4, 8, 16) and p.grid == caps.num_sms
             ring = p.stages * (W + 1) * 256 * 16 + (H // 8) * 16
             assert 3 <= p.stages <= 8 and ring + 1024 <= caps.max_smem_per_block
+            continue
+        C = H // 8
+        # the row kernel's chunks per thread, and whether it would prefetch
+        vpt = 1
+        while vpt < 8 and -(-C // vpt) > 512:
+            vpt *= 2
+        prefetch = W in (1, 2, 4, 8, 16) and vpt * (W + 1) <= 18
+        if p.path == arf.ARF_PATH_BULK:
+            # one CTA per row would run without the register prefetch: the bulk ring instead
+            assert pattern == arf.ARF_AR_RESIDUAL_RMSNORM and W <= 12 and not prefetch and C <= 4096
+            assert not (M < 16 and C >= 512 and caps.max_cluster > 1)  # decode-size wide rows split instead
+            assert p.cluster == 1 and p.vpt == 1 and p.threads in (64, 128, 256, 512)
+            assert p.threads == min(512, -(-C // 32) * 32) or p.threads < 512
+            ring = p.stages * (W + 1) * p.threads * 16 + C * 16 + 1024
+            per = 2 if 2 * ring <= caps.max_smem_per_block + 1024 - 2048 else 1
+            assert 2 <= p.stages <= (2 if per == 2 else 4) and ring <= caps.max_smem_per_block
+            assert p.grid == max(1, min(M, caps.num_sms * per))
             continue
         assert p.stages == 0
         if pattern == arf.ARF_ALLREDUCE:
@@ -210,6 +250,43 @@ def test_plan_check_rejects_bad_plans():
     assert arf.arf_plan_check(GB300, a, arf.ARF_ALLREDUCE, 16, 585, 7168, arf.ARF_FP16) == arf.ARF_ERR_UNSUPPORTED
 
 
+def test_bulk_plan_rules():
+    """ARF_PATH_BULK: kARResidualRMSNorm only, no cluster, vpt 1, 2..16 ring
+    slots, and (W+1) x slots x threads x 16 bytes of ring plus the 16-byte row
+    buffer must fit the opt-in shared memory (1 KiB kept for static use)."""
+    rms16 = (arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7168, arf.ARF_FP16)
+
+    def check(caps=GB300, args=rms16, **kw):
+        p = arf.Plan(path=arf.ARF_PATH_BULK, threads=128, vpt=1, cluster=1, grid=152, w_spec=16, stages=6)
+        for k, v in kw.items():
+            setattr(p, k, v)
+        return arf.arf_plan_check(caps, p, *args)
+
+    assert check() == arf.ARF_OK
+    assert check(w_spec=0) == arf.ARF_OK
+    assert check(w_spec=8) == arf.ARF_ERR_UNSUPPORTED
+    assert check(stages=1) == arf.ARF_ERR_UNSUPPORTED
+    assert check(stages=17) == arf.ARF_ERR_UNSUPPORTED
+    assert check(vpt=2) == arf.ARF_ERR_UNSUPPORTED
+    assert check(cluster=2, grid=304) == arf.ARF_ERR_UNSUPPORTED
+    assert check(args=(arf.ARF_ALLREDUCE, 16, 585, 7168, arf.ARF_FP16)) == arf.ARF_ERR_UNSUPPORTED
+    assert check(args=(arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7170, arf.ARF_FP16)) == arf.ARF_ERR_UNSUPPORTED
+    # shared memory: 17 x S x 128 x 16 + 896 x 16 + 1024 <= 232448  <=>  S <= 6
+    ring = lambda s, t=128, w=16, c=896: (w + 1) * s * t * 16 + c * 16 + 1024  # noqa: E731
+    assert ring(6) <= GB300.max_smem_per_block < ring(7)
+    assert check(stages=7) == arf.ARF_ERR_UNSUPPORTED
+    assert check(threads=64, stages=12) == arf.ARF_OK and ring(12, 64) <= 232448 < ring(13, 64)
+    assert check(threads=64, stages=13) == arf.ARF_ERR_UNSUPPORTED
+    tight = arf.DeviceCaps(152, 16, 2048, ring(6))
+    assert check(caps=tight) == arf.ARF_OK
+    tight.max_smem_per_block -= 16
+    assert check(caps=tight) == arf.ARF_ERR_UNSUPPORTED
+    # the row buffer alone: H = 32768 leaves room for fewer slots
+    long_rows = (arf.ARF_AR_RESIDUAL_RMSNORM, 2, 4, 32768, arf.ARF_BF16)
+    assert check(args=long_rows, w_spec=2, threads=512, stages=6) == arf.ARF_OK
+    assert check(args=long_rows, w_spec=2, threads=512, stages=7) == arf.ARF_ERR_UNSUPPORTED
+
+
 def test_staging_bytes():
     M, H, W = 128, 4096, 2
     plane = M * H * 2
@@ -235,3 +312,24 @@ def test_workspace_create_without_gpu_fails_cleanly():
     h = ctypes.c_void_p()
     assert arf.arf_workspace_create(0, h) == arf.ARF_ERR_CUDA
     assert not h.value
+
+
+def test_planner_bulk_choices():
+    """The bulk ring replaces one-CTA-per-row plans that would run without
+    the register prefetch, for up to 12 ranks; prefetching shapes, decode-size
+    wide rows (cluster path) and wider rank counts keep their kernels."""
+    def plan(W, M, H):
+        p = arf.Plan()
+        assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+        return p
+
+    p = plan(3, 2000, 7168)  # rank count not compiled in
+    assert (p.path, p.threads, p.grid, p.w_spec, p.stages) == (arf.ARF_PATH_BULK, 512, 304, 0, 2)
+    p = plan(12, 585, 7168)  # 13 x 8 KiB slots: one CTA per SM
+    assert (p.path, p.threads, p.grid, p.stages) == (arf.ARF_PATH_BULK, 512, 152, 2)
+    p = plan(4, 512, 32768)  # 8 chunks per thread in the row kernel
+    assert (p.path, p.threads, p.grid, p.stages, p.w_spec) == (arf.ARF_PATH_BULK, 512, 152, 4, 4)
+    for W, M, H, path in ((8, 1024, 7168, arf.ARF_PATH_ROW), (4, 1989, 7168, arf.ARF_PATH_ROW),
+                          (16, 585, 7168, arf.ARF_PATH_ROW), (24, 400, 7168, arf.ARF_PATH_ROW),
+                          (3, 4, 7168, arf.ARF_PATH_CLUSTER), (2, 128, 4096, arf.ARF_PATH_ROW)):
+        assert plan(W, M, H).path == path, (W, M, H)

@@ -1,0 +1,155 @@
+"""The bulk-copy kARResidualRMSNorm kernel (ARF_PATH_BULK) against the oracle:
+explicit plans over rank counts, ring depths, column-block widths (ragged last
+blocks included), grids smaller and larger than the row count, in-place
+residuals, row strides, and launch options; and its bounded waits: a ring
+slot that is never filled makes every CTA give up, count itself, and leave
+the context usable."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import all_reduce_residual_gb300 as arf
+import oracle
+import pins
+from all_reduce_residual_gb300 import workloads as wl
+from gpu_util import DT, assert_parity, gpu_run, oracle_run, to_device
+
+pytestmark = pytest.mark.gpu
+RMS = arf.ARF_AR_RESIDUAL_RMSNORM
+
+
+@pytest.fixture(scope="module")
+def ws():
+    with arf.Workspace(0) as w:
+        yield w
+
+
+def bulk(threads, stages, grid, w_spec):
+    return arf.Plan(path=arf.ARF_PATH_BULK, threads=threads, vpt=1, cluster=1, grid=grid, w_spec=w_spec,
+                    stages=stages)
+
+
+def legal(ws, plan, W, M, H, dtype="bf16"):
+    return arf.arf_plan_check(ws.caps, plan, RMS, W, M, H, arf.dtype_code(wl.TORCH_DTYPE[dtype])) == arf.ARF_OK
+
+
+def inputs(W, M, H, dtype, seed):
+    return wl.make_inputs(wl.custom(W, M, H, dtype, 0.7, 1e-6, config_id=3000 + seed))
+
+
+@pytest.mark.parametrize("W,M,H,dtype", [(1, 9, 8, "bf16"), (2, 37, 1000, "bf16"), (3, 5, 7168, "fp16"),
+                                         (8, 41, 7176, "bf16"), (16, 23, 7168, "fp16"), (16, 3, 4096, "bf16"),
+                                         (17, 6, 2056, "fp16"), (64, 2, 256, "bf16"), (4, 300, 264, "fp16"),
+                                         (4, 2, 32768, "bf16")])
+def test_bulk_plans(ws, W, M, H, dtype):
+    inp = inputs(W, M, H, dtype, W * 131 + M)
+    ref = oracle_run(RMS, inp)
+    P, R, G = to_device(inp)
+    w_specs = sorted({0, W if W in (1, 2, 4, 8, 16) else 0})
+    ran = 0
+    for threads in (32, 128, 256, 512):
+        for stages in (2, 3, 6, 16):
+            for grid in sorted({1, 7, M, 2 * M + 1}):
+                for w_spec in w_specs:
+                    plan = bulk(threads, stages, grid, w_spec)
+                    if not legal(ws, plan, W, M, H, dtype):
+                        continue
+                    got = gpu_run(ws, RMS, P, R, G, inp.workload.eps, plan=plan)
+                    assert_parity(DT[dtype], RMS, got, ref, f"{plan}")
+                    ran += 1
+    assert ran > 0
+
+
+def test_bulk_in_place_and_options(ws):
+    W, M, H = 16, 40, 7168
+    inp = inputs(W, M, H, "fp16", 7)
+    ref = oracle_run(RMS, inp)
+    P, R, G = to_device(inp)
+    plan = bulk(128, 4, 19, 16)
+    assert legal(ws, plan, W, M, H, "fp16")
+    assert_parity(oracle.FP16, RMS, gpu_run(ws, RMS, P, R, G, inp.workload.eps, plan=plan, in_place=True), ref,
+                  "in place")
+    for by_value, pdl in ((True, False), (False, True), (True, True)):
+        out, ro = arf.run(ws, RMS, P, R, G, inp.workload.eps, plan=plan, by_value=by_value, pdl=pdl)
+        torch.cuda.synchronize()
+        got = (wl.codes(out.cpu()), wl.codes(ro.cpu()))
+        assert_parity(oracle.FP16, RMS, got, ref, f"by_value={by_value} pdl={pdl}")
+
+
+@pytest.mark.parametrize("pads", [(8, 16, 24, 8), (0, 8, 0, 0), (64, 0, 8, 16)])
+def test_bulk_row_strides(ws, pads):
+    W, M, H = 4, 33, 4096
+    rng = np.random.default_rng(sum(pads))
+    d = oracle.BF16
+    Pc = [pins.nearest_codes(d, rng.standard_normal((M, H)) * 1.5) for _ in range(W)]
+    Rc = pins.nearest_codes(d, rng.standard_normal((M, H)))
+    Gc = pins.nearest_codes(d, 0.5 + rng.random(H))
+
+    def strided(codes, pad, fill=0x7FC1):
+        big = np.full((M, H + pad), fill, np.uint16)
+        big[:, :H] = codes
+        t = wl.from_codes(big, "bf16").cuda()
+        return t[:, :H], t
+
+    Pd = [strided(p, pads[0])[0] for p in Pc]
+    Rd = strided(Rc, pads[1])[0]
+    Od, Ob = strided(np.zeros((M, H), np.uint16), pads[2], 0x1234)
+    ROd, ROb = strided(np.zeros((M, H), np.uint16), pads[3], 0x1234)
+    G = wl.from_codes(Gc, "bf16").cuda()
+    arf.run(ws, RMS, Pd, Rd, G, 1e-6, out=Od, residual_out=ROd, plan=bulk(256, 3, 10, 4))
+    torch.cuda.synchronize()
+    ref = oracle.run(oracle.AR_RESIDUAL_RMSNORM, Pc, Rc, Gc, 1e-6, dtype=d)
+    got = (wl.codes(Od.cpu().contiguous()), wl.codes(ROd.cpu().contiguous()))
+    assert_parity(d, RMS, got, ref, f"pads={pads}")
+    for big in (Ob, ROb):
+        assert (wl.codes(big.cpu())[:, H:] == 0x1234).all(), "wrote outside the rows"
+
+
+def test_bulk_refuses_binary32_partials(ws):
+    M, H = 4, 64
+    P = [torch.zeros((M, H), dtype=torch.float32, device="cuda") for _ in range(2)]
+    R = torch.zeros((M, H), dtype=torch.bfloat16, device="cuda")
+    G = torch.ones((H,), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(arf.ArfError) as e:
+        arf.run(ws, RMS, P, R, G, 1e-6, plan=bulk(32, 2, 4, 0))
+    assert e.value.status == arf.ARF_ERR_UNSUPPORTED
+
+
+def run_opts_call(ws, P, R, G, out, ro, plan, **kw):
+    ptrs = arf.pointer_array(P)
+    M, H = R.shape
+    o = arf.RunOpts(plan=ctypes.pointer(plan), **kw)
+    st = arf.arf_run_ex(ws.handle, o, RMS, len(P), ptrs.data_ptr(), R.data_ptr(), G.data_ptr(), 1e-6,
+                        out.data_ptr(), ro.data_ptr(), M, H, arf.ARF_BF16, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    return st
+
+
+def timeouts(ws):
+    n = ctypes.c_uint(12345)
+    assert arf.arf_workspace_wait_timeouts(ws.handle, n) == arf.ARF_OK
+    return n.value
+
+
+def test_bulk_wait_gives_up_and_context_survives(ws):
+    """Every CTA leaves its first slot unfilled (hold_first_copy), so its first
+    wait runs out after wait_limit_cycles (about a millisecond here): each CTA
+    that owns rows counts itself once, and the next ordinary call is exact."""
+    W, M, H = 8, 24, 7168
+    inp = inputs(W, M, H, "bf16", 11)
+    ref = oracle_run(RMS, inp)
+    P, R, G = to_device(inp)
+    out, ro = torch.empty_like(R), torch.empty_like(R)
+    assert timeouts(ws) == 0
+    grid = 40  # 24 CTAs own rows, 16 own none and never wait
+    plan = bulk(128, 4, grid, 8)
+    st = run_opts_call(ws, P, R, G, out, ro, plan, wait_limit_cycles=2_000_000, hold_first_copy=1)
+    assert st == arf.ARF_OK
+    assert timeouts(ws) == M
+    assert timeouts(ws) == 0  # read-and-reset
+    st = run_opts_call(ws, P, R, G, out, ro, plan, wait_limit_cycles=2_000_000)
+    assert st == arf.ARF_OK
+    assert timeouts(ws) == 0
+    assert_parity(oracle.BF16, RMS, (wl.codes(out.cpu()), wl.codes(ro.cpu())), ref, "after the timeout")
