@@ -71,19 +71,21 @@ arf_plan_t row_plan(const arf_device_caps_t& caps, int w_spec, int64_t M, int64_
 }
 
 // The bulk-copy plan (ARF_PATH_BULK) for rows of H elements and W ranks:
-// column blocks of up to 512 chunks; two CTAs per SM with 2 ring slots each
-// when that fits (measured: a third slot, which costs the second CTA or
-// shares the SM's memory, was slower, e.g. W = 3: 29.4 vs 30.7 us), else one
-// CTA per SM with up to 4 slots; narrower blocks if not even 2 slots fit.
-// False if nothing fits.
+// column blocks of up to 512 chunks; as many CTAs per SM (up to 4, and at
+// most 2048 threads) as fit with 2 ring slots each, or else one CTA per SM
+// with up to 4 slots; narrower blocks if not even 2 slots fit. Measured on
+// GB300: more CTAs with 2 slots beat fewer with deeper rings (W = 3:
+// 29.4 us with 2 slots and 2 CTAs per SM, 30.7 us with 3 slots; W = 2,
+// M = 3315: 3 CTAs per SM 36.3 us, 2 CTAs 38.7 us). False if nothing fits.
 bool bulk_plan(const arf_device_caps_t& caps, int w_spec, int W, int64_t M, int64_t H, arf_plan_t* out) {
     const int64_t C = H / 8;
     const int64_t per_sm = (int64_t)caps.max_smem_per_block + 1024;  // the SM's shared memory
     const int64_t fixed = C * 16 + arf::kBulkStaticSmem;             // row buffer + static
     for (int B = (int)(C < kMaxThreads ? ceil_div(C, 32) * 32 : kMaxThreads); B >= 64; B /= 2) {
         const int64_t slot = (int64_t)(W + 1) * B * 16;
-        for (int per = 2; per >= 1; --per) {
-            const int64_t budget = per == 2 ? per_sm / 2 - 1024 : caps.max_smem_per_block;
+        for (int per = 4; per >= 1; --per) {
+            if ((int64_t)per * B > caps.max_threads_per_sm) continue;
+            const int64_t budget = per > 1 ? per_sm / per - 1024 : caps.max_smem_per_block;
             const int64_t s = (budget - fixed) / slot;
             if (s < 2) continue;
             arf_plan_t pl = {};
@@ -92,8 +94,7 @@ bool bulk_plan(const arf_device_caps_t& caps, int w_spec, int W, int64_t M, int6
             pl.vpt = 1;
             pl.cluster = 1;
             pl.w_spec = w_spec;
-            const int64_t cap = per == 2 ? 2 : 4;
-            pl.stages = (int)(s < cap ? s : cap);
+            pl.stages = per > 1 ? 2 : (int)(s < 4 ? s : 4);
             const int64_t g = (int64_t)caps.num_sms * per;
             pl.grid = (int)(M < g ? (M > 0 ? M : 1) : g);
             *out = pl;
@@ -339,7 +340,14 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
         // 2000: 0.49 -> 0.88; W = 5: 0.61 -> 0.85; W = 12: 0.61 -> 0.73;
         // W = 4, H = 32768: 0.65 -> 0.81. With the prefetch the row kernel
         // stays ahead (W = 4, M = 1989: 1.03 vs 0.93).
-        if (pl.path == ARF_PATH_ROW && !arf::rms_prefetches(pl.w_spec, pl.vpt) && W <= kBulkMaxRanks) {
+        // fp16 rows of 2 chunks per thread with W <= 4 and many rows: the
+        // prefetching fp16 instances stall on their loads far more than the
+        // bf16 ones (W = 2, M = 3315: 50.4 vs 38.8 us, same instruction
+        // count and DRAM bytes, whatever the data); the bulk ring does not
+        // (39.0 us), nor at W = 4, M = 5851 (99.9 -> 84.4 us) or W = 1
+        // (49.1 -> 43.4 us).
+        const bool fp16_rows = dtype == ARF_FP16 && pl.vpt == 2 && W <= 4 && M >= 2 * (int64_t)caps->num_sms;
+        if (pl.path == ARF_PATH_ROW && W <= kBulkMaxRanks && (!arf::rms_prefetches(pl.w_spec, pl.vpt) || fp16_rows)) {
             arf_plan_t b;
             if (bulk_plan(*caps, w_spec, W, M, H, &b)) pl = b;
         }

@@ -77,6 +77,18 @@ WORKLOADS = {
 }
 
 
+# Shapes beyond the five above, measured in the benchmark's sweep because the
+# planner sends them to the bulk-copy kernel: a rank count without a compiled
+# kernel (W = 3 and W = 12), fp16 rows of two chunks per thread with few ranks
+# (the 80 MiB shape in fp16), and rows of 32768 elements. Same input recipe.
+EXTRA_WORKLOADS = {
+    "w3_generic": Workload("w3_generic", 6, 3, 2000, 7168, "bf16", 0.5, 1e-6, ("rmsnorm",)),
+    "w12_generic": Workload("w12_generic", 7, 12, 585, 7168, "fp16", 0.1, 1e-6, ("rmsnorm",)),
+    "tp4_80mib_fp16": Workload("tp4_80mib_fp16", 8, 4, 5851, 7168, "fp16", 1.0, 1e-6, ("rmsnorm",)),
+    "h32768": Workload("h32768", 9, 4, 512, 32768, "bf16", 1.0, 1e-6, ("rmsnorm",)),
+}
+
+
 def custom(W: int, M: int, H: int, dtype: str = "bf16", sigma: float = 1.0,
            eps: float = 1e-6, config_id: int = 900) -> Workload:
     """An ad-hoc shape (edge cases in the tests) with the same recipe."""

@@ -39,7 +39,10 @@ sys.path.insert(0, ROOT)
 METRIC = "µs/call and achieved HBM GB/s (% of GB300 roofline) vs M, per W and pattern"
 FALLBACK_HBM_GBS = 6800.0
 PATTERNS = ("allreduce", "rmsnorm")
-KERNEL_SOURCE = os.path.join(ROOT, "all_reduce_residual_gb300", "csrc", "arf_kernels.cuh")
+# the kARResidualRMSNorm kernel of each plan path (arf_path_t order)
+KERNEL_OF_PATH = {0: "ar_flat_kernel", 1: "rms_kernel", 2: "rms_kernel", 3: "rms_async_kernel", 4: "rms_elem_kernel",
+                  5: "rms_bulk_kernel"}
+CSRC = os.path.join(ROOT, "all_reduce_residual_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -53,6 +56,11 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-config sweep table")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--pattern", choices=PATTERNS, default=None,
+                    help="time only this pattern of the workload (for profiling one kernel)")
+    ap.add_argument("--plan", default=None,
+                    help="explicit launch plan path,threads,vpt,cluster,grid,w_spec,stages for the step's calls "
+                         "(arf_plan_check rules; for profiling a kernel shape the planner does not pick)")
     return ap.parse_args()
 
 
@@ -113,15 +121,20 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def source_digests(kernel: str) -> dict:
+    """SHA-256 of each source file that defines `kernel`."""
+    files = ["arf_kernels.cuh"] + (["arf_bulk.cuh"] if kernel == "rms_bulk_kernel" else [])
+    return {f: hashlib.sha256(open(os.path.join(CSRC, f), "rb").read()).hexdigest() for f in files}
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source (else None)."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
-        src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
         e = rec.get(f"{kernel}/{workload}")
-        if e and e.get("kernel_source_sha256") == src:
+        if e and e.get("kernel_sources_sha256") == source_digests(kernel):
             return int(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -224,11 +237,16 @@ def run_arf(args):
     ws = arf.Workspace(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-    w = wl.WORKLOADS[args.workload]
-    pats = [p for p in PATTERNS if p in w.patterns]
+    w = {**wl.WORKLOADS, **wl.EXTRA_WORKLOADS}[args.workload]
+    pats = [p for p in PATTERNS if p in w.patterns and (args.pattern is None or p == args.pattern)]
     inp = wl.make_inputs(w)
     P = [p.to(dev) for p in inp.partials]
     R, G = inp.residual.to(dev), inp.gamma.to(dev)
+    plan = None
+    if args.plan:
+        f = [int(x) for x in args.plan.split(",")]
+        plan = arf.Plan(path=f[0], threads=f[1], vpt=f[2], cluster=f[3], grid=f[4], w_spec=f[5],
+                        stages=f[6] if len(f) > 6 else 0)
     ptrs = arf.pointer_array(P, dev)
     outs = {p: torch.empty_like(R) for p in pats}
     ro = torch.empty_like(R)
@@ -238,7 +256,8 @@ def run_arf(args):
     step_bytes = sum(bytes_call.values())
 
     def call(p):
-        arf.run(ws, p, P, R, G, w.eps, out=outs[p], residual_out=ro if p == "rmsnorm" else None, ptrs=ptrs)
+        arf.run(ws, p, P, R, G, w.eps, out=outs[p], residual_out=ro if p == "rmsnorm" else None, ptrs=ptrs,
+                plan=plan)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -269,7 +288,9 @@ def run_arf(args):
     dom = "rmsnorm" if "rmsnorm" in pats else pats[0]
     dom_s = statistics.mean(per_call[dom]) / 1e3
     achieved = bytes_call[dom] / dom_s / 1e9
-    kname = "rms_kernel" if dom == "rmsnorm" else "ar_flat_kernel"
+    dt_torch = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    plans = {p: (plan if plan is not None else ws.plan(p, w.W, w.M, w.H, dt_torch)) for p in pats}
+    kname = KERNEL_OF_PATH[plans[dom].path] if dom == "rmsnorm" else "ar_flat_kernel"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kname, args.workload),
                 "kernel": kname, "algorithmic_bytes_per_launch": bytes_call[dom], "peak_source": peak_src,
@@ -285,8 +306,8 @@ def run_arf(args):
                    "patterns": list(pats), "bytes_per_step": step_bytes,
                    "l2": flush.describe(),
                    "parallelism": f"replicas x{world}",
-                   "plans": {p: ws.plan(p, w.W, w.M, w.H, torch.bfloat16 if w.dtype == "bf16"
-                                        else torch.float16).as_dict() for p in pats}},
+                   "plans": {p: plans[p].as_dict() for p in pats},
+                   "plan_source": "explicit (--plan)" if plan is not None else "planner"},
         "us_per_call": {p: round(statistics.mean(v) * 1e3, 3) for p, v in per_call.items()},
         "roofline": roofline,
         "gpu_launches": len(pats) * K,
@@ -380,7 +401,7 @@ def sweep(ws, dev, flush, peak):
     rows = []
     stream = torch.cuda.current_stream(dev)
     ws_tuned = arf.Workspace(dev.index if dev.index is not None else 0)  # autotuned plans live here
-    for name, w in wl.WORKLOADS.items():
+    for name, w in list(wl.WORKLOADS.items()) + list(wl.EXTRA_WORKLOADS.items()):
         Ms = wl.K3_M_SWEEP if name == "k3_tp8" else (w.M,)
         for M in Ms:
             inp = wl.make_inputs(w, device=dev, M=M)
@@ -436,15 +457,17 @@ def sweep(ws, dev, flush, peak):
                 warm, warm_opt, warm_tuned = warm_us(False), warm_us(True), warm_us(False, ws_tuned)
                 nbytes = ww.bytes_per_call(pat)
                 plan = ws.plan(pat, w.W, M, w.H, torch.bfloat16 if w.dtype == "bf16" else torch.float16)
-                rows.append({"workload": name, "W": w.W, "M": M, "H": w.H, "dtype": w.dtype, "pattern": pat,
+                rows.append({"workload": name, "extra": name in wl.EXTRA_WORKLOADS,
+                             "W": w.W, "M": M, "H": w.H, "dtype": w.dtype, "pattern": pat,
                              "bytes": nbytes, "us_cold": round(us, 3), "us_warm_graph": round(warm, 3),
                              "gbs_cold": round(nbytes / us / 1e3, 1), "frac_cold": round(nbytes / us / 1e3 / peak, 4),
                              "us_cold_byvalue_pdl": round(us_opt, 3), "us_warm_graph_byvalue_pdl": round(warm_opt, 3),
                              "us_cold_write_only_flush": round(us_dirty, 3),
                              "us_warm_graph_autotuned": round(warm_tuned, 3),
                              "autotuned_plan": [tuned_plan.path, tuned_plan.threads, tuned_plan.vpt, tuned_plan.cluster,
-                                                tuned_plan.grid, tuned_plan.w_spec],
-                             "plan": [plan.path, plan.threads, plan.vpt, plan.cluster, plan.grid, plan.w_spec]})
+                                                tuned_plan.grid, tuned_plan.w_spec, tuned_plan.stages],
+                             "plan": [plan.path, plan.threads, plan.vpt, plan.cluster, plan.grid, plan.w_spec,
+                                      plan.stages]})
             del inp, P, R, G, out, ro, ptrs
             torch.cuda.empty_cache()
     ws_tuned.close()
@@ -506,8 +529,8 @@ def run_reference(args):
     import oracle
     from all_reduce_residual_gb300 import workloads as wl
 
-    w = wl.WORKLOADS[args.workload]
-    pats = [p for p in PATTERNS if p in w.patterns]
+    w = {**wl.WORKLOADS, **wl.EXTRA_WORKLOADS}[args.workload]
+    pats = [p for p in PATTERNS if p in w.patterns and (args.pattern is None or p == args.pattern)]
     inp = wl.make_inputs(w)
     codes = _codes(inp)
     oracle.default()

@@ -135,7 +135,9 @@ typedef struct arf_workspace* arf_workspace_t;
  * kernel can be launched with (the launch configuration is then derived
  * from these, as flashinfer PR #1507 "update allreduce to match trtllm",
  * Highlights, derives threads_per_block and cluster_size from the SM count).
- * Makes `device` current on the calling thread.
+ * Makes `device` current on the calling thread. Allocates the workspace's
+ * only device memory here: 256 bytes holding the bulk kernel's wait-timeout
+ * counter (arf_workspace_wait_timeouts); no later call allocates for it.
  * Errors: ws_out NULL -> INVALID_ARG; no such device or a CUDA failure -> CUDA. */
 arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out);
 

@@ -130,9 +130,15 @@ def test_planner_plans_are_legal(pattern, W, M, H):
             assert not (M < 16 and C >= 512 and caps.max_cluster > 1)  # decode-size wide rows split instead
             assert p.cluster == 1 and p.vpt == 1 and p.threads in (64, 128, 256, 512)
             assert p.threads == min(512, -(-C // 32) * 32) or p.threads < 512
-            ring = p.stages * (W + 1) * p.threads * 16 + C * 16 + 1024
-            per = 2 if 2 * ring <= caps.max_smem_per_block + 1024 - 2048 else 1
-            assert 2 <= p.stages <= (2 if per == 2 else 4) and ring <= caps.max_smem_per_block
+            per_sm = caps.max_smem_per_block + 1024
+
+            def fits(per, stages):
+                need = stages * (W + 1) * p.threads * 16 + C * 16 + 1024
+                room = per_sm // per - 1024 if per > 1 else caps.max_smem_per_block
+                return need <= room and per * p.threads <= caps.max_threads_per_sm
+
+            per = max(k for k in (1, 2, 3, 4) if fits(k, 2))  # the most CTAs per SM with 2 slots
+            assert p.stages == 2 if per > 1 else (2 <= p.stages <= 4 and fits(1, p.stages))
             assert p.grid == max(1, min(M, caps.num_sms * per))
             continue
         assert p.stages == 0
@@ -323,7 +329,7 @@ def test_planner_bulk_choices():
         assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
         return p
 
-    p = plan(3, 2000, 7168)  # rank count not compiled in
+    p = plan(3, 2000, 7168)  # rank count not compiled in: 2 x 4 x 8 KiB slots, 2 CTAs per SM
     assert (p.path, p.threads, p.grid, p.w_spec, p.stages) == (arf.ARF_PATH_BULK, 512, 304, 0, 2)
     p = plan(12, 585, 7168)  # 13 x 8 KiB slots: one CTA per SM
     assert (p.path, p.threads, p.grid, p.stages) == (arf.ARF_PATH_BULK, 512, 152, 2)
@@ -333,3 +339,10 @@ def test_planner_bulk_choices():
                           (16, 585, 7168, arf.ARF_PATH_ROW), (24, 400, 7168, arf.ARF_PATH_ROW),
                           (3, 4, 7168, arf.ARF_PATH_CLUSTER), (2, 128, 4096, arf.ARF_PATH_ROW)):
         assert plan(W, M, H).path == path, (W, M, H)
+    # fp16 rows of two chunks per thread with few ranks and many rows: the bulk ring
+    for W, M, H, path in ((2, 3315, 7168, arf.ARF_PATH_BULK), (4, 5851, 7168, arf.ARF_PATH_BULK),
+                          (1, 4972, 7168, arf.ARF_PATH_BULK), (8, 1024, 7168, arf.ARF_PATH_ROW),
+                          (2, 128, 7168, arf.ARF_PATH_ROW), (2, 8192, 4096, arf.ARF_PATH_ROW)):
+        p = arf.Plan()
+        assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_FP16, p) == arf.ARF_OK
+        assert p.path == path, (W, M, H)

@@ -1,6 +1,6 @@
-"""Parity of the CUDA path with the CPU oracle on every workload, at full
-size, through the C ABI with the planner's launch configuration (the one the
-benchmark times). residual_out and kAllReduce out must be bitwise equal;
+"""Parity of the CUDA path with the CPU oracle on every workload (and the
+extra shapes the benchmark's sweep measures), at full size, through the C
+ABI with the planner's launch configuration (the one the benchmark times). residual_out and kAllReduce out must be bitwise equal;
 kARResidualRMSNorm out within 1 ulp (see gpu_util)."""
 import pytest
 import torch
@@ -11,8 +11,9 @@ from gpu_util import DT, PAT, assert_parity, gpu_run, oracle_run, to_device
 
 pytestmark = pytest.mark.gpu
 
+ALL = {**wl.WORKLOADS, **wl.EXTRA_WORKLOADS}
 CASES = []
-for name, w in wl.WORKLOADS.items():
+for name, w in ALL.items():
     Ms = wl.K3_M_SWEEP if name == "k3_tp8" else (w.M,)
     for M in Ms:
         for pat in w.patterns:
@@ -27,9 +28,11 @@ def ws():
 
 @pytest.mark.parametrize("name,M,pattern", CASES, ids=[f"{n}-M{m}-{p}" for n, m, p in CASES])
 def test_workload_parity(ws, name, M, pattern):
-    inp = wl.make_inputs(wl.WORKLOADS[name], M=M)
+    inp = wl.make_inputs(ALL[name], M=M)
     P, R, G = to_device(inp)
     pat = PAT[pattern]
+    if name in wl.EXTRA_WORKLOADS:  # these shapes exist to exercise the bulk-copy kernel
+        assert ws.plan(pattern, len(P), M, inp.workload.H, P[0].dtype).path == arf.ARF_PATH_BULK
     got = gpu_run(ws, pat, P, R, G, inp.workload.eps)
     ref = oracle_run(pat, inp)
     n1 = assert_parity(DT[inp.workload.dtype], pat, got, ref, f"{name} M={M} {pattern}")
