@@ -153,3 +153,30 @@ def test_bulk_wait_gives_up_and_context_survives(ws):
     assert st == arf.ARF_OK
     assert timeouts(ws) == 0
     assert_parity(oracle.BF16, RMS, (wl.codes(out.cpu()), wl.codes(ro.cpu())), ref, "after the timeout")
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_bulk_fuzz(ws, case):
+    """Random rank counts, shapes, dtypes and legal bulk plans (any block width,
+    ring depth and grid), half of them in place; no wait may give up."""
+    rng = np.random.default_rng(5000 + case)
+    W = int(rng.choice([1, 2, 3, 4, 6, 8, 12, 16, 24, 33, 64]))
+    M = int(rng.choice([1, 3, 17, 150, 301]))
+    H = 8 * int(rng.choice([1, 5, 64, 130, 513, 896, 2048]))
+    dtype = str(rng.choice(["bf16", "fp16"]))
+    inp = wl.make_inputs(wl.custom(W, M, H, dtype, float(rng.choice([0.01, 1.0, 30.0])), 1e-6, config_id=6000 + case))
+    for _ in range(100):
+        plan = bulk(int(rng.choice([32, 64, 96, 128, 256, 384, 512])), int(rng.integers(2, 17)),
+                    int(rng.integers(1, 700)), int(rng.choice([0, W])) if W in (1, 2, 4, 8, 16) else 0)
+        if legal(ws, plan, W, M, H, dtype):
+            break
+    else:
+        pytest.skip("no legal bulk plan drawn for this shape")
+    P, R, G = to_device(inp)
+    try:
+        got = gpu_run(ws, RMS, P, R, G, inp.workload.eps, plan=plan, in_place=bool(case % 2))
+    except arf.ArfError as e:  # legal by the rules, but more shared memory than this device lets it have
+        assert e.status == arf.ARF_ERR_UNSUPPORTED
+        return
+    assert_parity(DT[dtype], RMS, got, oracle_run(RMS, inp), f"case {case}: W={W} M={M} H={H} {dtype} {plan}")
+    assert timeouts(ws) == 0

@@ -1,6 +1,8 @@
 """Seeded random cases on the GPU against the oracle: random rank counts,
 shapes (ragged ones included), dtypes, patterns, value scales, and either the
 planner's plan or a random legal plan of any kernel shape."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -31,9 +33,13 @@ def random_plan(rng, ws, pattern, W, M, H, dtype):
             p = arf.Plan(path=arf.ARF_PATH_FLAT, threads=int(rng.choice([32, 64, 128, 256, 512])),
                          vpt=int(rng.choice([1, 2, 4])), cluster=1, grid=int(rng.integers(1, 2000)), w_spec=w_spec)
         else:
-            kind = rng.integers(0, 3)
+            kind = rng.integers(0, 4)
             C = H // 8
-            if kind == 2 and W in (1, 2, 4, 8, 16):
+            if kind == 3:
+                p = arf.Plan(path=arf.ARF_PATH_BULK, threads=int(rng.choice([32, 64, 128, 256, 512])), vpt=1,
+                             cluster=1, grid=int(rng.integers(1, 600)), w_spec=w_spec,
+                             stages=int(rng.integers(2, 17)))
+            elif kind == 2 and W in (1, 2, 4, 8, 16):
                 p = arf.Plan(path=arf.ARF_PATH_ASYNC, threads=256, vpt=1, cluster=1,
                              grid=int(rng.integers(1, 200)), w_spec=W, stages=int(rng.integers(2, 9)))
             else:
@@ -69,6 +75,8 @@ def test_fuzz(ws, case):
     except arf.ArfError as e:  # a cluster or ring shape this device cannot keep resident
         assert plan is not None and (plan.cluster > 1 or plan.stages > 0) and e.status == arf.ARF_ERR_UNSUPPORTED
         return
+    n = ctypes.c_uint(0)
+    assert arf.arf_workspace_wait_timeouts(ws.handle, n) == arf.ARF_OK and n.value == 0, "a bulk wait gave up"
     if eps == 0.0 and pattern == RMS:
         # an all-zero row would give NaN in both; the seeded data has none
         pass
