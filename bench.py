@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-config sweep table")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--m", type=int, default=None, help="override the workload's row count M (for profiling)")
     ap.add_argument("--pattern", choices=PATTERNS, default=None,
                     help="time only this pattern of the workload (for profiling one kernel)")
     ap.add_argument("--plan", default=None,
@@ -238,6 +239,8 @@ def run_arf(args):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     w = {**wl.WORKLOADS, **wl.EXTRA_WORKLOADS}[args.workload]
+    if args.m is not None:
+        w = w.with_m(args.m)
     pats = [p for p in PATTERNS if p in w.patterns and (args.pattern is None or p == args.pattern)]
     inp = wl.make_inputs(w)
     P = [p.to(dev) for p in inp.partials]
@@ -385,7 +388,8 @@ def _e2e(ws, w, inp, pats, flush, dev, K, world, zero_copy):
 
 
 def sweep(ws, dev, flush, peak):
-    """µs/call and GB/s for every workload, pattern and (k3_tp8) M, through
+    """µs/call and GB/s for every workload, pattern and (k3_tp8) M, beside a
+    device-to-device copy of the same bytes timed the same way, through
     arf_run (planner's plan; and the plan arf_workspace_autotune picks, in a
     workspace of its own) and through arf_run_ex with partials by value + PDL: cold
     (L2 flushed clean before each call, mean of 50 CUDA-event timings: the event
@@ -401,6 +405,26 @@ def sweep(ws, dev, flush, peak):
     rows = []
     stream = torch.cuda.current_stream(dev)
     ws_tuned = arf.Workspace(dev.index if dev.index is not None else 0)  # autotuned plans live here
+
+    def copy_cold_us(nbytes):
+        """A plain device-to-device copy moving the same bytes (nbytes/2 read,
+        nbytes/2 written), timed like the calls: the practical peak at this size."""
+        half = max(16, nbytes // 2 // 16 * 16)
+        src = torch.empty(half, dtype=torch.uint8, device=dev)
+        dst = torch.empty(half, dtype=torch.uint8, device=dev)
+        for _ in range(5):
+            dst.copy_(src)
+        ts = []
+        for _ in range(50):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dst.copy_(src)
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.mean(ts)
+
     for name, w in list(wl.WORKLOADS.items()) + list(wl.EXTRA_WORKLOADS.items()):
         Ms = wl.K3_M_SWEEP if name == "k3_tp8" else (w.M,)
         for M in Ms:
@@ -454,6 +478,7 @@ def sweep(ws, dev, flush, peak):
                     return best
 
                 us, us_opt, us_dirty = cold_us(False), cold_us(True), cold_us(False, dirty=True)
+                us_copy = copy_cold_us(ww.bytes_per_call(pat))
                 warm, warm_opt, warm_tuned = warm_us(False), warm_us(True), warm_us(False, ws_tuned)
                 nbytes = ww.bytes_per_call(pat)
                 plan = ws.plan(pat, w.W, M, w.H, torch.bfloat16 if w.dtype == "bf16" else torch.float16)
@@ -463,6 +488,7 @@ def sweep(ws, dev, flush, peak):
                              "gbs_cold": round(nbytes / us / 1e3, 1), "frac_cold": round(nbytes / us / 1e3 / peak, 4),
                              "us_cold_byvalue_pdl": round(us_opt, 3), "us_warm_graph_byvalue_pdl": round(warm_opt, 3),
                              "us_cold_write_only_flush": round(us_dirty, 3),
+                             "us_cold_copy_same_bytes": round(us_copy, 3),
                              "us_warm_graph_autotuned": round(warm_tuned, 3),
                              "autotuned_plan": [tuned_plan.path, tuned_plan.threads, tuned_plan.vpt, tuned_plan.cluster,
                                                 tuned_plan.grid, tuned_plan.w_spec, tuned_plan.stages],
@@ -530,6 +556,8 @@ def run_reference(args):
     from all_reduce_residual_gb300 import workloads as wl
 
     w = {**wl.WORKLOADS, **wl.EXTRA_WORKLOADS}[args.workload]
+    if args.m is not None:
+        w = w.with_m(args.m)
     pats = [p for p in PATTERNS if p in w.patterns and (args.pattern is None or p == args.pattern)]
     inp = wl.make_inputs(w)
     codes = _codes(inp)
