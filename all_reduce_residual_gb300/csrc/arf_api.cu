@@ -291,14 +291,16 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
         pl = elem_plan(*caps, pattern, M, H);
     } else if (pattern == ARF_ALLREDUCE) {
         // One pass over all chunks (no grid-stride trips). Bandwidth sizes:
-        // 256-thread CTAs with about 8 loads outstanding per thread. Sizes
-        // below two device-fulls of chunks (latency-bound): 128-thread CTAs
-        // with 2 chunks per thread (4 for W <= 2), the fastest shape in
-        // measured sweeps of decode-size calls on GB300.
+        // 256-thread CTAs with 2 chunks per thread (4 for W <= 2) where the
+        // rank count is compiled in with W <= 8; measured on GB300 for W = 8,
+        // H = 7168: M = 1024 24.0 -> 23.0 us, M = 2048 40.0 -> 39.2 us against
+        // one chunk per thread. Sizes below two device-fulls of chunks
+        // (latency-bound): 128-thread CTAs with the same chunks per thread,
+        // the fastest shape in measured sweeps of decode-size calls.
         const int64_t nchunks = M * H / 8;
         const bool small = nchunks < (int64_t)caps->num_sms * caps->max_threads_per_sm * 2;
         int u = 1;
-        if (w_spec > 0) u = w_spec <= 2 ? 4 : (w_spec <= 4 || small ? 2 : 1);
+        if (w_spec > 0) u = w_spec <= 2 ? 4 : 2;
         while (!arf::flat_unroll_compiled(w_spec, u)) u /= 2;
         pl.path = ARF_PATH_FLAT;
         pl.threads = small ? 128 : 256;
