@@ -441,10 +441,11 @@ __device__ __forceinline__ void normalise_chunk(const uint4& xs, const uint4& gv
     st_out(dst, Pack8<T>::narrow(y));
 }
 
-template <typename T, int WS, int VPT, bool F32P = false>
+template <typename T, int WS, int VPT, bool F32P = false, bool ONE_ROW = false>
 __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
     using Shape = RmsShape<WS, VPT>;
     static_assert(!F32P || WS == 0, "binary32 partials use the run-time rank count");
+    static_assert(!ONE_ROW || Shape::kPrefetch, "the one-row form is the prefetching form without its row loop");
     __shared__ const uint4* s_ptr[ARF_MAX_W];
     __shared__ float s_warp[2][kMaxThreads / 32];  // per-warp partial sums, by row parity
     __shared__ float s_cta[2];                     // this CTA's partial, read by its peers
@@ -468,7 +469,42 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
     }
     __syncthreads();
 
-    if constexpr (Shape::kPrefetch) {
+    if constexpr (ONE_ROW) {
+        // Every cluster owns at most one row (grid >= rows): the same work as
+        // the first trip of the prefetching loop below, without the loop and
+        // the next-row prefetch (less code to fetch on a cold call).
+        const int64_t row = cluster_id;
+        if (row < p.M) {  // uniform over the cluster
+            uint4 L[VPT][WS + 1];
+            issue_row<WS, VPT>(L, s_ptr, p.residual, row * p.ly.ldp, row * p.ly.ldr, c0, c1);
+            const int64_t ob = row * p.ly.ldo, rob = row * p.ly.ldro;
+            uint4 xs[VPT];
+            float ss = 0.0f;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int c = c0 + warp_run_chunk<VPT>(k);
+                if (c < c1) {
+                    float acc[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+                    for (int r = 0; r < WS; ++r) accumulate<T>(acc, L[k][r]);
+                    xs[k] = residual_chunk<T>(acc, L[k][WS], p.residual_out + rob + c, ss);
+                }
+            }
+            const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, 0) / (float)p.H + p.eps);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int c = c0 + warp_run_chunk<VPT>(k);
+                if (c < c1) {
+                    uint4 gv;
+                    if constexpr (Shape::kGammaRegs) gv = g[k];
+                    else gv = ld_keep(p.gamma + c);
+                    normalise_chunk<T>(xs[k], gv, inv, p.out + ob + c);
+                }
+            }
+        }
+    } else if constexpr (Shape::kPrefetch) {
         uint4 L[VPT][WS + 1];
         int64_t row = cluster_id;
         if (row < p.M) issue_row<WS, VPT>(L, s_ptr, p.residual, row * p.ly.ldp, row * p.ly.ldr, c0, c1);

@@ -77,6 +77,30 @@ RmsFn rms_kernel_for(int ws, int vpt, bool f32p = false) {
     }
 }
 
+// The one-row form of the prefetching instances (grid covers every row).
+template <typename T, int WS>
+RmsFn one_row_by_vpt(int vpt) {
+    switch (vpt) {
+        case 1: if constexpr (rms_prefetches(WS, 1)) return rms_kernel<T, WS, 1, false, true>; else return nullptr;
+        case 2: if constexpr (rms_prefetches(WS, 2)) return rms_kernel<T, WS, 2, false, true>; else return nullptr;
+        case 4: if constexpr (rms_prefetches(WS, 4)) return rms_kernel<T, WS, 4, false, true>; else return nullptr;
+        case 8: if constexpr (rms_prefetches(WS, 8)) return rms_kernel<T, WS, 8, false, true>; else return nullptr;
+        default: return nullptr;
+    }
+}
+
+template <typename T>
+RmsFn one_row_kernel_for(int ws, int vpt) {
+    switch (ws) {
+        case 1: return one_row_by_vpt<T, 1>(vpt);
+        case 2: return one_row_by_vpt<T, 2>(vpt);
+        case 4: return one_row_by_vpt<T, 4>(vpt);
+        case 8: return one_row_by_vpt<T, 8>(vpt);
+        case 16: return one_row_by_vpt<T, 16>(vpt);
+        default: return nullptr;
+    }
+}
+
 template <typename T>
 RmsFn async_kernel_for(int ws) {
     switch (ws) {
@@ -103,11 +127,16 @@ RmsFn bulk_kernel_for(int ws) {
 }
 
 // The RMS kernel of a plan and its dynamic shared memory (rows of C chunks,
-// W ranks).
+// W ranks). one_row: every cluster of the grid owns at most one row, so the
+// prefetching instances may use their one-row form.
 template <typename T>
-RmsFn rms_fn_for(const arf_plan_t& plan, bool f32p) {
+RmsFn rms_fn_for(const arf_plan_t& plan, bool f32p, bool one_row = false) {
     if (plan.path == ARF_PATH_ASYNC) return f32p ? nullptr : async_kernel_for<T>(plan.w_spec);
     if (plan.path == ARF_PATH_BULK) return f32p ? nullptr : bulk_kernel_for<T>(plan.w_spec);
+    if (one_row && !f32p) {
+        RmsFn fn = one_row_kernel_for<T>(plan.w_spec, plan.vpt);
+        if (fn) return fn;
+    }
     return rms_kernel_for<T>(plan.w_spec, plan.vpt, f32p);
 }
 
@@ -137,7 +166,8 @@ cudaError_t launch_flat_t(const FlatParams& p, const arf_plan_t& plan, cudaStrea
 
 template <typename T>
 cudaError_t launch_rms_t(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p) {
-    RmsFn fn = rms_fn_for<T>(plan, f32p);
+    const bool one_row = (int64_t)(plan.grid / plan.cluster) >= p.M;
+    RmsFn fn = rms_fn_for<T>(plan, f32p, one_row);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = {};
@@ -188,8 +218,8 @@ cudaError_t configure_kernels_t(bool clusters, int max_dyn_smem) {
     if (clusters)
         for (int ws : ws_list)
             for (int vpt : vpt_list)
-                for (int f32p = 0; f32p < 2; ++f32p) {
-                    RmsFn fn = rms_kernel_for<T>(ws, vpt, f32p != 0);
+                for (int f32p = 0; f32p < 3; ++f32p) {
+                    RmsFn fn = f32p == 2 ? one_row_kernel_for<T>(ws, vpt) : rms_kernel_for<T>(ws, vpt, f32p != 0);
                     if (!fn) continue;
                     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
                     if (e != cudaSuccess) return e;
@@ -205,9 +235,12 @@ cudaError_t configure_kernels_t(bool clusters, int max_dyn_smem) {
 }
 
 template <typename T>
+// Occupancy answers cover both forms a plan may launch (the row loop and,
+// where it exists, the one-row form): the smaller of the two.
 cudaError_t rms_max_active_clusters_t(const arf_plan_t& plan, int* n, bool f32p) {
-    RmsFn fn = rms_kernel_for<T>(plan.w_spec, plan.vpt, f32p);
-    if (!fn) return cudaErrorInvalidValue;
+    RmsFn fns[2] = {rms_kernel_for<T>(plan.w_spec, plan.vpt, f32p),
+                    f32p ? nullptr : one_row_kernel_for<T>(plan.w_spec, plan.vpt)};
+    if (!fns[0]) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.grid);
@@ -218,14 +251,31 @@ cudaError_t rms_max_active_clusters_t(const arf_plan_t& plan, int* n, bool f32p)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(n, fn, &cfg);
+    int best = -1;
+    for (RmsFn fn : fns) {
+        if (!fn) continue;
+        int k = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&k, fn, &cfg);
+        if (e != cudaSuccess) return e;
+        best = best < 0 || k < best ? k : best;
+    }
+    *n = best;
+    return cudaSuccess;
 }
 
 template <typename T>
 cudaError_t rms_max_active_blocks_t(const arf_plan_t& plan, int C, int W, int* n, bool f32p) {
-    RmsFn fn = rms_fn_for<T>(plan, f32p);
-    if (!fn) return cudaErrorInvalidValue;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fn, plan.threads, rms_dyn_smem(plan, C, W));
+    int best = -1;
+    for (int one_row = 0; one_row < 2; ++one_row) {
+        RmsFn fn = rms_fn_for<T>(plan, f32p, one_row != 0);
+        if (!fn) return cudaErrorInvalidValue;
+        int k = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, fn, plan.threads, rms_dyn_smem(plan, C, W));
+        if (e != cudaSuccess) return e;
+        best = best < 0 || k < best ? k : best;
+    }
+    *n = best;
+    return cudaSuccess;
 }
 
 }  // namespace arf
