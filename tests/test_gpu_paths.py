@@ -517,3 +517,25 @@ def test_autotune_memoises_a_legal_plan(pattern, W, M, H, dtype):
         assert memo.as_dict() == plan.as_dict()
         got = gpu_run(ws, pattern, P, R, G, inp.workload.eps)
         assert_parity(DT[dtype], pattern, got, oracle_run(pattern, inp), f"autotuned {plan}")
+
+
+@pytest.mark.parametrize("W,M,H,vpt,cs", [(2, 40, 4096, 1, 1), (8, 33, 7168, 2, 1), (1, 9, 16384, 8, 1),
+                                          (16, 7, 7168, 1, 2), (4, 12, 8192, 1, 4), (8, 5, 7168, 1, 8)])
+def test_one_row_form_matches_the_row_loop(ws, W, M, H, vpt, cs):
+    """A grid that gives every cluster one row launches the one-row form; a
+    smaller grid of the same CTA shape runs the row loop. Both compute each
+    row with the same threads and reduction tree: outputs bitwise equal,
+    and both match the oracle."""
+    inp = inputs(W, M, H, "bf16", 0.8, cid=990 + W)
+    ref = oracle_run(RMS, inp)
+    P, R, G = to_device(inp)
+    C = H // 8
+    threads = max(32, -(-(-(-C // cs) // vpt) // 32) * 32)
+    path = arf.ARF_PATH_ROW if cs == 1 else arf.ARF_PATH_CLUSTER
+    got = []
+    for clusters in (M, max(1, M // 3)):  # one row per cluster; several rows per cluster
+        plan = arf.Plan(path=path, threads=threads, vpt=vpt, cluster=cs, grid=clusters * cs, w_spec=W)
+        assert arf.arf_plan_check(ws.caps, plan, RMS, W, M, H, arf.ARF_BF16) == arf.ARF_OK, plan
+        got.append(gpu_run(ws, RMS, P, R, G, inp.workload.eps, plan=plan))
+        assert_parity(oracle.BF16, RMS, got[-1], ref, f"{plan}")
+    assert np.array_equal(got[0][0], got[1][0]) and np.array_equal(got[0][1], got[1][1])
