@@ -180,3 +180,59 @@ def test_bulk_fuzz(ws, case):
         return
     assert_parity(DT[dtype], RMS, got, oracle_run(RMS, inp), f"case {case}: W={W} M={M} H={H} {dtype} {plan}")
     assert timeouts(ws) == 0
+
+
+@pytest.mark.parametrize("warm", [True, False])
+def test_bulk_graph_replay(ws, warm):
+    """A shape the planner sends to the bulk kernel (W = 3, no compiled rank
+    count), captured in a CUDA graph and replayed with new values in the same
+    buffers; warm=False makes the first call for the shape under capture."""
+    W, M, H = (3, 300, 7168) if warm else (3, 301, 7168)
+    P, R, G = to_device(inputs(W, M, H, "bf16", 40 + warm))
+    assert ws.plan(RMS, W, M, H, torch.bfloat16).path == arf.ARF_PATH_BULK
+    ptrs = arf.pointer_array(P)
+    out, ro = torch.empty_like(R), torch.empty_like(R)
+    if warm:
+        arf.run(ws, RMS, P, R, G, 1e-6, out=out, residual_out=ro, ptrs=ptrs)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            arf.run(ws, RMS, P, R, G, 1e-6, out=out, residual_out=ro, ptrs=ptrs)
+    for k in range(3):
+        inp = inputs(W, M, H, "bf16", 50 + k)
+        for dst, src in zip(P + [R, G], inp.partials + [inp.residual, inp.gamma]):
+            dst.copy_(src)
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.run(oracle.AR_RESIDUAL_RMSNORM, [wl.codes(p) for p in inp.partials], wl.codes(inp.residual),
+                         wl.codes(inp.gamma), 1e-6, dtype=oracle.BF16)
+        assert_parity(oracle.BF16, RMS, (wl.codes(out.cpu()), wl.codes(ro.cpu())), ref, f"replay {k}")
+    assert timeouts(ws) == 0
+
+
+def test_bulk_pdl_chain(ws):
+    """Bulk-kernel calls chained through their outputs, with programmatic
+    dependent launches: each waits for its predecessor's writes before its
+    first copy. Bitwise equal to the same chain without PDL."""
+    M, H = 200, 7168
+    base = [torch.randn((M, H), device="cuda").to(torch.bfloat16) for _ in range(3)]
+    G = torch.ones((H,), device="cuda", dtype=torch.bfloat16)
+    R = torch.randn((M, H), device="cuda").to(torch.bfloat16)
+
+    def chain(pdl):
+        x = base[0].clone()
+        outs = []
+        for _ in range(8):
+            y, _ = arf.run(ws, RMS, [x, base[1], base[2]], R, G, 1e-6, pdl=pdl)
+            outs.append(y)
+            x = y
+        torch.cuda.synchronize()
+        return [wl.codes(o.cpu()) for o in outs]
+
+    assert ws.plan(RMS, 3, M, H, torch.bfloat16).path == arf.ARF_PATH_BULK
+    ref = chain(False)
+    for _ in range(3):
+        for k, (a, b) in enumerate(zip(chain(True), ref)):
+            assert np.array_equal(a, b), f"step {k} differs under PDL"
