@@ -73,6 +73,14 @@ def test_binding_constants_match_the_header():
     assert not missing, missing
 
 
+def test_wait_timeouts_argument_errors():
+    """No workspace or no output: INVALID_ARG, without touching a device."""
+    n = ctypes.c_uint(7)
+    assert arf.arf_workspace_wait_timeouts(None, n) == arf.ARF_ERR_INVALID_ARG
+    assert n.value == 7
+    assert arf.load().arf_workspace_wait_timeouts(None, None) == arf.ARF_ERR_INVALID_ARG
+
+
 def test_status_strings():
     for s in range(5):
         assert arf.arf_status_string(s)
