@@ -97,6 +97,7 @@ _SIGNATURES = {
     "arf_host_staging_bytes": (_c.c_size_t, [_c.c_int, _c.c_int, _i64, _i64, _c.c_int]),
     "arf_run_host": (_c.c_int, [_vp, _c.c_int, _c.c_int, _c.POINTER(_vp), _vp, _vp, _c.c_float, _vp, _vp, _i64,
                                 _i64, _c.c_int, _vp, _c.c_size_t, _vp]),
+    "arf_read_pass": (_c.c_int, [_vp, _vp, _i64, _vp]),
     "arf_run_host_static": (_c.c_int, [_vp, _c.c_int, _c.c_int, _c.POINTER(_vp), _vp, _vp, _c.c_float, _vp, _vp,
                                        _i64, _i64, _c.c_int, _vp]),
 }
@@ -222,6 +223,10 @@ def arf_run_host(ws, pattern, W, partials_host, residual_host, gamma_host, eps, 
     arr = (ctypes.c_void_p * W)(*partials_host)
     return load().arf_run_host(ws, pattern, W, arr, residual_host, gamma_host, eps, out_host, residual_out_host,
                                M, H, dtype, staging_dev, staging_bytes, stream)
+
+
+def arf_read_pass(ws, buf, nbytes, stream) -> int:
+    return load().arf_read_pass(ws, buf, nbytes, stream)
 
 
 def arf_run_host_static(ws, pattern, W, partials_host, residual_host, gamma_host, eps, out_host,

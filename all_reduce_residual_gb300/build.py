@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libarf.so")
 
-SOURCES = ["arf_api.cu", "arf_launch_bf16.cu", "arf_launch_fp16.cu", "arf_static.cu"]
+SOURCES = ["arf_api.cu", "arf_launch_bf16.cu", "arf_launch_fp16.cu", "arf_static.cu", "arf_measure.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 # No fast-math and no automatic FMA contraction: the rank-order sum and the
 # normalisation are written with explicit IEEE operations.

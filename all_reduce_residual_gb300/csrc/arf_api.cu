@@ -990,3 +990,16 @@ extern "C" arf_status_t arf_run_host(arf_workspace_t ws, arf_pattern_t pattern, 
     if (e != cudaSuccess) return cuda_fail(ws, e);
     return ARF_OK;
 }
+
+extern "C" arf_status_t arf_read_pass(arf_workspace_t ws, const void* buf, int64_t bytes, void* stream) {
+    if (!ws || bytes < 0 || bytes % 16 != 0) return ARF_ERR_INVALID_ARG;
+    if (bytes == 0) return ARF_OK;
+    if (!buf || !aligned16(buf)) return ARF_ERR_INVALID_ARG;
+    // two CTAs of 512 threads per SM, grid-stride (measured the fastest
+    // shape for a plain read on GB300); the sink is a spare word of the
+    // workspace's device allocation, past the wait-timeout counter
+    cudaError_t e = arf::launch_read_pass(buf, bytes, 2 * ws->caps.num_sms, ws->wait_timeouts + 32,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(ws, e);
+    return ARF_OK;
+}

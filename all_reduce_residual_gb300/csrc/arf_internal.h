@@ -137,6 +137,9 @@ cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int C, int W, int
 // Record a CUDA error as the workspace's last one (arf_last_cuda_error).
 void note_cuda_error(arf_workspace_t ws, cudaError_t e);
 
+// The read-only measurement pass (arf_measure.cu): `grid` CTAs of 512 threads.
+cudaError_t launch_read_pass(const void* buf, int64_t bytes, int grid, unsigned int* sink, cudaStream_t s);
+
 // Host-buffer helper kernel launcher (arf_api.cu).
 cudaError_t launch_fill_pointer_array(const void** array, const char* first, int64_t stride, int W,
                                       cudaStream_t s);

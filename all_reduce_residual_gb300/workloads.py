@@ -58,6 +58,14 @@ class Workload:
     def with_m(self, M: int) -> "Workload":
         return replace(self, M=M)
 
+    def read_bytes_per_call(self, pattern: str) -> int:
+        """The reads among bytes_per_call: the partials, and for the RMS
+        pattern the residual and gamma."""
+        s, n = ELEM_BYTES, self.M * self.H
+        if pattern == "allreduce":
+            return self.W * n * s
+        return (self.W + 1) * n * s + self.H * s
+
     def bytes_per_call(self, pattern: str) -> int:
         """Algorithmic HBM bytes of one call: every partial element read once,
         the residual read once, gamma once, each output written once."""

@@ -425,6 +425,31 @@ def sweep(ws, dev, flush, peak):
             ts.append(a.elapsed_time(b) * 1e3)
         return statistics.mean(ts)
 
+    def read_cold_us(nbytes):
+        """arf_read_pass over as many bytes as the call reads, timed like the
+        calls: the read-only reference (on this GPU reads alone stream slower
+        than a copy's mix of reads and writes at these sizes)."""
+        n16 = max(16, (nbytes + 15) // 16 * 16)
+        buf = torch.zeros(n16, dtype=torch.uint8, device=dev)
+
+        def one():
+            st = arf.arf_read_pass(ws.handle, buf.data_ptr(), n16, stream.cuda_stream)
+            if st != arf.ARF_OK:
+                raise arf.ArfError(st, "arf_read_pass")
+
+        for _ in range(5):
+            one()
+        ts = []
+        for _ in range(50):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            one()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.mean(ts)
+
     for name, w in list(wl.WORKLOADS.items()) + list(wl.EXTRA_WORKLOADS.items()):
         Ms = wl.K3_M_SWEEP if name == "k3_tp8" else (w.M,)
         for M in Ms:
@@ -479,6 +504,7 @@ def sweep(ws, dev, flush, peak):
 
                 us, us_opt, us_dirty = cold_us(False), cold_us(True), cold_us(False, dirty=True)
                 us_copy = copy_cold_us(ww.bytes_per_call(pat))
+                us_read = read_cold_us(ww.read_bytes_per_call(pat))
                 warm, warm_opt, warm_tuned = warm_us(False), warm_us(True), warm_us(False, ws_tuned)
                 nbytes = ww.bytes_per_call(pat)
                 plan = ws.plan(pat, w.W, M, w.H, torch.bfloat16 if w.dtype == "bf16" else torch.float16)
@@ -489,6 +515,7 @@ def sweep(ws, dev, flush, peak):
                              "us_cold_byvalue_pdl": round(us_opt, 3), "us_warm_graph_byvalue_pdl": round(warm_opt, 3),
                              "us_cold_write_only_flush": round(us_dirty, 3),
                              "us_cold_copy_same_bytes": round(us_copy, 3),
+                             "us_cold_read_only_same_reads": round(us_read, 3),
                              "us_warm_graph_autotuned": round(warm_tuned, 3),
                              "autotuned_plan": [tuned_plan.path, tuned_plan.threads, tuned_plan.vpt, tuned_plan.cluster,
                                                 tuned_plan.grid, tuned_plan.w_spec, tuned_plan.stages],

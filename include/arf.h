@@ -373,6 +373,21 @@ arf_status_t arf_run_host_static(arf_workspace_t ws, arf_pattern_t pattern, int 
                                  void* out_host, void* residual_out_host,
                                  int64_t M, int64_t H, arf_dtype_t dtype, void* stream);
 
+/* ---- measurement ----------------------------------------------------- */
+
+/* Read `bytes` bytes at `buf` once, in 16-byte vectors from every SM, and
+ * discard them (nothing is written but, with vanishing probability, one word
+ * of the workspace's own device memory). No counterpart on the source pages:
+ * it is the roofline reference for calls that mostly read. On GB300 reads
+ * alone stream slower than a copy's mix of reads and writes at the sizes the
+ * epilogue runs at, so such a call is bounded by this pass over its reads.
+ * Asynchronous on `stream`; time it with events.
+ *   buf    device (or device-addressable host) memory, 16-byte aligned
+ *   bytes  a multiple of 16; 0 launches nothing
+ * Errors: NULL ws or buf (bytes > 0), misaligned buf, bytes < 0 or not a
+ * multiple of 16 -> INVALID_ARG; launch failure -> CUDA. */
+arf_status_t arf_read_pass(arf_workspace_t ws, const void* buf, int64_t bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

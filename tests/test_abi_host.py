@@ -73,6 +73,11 @@ def test_binding_constants_match_the_header():
     assert not missing, missing
 
 
+def test_read_pass_argument_errors():
+    """arf_read_pass checks its arguments before touching a device."""
+    assert arf.arf_read_pass(None, 256, 1024, None) == arf.ARF_ERR_INVALID_ARG
+
+
 def test_wait_timeouts_argument_errors():
     """No workspace or no output: INVALID_ARG, without touching a device."""
     n = ctypes.c_uint(7)

@@ -539,3 +539,17 @@ def test_one_row_form_matches_the_row_loop(ws, W, M, H, vpt, cs):
         got.append(gpu_run(ws, RMS, P, R, G, inp.workload.eps, plan=plan))
         assert_parity(oracle.BF16, RMS, got[-1], ref, f"{plan}")
     assert np.array_equal(got[0][0], got[1][0]) and np.array_equal(got[0][1], got[1][1])
+
+
+def test_read_pass(ws):
+    """The read-only measurement pass: reads, writes nothing it was given,
+    and checks alignment and size."""
+    buf = torch.arange(1 << 20, dtype=torch.int32, device="cuda")
+    keep = buf.clone()
+    s = torch.cuda.current_stream().cuda_stream
+    assert arf.arf_read_pass(ws.handle, buf.data_ptr(), buf.numel() * 4, s) == arf.ARF_OK
+    assert arf.arf_read_pass(ws.handle, buf.data_ptr(), 0, s) == arf.ARF_OK
+    assert arf.arf_read_pass(ws.handle, buf.data_ptr() + 4, 1024, s) == arf.ARF_ERR_INVALID_ARG
+    assert arf.arf_read_pass(ws.handle, buf.data_ptr(), 1000, s) == arf.ARF_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.equal(buf, keep)
