@@ -386,9 +386,11 @@ extern "C" arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_
         return ARF_OK;
     }
     if (pl->path == ARF_PATH_BULK) {
-        if (pattern != ARF_AR_RESIDUAL_RMSNORM || pl->cluster != 1 || pl->vpt != 1) return ARF_ERR_UNSUPPORTED;
+        if (pl->cluster != 1 || pl->vpt != 1) return ARF_ERR_UNSUPPORTED;
         if (pl->stages < 2 || pl->stages > arf::kBulkMaxStages) return ARF_ERR_UNSUPPORTED;
-        const size_t need = arf::bulk_dyn_smem(W, pl->stages, pl->threads, (int)(H / 8)) + arf::kBulkStaticSmem;
+        const size_t need = (pattern == ARF_ALLREDUCE ? arf::bulk_ar_dyn_smem(W, pl->stages, pl->threads)
+                                                      : arf::bulk_dyn_smem(W, pl->stages, pl->threads, (int)(H / 8))) +
+                            arf::kBulkStaticSmem;
         if (need > (size_t)caps->max_smem_per_block) return ARF_ERR_UNSUPPORTED;
         return ARF_OK;
     }
@@ -599,7 +601,23 @@ arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t patt
     rl.ldr = L.ldr / 8;
     rl.ldo = L.ldo / 8;
     rl.ldro = L.ldro / 8;
-    if (pattern == ARF_ALLREDUCE) {
+    if (pattern == ARF_ALLREDUCE && pl.path == ARF_PATH_BULK) {
+        arf::RmsParams p = {};
+        fill_common(p.lc, partials, W, by_value, pdl);
+        p.ly = rl;
+        p.out = static_cast<uint4*>(out);
+        p.M = M;
+        p.C = (int)(H / 8);
+        p.H = (int)H;
+        p.W = W;
+        p.cs = 1;
+        p.slice = p.C;
+        p.stages = pl.stages;
+        p.status = ws->wait_timeouts;
+        p.spin_limit = opts && opts->wait_limit_cycles > 0 ? (long long)opts->wait_limit_cycles : arf::kBulkSpinLimit;
+        p.hold_first = opts && opts->hold_first_copy ? 1 : 0;
+        e = bf ? arf::launch_bulk_ar_bf16(p, pl, stream) : arf::launch_bulk_ar_fp16(p, pl, stream);
+    } else if (pattern == ARF_ALLREDUCE) {
         arf::FlatParams p = {};
         fill_common(p.lc, partials, W, by_value, pdl);
         p.ly = rl;
@@ -679,7 +697,10 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
         }
         if ((pl.path == ARF_PATH_ASYNC || pl.path == ARF_PATH_BULK) && !capturing) {
             int b = 0;
-            cudaError_t e = max_active_blocks(dtype, pl, H, W, &b);
+            cudaError_t e = pattern == ARF_ALLREDUCE
+                                ? (dtype == ARF_BF16 ? arf::bulk_ar_max_active_blocks_bf16(pl, W, &b)
+                                                     : arf::bulk_ar_max_active_blocks_fp16(pl, W, &b))
+                                : max_active_blocks(dtype, pl, H, W, &b);
             if (e != cudaSuccess) return cuda_fail(ws, e);
             if (b < 1) return ARF_ERR_UNSUPPORTED;
         }

@@ -64,7 +64,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  : "memory");
 }
 
-template <typename T, int WS>
+// RMS = false: the kAllReduce form. Items carry the W partials only, every
+// thread stores rn(sum) of its chunk, and there is no row buffer or row
+// statistic; the ring, the producer and the bounded waits are the same.
+template <typename T, int WS, bool RMS = true>
 __global__ void __launch_bounds__(kMaxThreads) rms_bulk_kernel(RmsParams p) {
     extern __shared__ __align__(128) uint4 bulk_smem[];
     __shared__ const uint4* s_ptr[ARF_MAX_W];
@@ -74,15 +77,16 @@ __global__ void __launch_bounds__(kMaxThreads) rms_bulk_kernel(RmsParams p) {
     prologue(s_ptr, p.lc, p.W);
 
     const int W = WS > 0 ? WS : p.W;
+    const int NT = RMS ? W + 1 : W;  // segments per item: the partials (and the residual)
     const int B = blockDim.x, tid = threadIdx.x;
     const int S = p.stages, C = p.C;
     const int nb = (C + B - 1) / B;  // column blocks per row
-    uint4* ring = bulk_smem;                                   // [S][W+1][B]
-    uint4* xrow = bulk_smem + (size_t)S * (W + 1) * B;         // [C]: the row's rounded residual_out
+    uint4* ring = bulk_smem;                                   // [S][NT][B]
+    uint4* xrow = bulk_smem + (size_t)S * NT * B;              // [C]: the row's rounded residual_out (RMS)
     const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(s_bar);
     const uint32_t ring0 = (uint32_t)__cvta_generic_to_shared(ring);
     const uint32_t rank_bytes = (uint32_t)B * 16u;             // one segment's slot space
-    const uint32_t slot_bytes = (uint32_t)(W + 1) * rank_bytes;
+    const uint32_t slot_bytes = (uint32_t)NT * rank_bytes;
     const long long limit = p.spin_limit;
 
     if (tid == 0) {
@@ -103,10 +107,10 @@ __global__ void __launch_bounds__(kMaxThreads) rms_bulk_kernel(RmsParams p) {
         const uint32_t bar = bar0 + 8u * (uint32_t)in_slot;
         const uint32_t dst = ring0 + (uint32_t)in_slot * slot_bytes;
         if (!(p.hold_first && issued == 0)) {
-            mbar_arrive_expect_tx(bar, bytes * (uint32_t)(W + 1));
+            mbar_arrive_expect_tx(bar, bytes * (uint32_t)NT);
             const int64_t poff = in_row * p.ly.ldp + c0;
             for (int r = 0; r < W; ++r) bulk_load(dst + (uint32_t)r * rank_bytes, s_ptr[r] + poff, bytes, bar);
-            bulk_load(dst + (uint32_t)W * rank_bytes, p.residual + in_row * p.ly.ldr + c0, bytes, bar);
+            if constexpr (RMS) bulk_load(dst + (uint32_t)W * rank_bytes, p.residual + in_row * p.ly.ldr + c0, bytes, bar);
         }
         ++issued;
         if (++in_b == nb) {
@@ -130,7 +134,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_bulk_kernel(RmsParams p) {
             const bool ok = mbar_wait_bounded(bar0 + 8u * (uint32_t)slot, phase, limit);
             const int c = b * B + tid;
             if (ok && c < C) {
-                const uint4* src = ring + (size_t)slot * (W + 1) * B + tid;
+                const uint4* src = ring + (size_t)slot * NT * B + tid;
                 float acc[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
@@ -140,7 +144,8 @@ __global__ void __launch_bounds__(kMaxThreads) rms_bulk_kernel(RmsParams p) {
                 } else {
                     for (int r = 0; r < W; ++r) accumulate<T>(acc, src[(size_t)r * B]);
                 }
-                xrow[c] = residual_chunk<T>(acc, src[(size_t)W * B], p.residual_out + rob + c, ss);
+                if constexpr (RMS) xrow[c] = residual_chunk<T>(acc, src[(size_t)W * B], p.residual_out + rob + c, ss);
+                else st_out(p.out + ob + c, Pack8<T>::narrow(acc));
             }
             // every thread is done with this slot (or the CTA gives up)
             if (__syncthreads_or(!ok)) {
@@ -160,8 +165,10 @@ __global__ void __launch_bounds__(kMaxThreads) rms_bulk_kernel(RmsParams p) {
             }
         }
         if (failed) break;
-        const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
-        for (int c = tid; c < C; c += B) normalise_chunk<T>(xrow[c], ld_keep(p.gamma + c), inv, p.out + ob + c);
+        if constexpr (RMS) {
+            const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
+            for (int c = tid; c < C; c += B) normalise_chunk<T>(xrow[c], ld_keep(p.gamma + c), inv, p.out + ob + c);
+        }
     }
     if (failed && tid == 0) {
         // leave with no copy in flight into this CTA's shared memory

@@ -96,6 +96,12 @@ cudaError_t launch_flat_bf16(const FlatParams& p, const arf_plan_t& plan, cudaSt
 cudaError_t launch_flat_fp16(const FlatParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p);
 cudaError_t launch_rms_bf16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p);
 cudaError_t launch_rms_fp16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s, bool f32p);
+// kAllReduce on the bulk-copy kernel (ARF_PATH_BULK): RmsParams with the
+// residual, gamma and residual_out unused.
+cudaError_t launch_bulk_ar_bf16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s);
+cudaError_t launch_bulk_ar_fp16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s);
+cudaError_t bulk_ar_max_active_blocks_bf16(const arf_plan_t& plan, int W, int* n);
+cudaError_t bulk_ar_max_active_blocks_fp16(const arf_plan_t& plan, int W, int* n);
 cudaError_t launch_elem_bf16(const ElemParams& p, const arf_plan_t& plan, bool rms, cudaStream_t s, bool f32p);
 cudaError_t launch_elem_fp16(const ElemParams& p, const arf_plan_t& plan, bool rms, cudaStream_t s, bool f32p);
 
@@ -121,6 +127,10 @@ constexpr int kBulkMaxStages = 16;
 constexpr int kBulkStaticSmem = 1024;  // upper bound, for the planner
 constexpr size_t bulk_dyn_smem(int W, int stages, int threads, int C) {
     return (size_t)stages * (size_t)(W + 1) * (size_t)threads * 16u + (size_t)C * 16u;
+}
+// ... and of its kAllReduce form (partials only, no row buffer).
+constexpr size_t bulk_ar_dyn_smem(int W, int stages, int threads) {
+    return (size_t)stages * (size_t)W * (size_t)threads * 16u;
 }
 // Default wait limit of the bulk kernel: 2^31 SM cycles, about a second.
 constexpr long long kBulkSpinLimit = 1ll << 31;

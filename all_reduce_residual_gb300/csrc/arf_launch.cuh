@@ -126,6 +126,45 @@ RmsFn bulk_kernel_for(int ws) {
     }
 }
 
+template <typename T>
+RmsFn bulk_ar_kernel_for(int ws) {
+    switch (ws) {
+        case 0: return rms_bulk_kernel<T, 0, false>;
+        case 1: return rms_bulk_kernel<T, 1, false>;
+        case 2: return rms_bulk_kernel<T, 2, false>;
+        case 4: return rms_bulk_kernel<T, 4, false>;
+        case 8: return rms_bulk_kernel<T, 8, false>;
+        case 16: return rms_bulk_kernel<T, 16, false>;
+        default: return nullptr;
+    }
+}
+
+template <typename T>
+cudaError_t launch_bulk_ar_t(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s) {
+    RmsFn fn = bulk_ar_kernel_for<T>(plan.w_spec);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.grid);
+    cfg.blockDim = dim3((unsigned)plan.threads);
+    cfg.dynamicSmemBytes = bulk_ar_dyn_smem(p.W, plan.stages, plan.threads);
+    cfg.stream = s;
+    if (p.lc.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+template <typename T>
+cudaError_t bulk_ar_max_active_blocks_t(const arf_plan_t& plan, int W, int* n) {
+    RmsFn fn = bulk_ar_kernel_for<T>(plan.w_spec);
+    if (!fn) return cudaErrorInvalidValue;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fn, plan.threads, bulk_ar_dyn_smem(W, plan.stages, plan.threads));
+}
+
 // The RMS kernel of a plan and its dynamic shared memory (rows of C chunks,
 // W ranks). one_row: every cluster of the grid owns at most one row, so the
 // prefetching instances may use their one-row form.
@@ -225,7 +264,7 @@ cudaError_t configure_kernels_t(bool clusters, int max_dyn_smem) {
                     if (e != cudaSuccess) return e;
                 }
     for (int ws : ws_list) {
-        for (RmsFn fn : {async_kernel_for<T>(ws), bulk_kernel_for<T>(ws)}) {
+        for (RmsFn fn : {async_kernel_for<T>(ws), bulk_kernel_for<T>(ws), bulk_ar_kernel_for<T>(ws)}) {
             if (!fn) continue;
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
             if (e != cudaSuccess) return e;

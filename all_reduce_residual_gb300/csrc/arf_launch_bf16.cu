@@ -23,4 +23,11 @@ cudaError_t rms_max_active_blocks_bf16(const arf_plan_t& plan, int C, int W, int
     return rms_max_active_blocks_t<__nv_bfloat16>(plan, C, W, n, f32p);
 }
 
+cudaError_t launch_bulk_ar_bf16(const RmsParams& p, const arf_plan_t& plan, cudaStream_t s) {
+    return launch_bulk_ar_t<__nv_bfloat16>(p, plan, s);
+}
+cudaError_t bulk_ar_max_active_blocks_bf16(const arf_plan_t& plan, int W, int* n) {
+    return bulk_ar_max_active_blocks_t<__nv_bfloat16>(plan, W, n);
+}
+
 }  // namespace arf

@@ -87,12 +87,12 @@ typedef enum arf_path {
     ARF_PATH_ELEM = 4,    /* either pattern, any layout: one element per thread
                              per step (H not a multiple of 8, row strides not a
                              multiple of 8, tensors only 2-byte aligned) */
-    ARF_PATH_BULK = 5     /* kARResidualRMSNorm, 16-bit partials: each CTA
-                             walks its rows in column blocks of `threads`
-                             chunks; one thread keeps `stages` blocks in
-                             flight as TMA bulk copies (cp.async.bulk) into a
-                             shared-memory ring, completed on mbarriers by byte
-                             count. Its waits are bounded: see
+    ARF_PATH_BULK = 5     /* either pattern, 16-bit partials: each CTA walks
+                             its rows in column blocks of `threads` chunks;
+                             one thread keeps `stages` blocks in flight as TMA
+                             bulk copies (cp.async.bulk) into a shared-memory
+                             ring, completed on mbarriers by byte count. Its
+                             waits are bounded: see
                              arf_workspace_wait_timeouts. */
 } arf_path_t;
 

@@ -270,9 +270,10 @@ def test_plan_check_rejects_bad_plans():
 
 
 def test_bulk_plan_rules():
-    """ARF_PATH_BULK: kARResidualRMSNorm only, no cluster, vpt 1, 2..16 ring
-    slots, and (W+1) x slots x threads x 16 bytes of ring plus the 16-byte row
-    buffer must fit the opt-in shared memory (1 KiB kept for static use)."""
+    """ARF_PATH_BULK: no cluster, vpt 1, 2..16 ring slots, and (W+1) x slots x
+    threads x 16 bytes of ring plus the 16-byte row buffer (kAllReduce: W x
+    slots x threads x 16 bytes) must fit the opt-in shared memory (1 KiB kept
+    for static use)."""
     rms16 = (arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7168, arf.ARF_FP16)
 
     def check(caps=GB300, args=rms16, **kw):
@@ -288,7 +289,10 @@ def test_bulk_plan_rules():
     assert check(stages=17) == arf.ARF_ERR_UNSUPPORTED
     assert check(vpt=2) == arf.ARF_ERR_UNSUPPORTED
     assert check(cluster=2, grid=304) == arf.ARF_ERR_UNSUPPORTED
-    assert check(args=(arf.ARF_ALLREDUCE, 16, 585, 7168, arf.ARF_FP16)) == arf.ARF_ERR_UNSUPPORTED
+    # kAllReduce form: partials only, no row buffer: 16 x S x 128 x 16 + 1024 <= 232448  <=>  S <= 7
+    ar16 = (arf.ARF_ALLREDUCE, 16, 585, 7168, arf.ARF_FP16)
+    assert check(args=ar16, stages=7) == arf.ARF_OK
+    assert check(args=ar16, stages=8) == arf.ARF_ERR_UNSUPPORTED
     assert check(args=(arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7170, arf.ARF_FP16)) == arf.ARF_ERR_UNSUPPORTED
     # shared memory: 17 x S x 128 x 16 + 896 x 16 + 1024 <= 232448  <=>  S <= 6
     ring = lambda s, t=128, w=16, c=896: (w + 1) * s * t * 16 + c * 16 + 1024  # noqa: E731

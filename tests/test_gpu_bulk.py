@@ -17,7 +17,7 @@ from all_reduce_residual_gb300 import workloads as wl
 from gpu_util import DT, assert_parity, gpu_run, oracle_run, to_device
 
 pytestmark = pytest.mark.gpu
-RMS = arf.ARF_AR_RESIDUAL_RMSNORM
+RMS, AR = arf.ARF_AR_RESIDUAL_RMSNORM, arf.ARF_ALLREDUCE
 
 
 @pytest.fixture(scope="module")
@@ -236,3 +236,25 @@ def test_bulk_pdl_chain(ws):
     for _ in range(3):
         for k, (a, b) in enumerate(zip(chain(True), ref)):
             assert np.array_equal(a, b), f"step {k} differs under PDL"
+
+
+@pytest.mark.parametrize("W,M,H,dtype", [(1, 9, 8, "bf16"), (2, 37, 1000, "fp16"), (3, 5, 7168, "bf16"),
+                                         (8, 41, 7176, "bf16"), (16, 23, 7168, "fp16"), (64, 2, 256, "bf16"),
+                                         (4, 300, 264, "fp16")])
+def test_bulk_allreduce_plans(ws, W, M, H, dtype):
+    """The kAllReduce form of the bulk kernel: bitwise equal to the oracle for
+    every block width, ring depth and grid drawn."""
+    inp = inputs(W, M, H, dtype, 700 + W)
+    ref = oracle_run(AR, inp)
+    P, R, G = to_device(inp)
+    ran = 0
+    for threads in (32, 128, 512):
+        for stages in (2, 5, 16):
+            for grid in sorted({1, 7, M, 2 * M + 1}):
+                for w_spec in sorted({0, W if W in (1, 2, 4, 8, 16) else 0}):
+                    plan = bulk(threads, stages, grid, w_spec)
+                    if arf.arf_plan_check(ws.caps, plan, AR, W, M, H, arf.dtype_code(wl.TORCH_DTYPE[dtype])) != 0:
+                        continue
+                    assert_parity(DT[dtype], AR, gpu_run(ws, AR, P, R, G, 1e-6, plan=plan), ref, f"{plan}")
+                    ran += 1
+    assert ran > 0 and timeouts(ws) == 0
