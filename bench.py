@@ -318,7 +318,8 @@ def run_arf(args):
     }
     if not args.no_e2e:
         result["e2e"] = e2e_leg(ws, w, inp, pats, flush, dev, K, world)
-    if not args.no_sweep:
+    result["roofline_context"] = roofline_context(ws, dev, flush, w, dom, per_call[dom])
+    if not args.no_sweep and world == 1:  # the scaling runs (N > 1) time the headline only
         result["sweep"] = sweep(ws, dev, flush, peak)
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(w, inp, budget_s=10.0)
@@ -385,6 +386,55 @@ def _e2e(ws, w, inp, pats, flush, dev, K, world, zero_copy):
     return {"value": round(units / slowest / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": round(statistics.mean(times) * 1e3, 4),
             "api": api}
+
+
+def cold_event_us(fn, flush, stream, n=50):
+    """Mean CUDA-event time of fn() with the L2 flushed clean before each call."""
+    import torch
+
+    for _ in range(5):
+        fn()
+    ts = []
+    for _ in range(n):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    return statistics.mean(ts)
+
+
+def roofline_context(ws, dev, flush, w, pattern, call_ms):
+    """For the dominant call: the same-bytes device copy and the read-only
+    pass over its reads, timed like the call (cold). At decode sizes all three
+    sit at the launch-and-first-touch floor, which the HBM fraction cannot show."""
+    import torch
+
+    import all_reduce_residual_gb300 as arf
+
+    stream = torch.cuda.current_stream(dev)
+    nbytes, nread = w.bytes_per_call(pattern), w.read_bytes_per_call(pattern)
+    half = max(16, nbytes // 2 // 16 * 16)
+    src = torch.empty(half, dtype=torch.uint8, device=dev)
+    dst = torch.empty(half, dtype=torch.uint8, device=dev)
+    n16 = max(16, (nread + 15) // 16 * 16)
+    buf = torch.zeros(n16, dtype=torch.uint8, device=dev)
+
+    def read_pass():
+        st = arf.arf_read_pass(ws.handle, buf.data_ptr(), n16, stream.cuda_stream)
+        if st != arf.ARF_OK:
+            raise arf.ArfError(st, "arf_read_pass")
+
+    copy_us = cold_event_us(lambda: dst.copy_(src), flush, stream)
+    read_us = cold_event_us(read_pass, flush, stream)
+    call_us = statistics.mean(call_ms) * 1e3
+    return {"pattern": pattern, "call_us": round(call_us, 3), "copy_same_bytes_us": round(copy_us, 3),
+            "read_only_pass_same_reads_us": round(read_us, 3),
+            "call_over_read_only": round(call_us / read_us, 3),
+            "note": "the call's time against a device copy of its bytes and a read-only pass over its reads, "
+                    "all cold (L2 flushed) and event-timed"}
 
 
 def sweep(ws, dev, flush, peak):
