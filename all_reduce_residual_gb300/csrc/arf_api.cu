@@ -342,13 +342,18 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
         // 2000: 0.49 -> 0.88; W = 5: 0.61 -> 0.85; W = 12: 0.61 -> 0.73;
         // W = 4, H = 32768: 0.65 -> 0.81. With the prefetch the row kernel
         // stays ahead (W = 4, M = 1989: 1.03 vs 0.93).
-        // fp16 rows of 2 chunks per thread with W <= 4 and many rows: the
-        // prefetching fp16 instances stall on their loads far more than the
-        // bf16 ones (W = 2, M = 3315: 50.4 vs 38.8 us, same instruction
-        // count and DRAM bytes, whatever the data); the bulk ring does not
-        // (39.0 us), nor at W = 4, M = 5851 (99.9 -> 84.4 us) or W = 1
-        // (49.1 -> 43.4 us).
-        const bool fp16_rows = dtype == ARF_FP16 && pl.vpt == 2 && W <= 4 && M >= 2 * (int64_t)caps->num_sms;
+        // fp16 rows of 2 chunks per thread with few ranks, once every CTA
+        // loops over several rows: the prefetching fp16 instances then stall
+        // on their loads far more than the bf16 ones (W = 2, M = 3315: 50.4
+        // vs 38.8 us, same instruction count and DRAM bytes, whatever the
+        // data); with one row per CTA they match bf16. Measured crossover
+        // (fp16, H = 7168, row -> bulk): W <= 2 ties from M = 2 SMs and wins
+        // from M = 800 (W = 2, M = 1024: 20.2 -> 16.4 us); W = 4 loses at
+        // M = 304 (10.4 vs 12.2 us), ties to M = 1500 and wins from 8 SMs'
+        // worth (M = 2400: 40.8 -> 38.1 us; M = 5851: 99.9 -> 84.4 us).
+        const int64_t sms = caps->num_sms;
+        const bool fp16_rows = dtype == ARF_FP16 && pl.vpt == 2 &&
+                               ((W <= 2 && M >= 2 * sms) || (W <= 4 && M >= 8 * sms));
         if (pl.path == ARF_PATH_ROW && W <= kBulkMaxRanks && (!arf::rms_prefetches(pl.w_spec, pl.vpt) || fp16_rows)) {
             arf_plan_t b;
             if (bulk_plan(*caps, w_spec, W, M, H, &b)) pl = b;

@@ -359,7 +359,9 @@ def test_planner_bulk_choices():
     # fp16 rows of two chunks per thread with few ranks and many rows: the bulk ring
     for W, M, H, path in ((2, 3315, 7168, arf.ARF_PATH_BULK), (4, 5851, 7168, arf.ARF_PATH_BULK),
                           (1, 4972, 7168, arf.ARF_PATH_BULK), (8, 1024, 7168, arf.ARF_PATH_ROW),
-                          (2, 128, 7168, arf.ARF_PATH_ROW), (2, 8192, 4096, arf.ARF_PATH_ROW)):
+                          (2, 128, 7168, arf.ARF_PATH_ROW), (2, 8192, 4096, arf.ARF_PATH_ROW),
+                          (2, 304, 7168, arf.ARF_PATH_BULK), (4, 304, 7168, arf.ARF_PATH_ROW),
+                          (4, 1215, 7168, arf.ARF_PATH_ROW), (4, 1216, 7168, arf.ARF_PATH_BULK)):
         p = arf.Plan()
         assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_FP16, p) == arf.ARF_OK
         assert p.path == path, (W, M, H)
