@@ -62,6 +62,14 @@ arf_plan_t rms_plan(const arf_device_caps_t& caps, int w_spec, int64_t M, int64_
     return pl;
 }
 
+// Whether a row plan should launch one CTA per row (grid = M, the kernel's
+// one-row form) rather than a resident grid looping over rows: W = 2 and 4
+// at two chunks per thread, measured faster that way (the planner's RMS
+// branch gives the numbers).
+bool one_row_grid_wanted(const arf_plan_t& pl, int W) {
+    return pl.path == ARF_PATH_ROW && pl.vpt == 2 && (W == 2 || W == 4) && pl.w_spec == W;
+}
+
 // One CTA per row with the fewest chunks per thread that keep it at <= 512
 // threads (rows of up to 8 x 512 chunks).
 arf_plan_t row_plan(const arf_device_caps_t& caps, int w_spec, int64_t M, int64_t H) {
@@ -352,8 +360,16 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
         // M = 304 (10.4 vs 12.2 us), ties to M = 1500 and wins from 8 SMs'
         // worth (M = 2400: 40.8 -> 38.1 us; M = 5851: 99.9 -> 84.4 us).
         const int64_t sms = caps->num_sms;
-        const bool fp16_rows = dtype == ARF_FP16 && pl.vpt == 2 &&
-                               ((W <= 2 && M >= 2 * sms) || (W <= 4 && M >= 8 * sms));
+        // W = 2 and 4 (two chunks per thread, prefetching): one CTA per row,
+        // grid = M, in the one-row form. Its smaller register footprint lets
+        // CTAs share an SM, which replaces the in-CTA prefetch, and it has no
+        // fp16 penalty. Measured (H = 7168, cold): W = 2, M = 3315 bf16 39.1
+        // -> 37.7 us, fp16 50.6 -> 38.7 us; W = 4, M = 5851 bf16 83.9 ->
+        // 83.0 us, fp16 100.2 -> 83.3 us; W = 4, M = 1989 fp16 35.2 -> 29.0
+        // us. W = 8 (53.8 vs 46.4 us) and W = 1 (49.1 vs 43.3 us) keep the
+        // row loop.
+        if (one_row_grid_wanted(pl, W)) pl.grid = (int)(M < INT32_MAX ? M : INT32_MAX);
+        const bool fp16_rows = dtype == ARF_FP16 && pl.vpt == 2 && W == 1 && M >= 2 * sms;
         if (pl.path == ARF_PATH_ROW && W <= kBulkMaxRanks && (!arf::rms_prefetches(pl.w_spec, pl.vpt) || fp16_rows)) {
             arf_plan_t b;
             if (bulk_plan(*caps, w_spec, W, M, H, &b)) pl = b;
@@ -484,7 +500,7 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
     // only smaller clusters) is refused rather than launched
     st = arf_plan_check(&ws->caps, &pl, pattern, W, M, H, dtype);
     if (st != ARF_OK) return st;
-    if (!capturing && pl.path == ARF_PATH_ROW) {
+    if (!capturing && pl.path == ARF_PATH_ROW && !one_row_grid_wanted(pl, W)) {
         int b = 0;
         cudaError_t e = max_active_blocks(dtype, pl, H, W, &b);
         if (e == cudaSuccess && b > 0) {

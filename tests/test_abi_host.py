@@ -167,6 +167,8 @@ def test_planner_plans_are_legal(pattern, W, M, H):
                 assert M < 16 and C >= 512 and p.vpt == 1
                 assert 2 <= p.cluster <= min(8, caps.max_cluster)
                 assert p.grid == p.cluster * min(M, max(1, caps.num_sms * per_sm // p.cluster))
+            elif p.vpt == 2 and W in (2, 4) and p.w_spec == W:
+                assert p.cluster == 1 and p.grid == M  # one CTA per row: the kernel's one-row form
             else:
                 assert p.cluster == 1 and p.grid == max(1, min(M, caps.num_sms * per_sm))
 
@@ -181,7 +183,7 @@ def test_planner_uses_the_sm_count():
     arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 2048, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and (p.threads, p.vpt) == (448, 2) and p.grid % 152 == 0
     arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 4, 5851, 7168, arf.ARF_BF16, p)
-    assert p.path == arf.ARF_PATH_ROW and p.vpt * (4 + 1) <= 18 and p.grid % 152 == 0
+    assert p.path == arf.ARF_PATH_ROW and p.vpt * (4 + 1) <= 18 and p.grid == 5851  # one CTA per row
     arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and (p.threads, p.vpt) == (448, 2)  # 896 chunks > 512 threads
     no_cluster = arf.DeviceCaps(152, 1, 2048, 232448)
@@ -356,12 +358,14 @@ def test_planner_bulk_choices():
                           (16, 585, 7168, arf.ARF_PATH_ROW), (24, 400, 7168, arf.ARF_PATH_ROW),
                           (3, 4, 7168, arf.ARF_PATH_CLUSTER), (2, 128, 4096, arf.ARF_PATH_ROW)):
         assert plan(W, M, H).path == path, (W, M, H)
-    # fp16 rows of two chunks per thread with few ranks and many rows: the bulk ring
-    for W, M, H, path in ((2, 3315, 7168, arf.ARF_PATH_BULK), (4, 5851, 7168, arf.ARF_PATH_BULK),
-                          (1, 4972, 7168, arf.ARF_PATH_BULK), (8, 1024, 7168, arf.ARF_PATH_ROW),
-                          (2, 128, 7168, arf.ARF_PATH_ROW), (2, 8192, 4096, arf.ARF_PATH_ROW),
-                          (2, 304, 7168, arf.ARF_PATH_BULK), (4, 304, 7168, arf.ARF_PATH_ROW),
-                          (4, 1215, 7168, arf.ARF_PATH_ROW), (4, 1216, 7168, arf.ARF_PATH_BULK)):
+    # fp16 rows of two chunks per thread: W = 2 and 4 take one CTA per row (the
+    # one-row form has no fp16 penalty); W = 1 with many rows takes the bulk ring
+    for W, M, H, path, grid in ((2, 3315, 7168, arf.ARF_PATH_ROW, 3315), (4, 5851, 7168, arf.ARF_PATH_ROW, 5851),
+                                (1, 4972, 7168, arf.ARF_PATH_BULK, None), (1, 200, 7168, arf.ARF_PATH_ROW, None),
+                                (8, 1024, 7168, arf.ARF_PATH_ROW, None), (2, 128, 7168, arf.ARF_PATH_ROW, 128),
+                                (2, 8192, 4096, arf.ARF_PATH_ROW, None), (4, 304, 7168, arf.ARF_PATH_ROW, 304)):
         p = arf.Plan()
         assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_FP16, p) == arf.ARF_OK
         assert p.path == path, (W, M, H)
+        if grid is not None:
+            assert p.grid == grid, (W, M, H, p)

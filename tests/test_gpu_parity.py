@@ -31,8 +31,12 @@ def test_workload_parity(ws, name, M, pattern):
     inp = wl.make_inputs(ALL[name], M=M)
     P, R, G = to_device(inp)
     pat = PAT[pattern]
-    if name in wl.EXTRA_WORKLOADS:  # these shapes exist to exercise the bulk-copy kernel
-        assert ws.plan(pattern, len(P), M, inp.workload.H, P[0].dtype).path == arf.ARF_PATH_BULK
+    if name in wl.EXTRA_WORKLOADS:  # these shapes exist to reach particular kernel paths
+        plan = ws.plan(pattern, len(P), M, inp.workload.H, P[0].dtype)
+        if wl.EXTRA_PATHS[name] == "bulk":
+            assert plan.path == arf.ARF_PATH_BULK, plan
+        else:
+            assert plan.path == arf.ARF_PATH_ROW and plan.grid == M, plan
     got = gpu_run(ws, pat, P, R, G, inp.workload.eps)
     ref = oracle_run(pat, inp)
     n1 = assert_parity(DT[inp.workload.dtype], pat, got, ref, f"{name} M={M} {pattern}")
