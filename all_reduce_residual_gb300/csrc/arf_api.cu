@@ -611,6 +611,7 @@ arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t patt
         p.H = (int)H;
         p.W = W;
         p.eps = eps;
+        p.flat_ok = pattern == ARF_ALLREDUCE && !L.f32p && L.ldp == H && L.ldo == H && aligned16(out) ? 1 : 0;
         const bool rms = pattern == ARF_AR_RESIDUAL_RMSNORM;
         e = bf ? arf::launch_elem_bf16(p, pl, rms, stream, L.f32p) : arf::launch_elem_fp16(p, pl, rms, stream, L.f32p);
         if (e != cudaSuccess) return cuda_fail(ws, e);

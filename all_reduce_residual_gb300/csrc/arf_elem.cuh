@@ -47,11 +47,34 @@ __device__ __forceinline__ float elem_rank_sum(const uint4* const* s_ptr, int W,
 }
 
 // kAllReduce: tiles of blockDim.x elements, never crossing a row.
+// Contiguous tensors (p.flat_ok) whose partial pointers are all 16-byte
+// aligned are one flat range of M*H elements instead: 16-byte vectors over
+// the first (M*H)/8 chunks, then the last (M*H)%8 elements one by one. The
+// arithmetic is the same either way (rank-order mixed-precision adds, one
+// rounding per element).
 template <typename T, bool F32P>
 __global__ void __launch_bounds__(kMaxThreads) ar_elem_kernel(ElemParams p) {
     __shared__ const uint4* s_ptr[ARF_MAX_W];
     prologue(s_ptr, p.lc, p.W);
     __syncthreads();
+    if constexpr (!F32P) {
+        bool vec = p.flat_ok != 0;
+        for (int r = 0; r < p.W && vec; ++r) vec = (reinterpret_cast<uintptr_t>(s_ptr[r]) & 15u) == 0;
+        if (vec) {  // the same answer in every thread of every CTA
+            const int64_t total = p.M * (int64_t)p.H, nch = total / 8;
+            const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+            const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+            uint4* out16 = reinterpret_cast<uint4*>(p.out);
+            for (int64_t c = first; c < nch; c += stride) {
+                float acc[8];
+                rank_sum<T, 0, false>(acc, s_ptr, p.W, c);
+                st_out(out16 + c, Pack8<T>::narrow(acc));
+            }
+            for (int64_t e = nch * 8 + first; e < total; e += stride)
+                p.out[e] = narrow1<T>(elem_rank_sum<T, false>(s_ptr, p.W, e));
+            return;
+        }
+    }
     const int64_t per_row = (p.H + blockDim.x - 1) / blockDim.x;
     const int64_t ntiles = per_row * p.M;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {

@@ -88,6 +88,11 @@ struct ElemParams {
     int H;
     int W;
     float eps;
+    // kAllReduce: partials and out contiguous ([M,H], strides H) and out
+    // 16-byte aligned, so the whole tensor is one flat range of M*H
+    // elements; the kernel then takes 16-byte vectors if every partial
+    // pointer is 16-byte aligned too (it checks), with an elementwise tail.
+    int flat_ok;
 };
 
 // Launchers, one per I/O type (arf_launch_bf16.cu / arf_launch_fp16.cu).

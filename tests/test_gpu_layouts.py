@@ -159,3 +159,25 @@ def test_layout_argument_errors(ws):
     assert arf.arf_run_ex(ws.handle, o, RMS, 2, ptrs.data_ptr(), R.data_ptr(), G.data_ptr(), 1e-6,
                           out.data_ptr(), R.data_ptr(), M, H, arf.ARF_BF16, s) == arf.ARF_ERR_UNSUPPORTED
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("M,H", [(5, 13), (64, 7170), (3, 1)])
+@pytest.mark.parametrize("misaligned", [False, True])
+def test_allreduce_odd_h_flat_range(ws, M, H, misaligned):
+    """kAllReduce on contiguous tensors with H % 8 != 0 takes the whole tensor as
+    one flat range (16-byte body, elementwise tail) when every partial pointer is
+    16-byte aligned, and stays elementwise when one is only 2-byte aligned."""
+    W = 3
+    rng = np.random.default_rng(M * 7 + H)
+    P = [codes_of(rng, oracle.BF16, (M, H), 1.0) for _ in range(W)]
+    bufs = [torch.zeros(M * H + 8, dtype=torch.int16, device="cuda") for _ in range(W)]
+    Pd = []
+    for r, (b, p) in enumerate(zip(bufs, P)):
+        off = 1 if (misaligned and r == 1) else 0
+        v = b[off:off + M * H].view(torch.bfloat16).view(M, H)
+        v.copy_(wl.from_codes(p, "bf16").cuda())
+        Pd.append(v)
+    out, _ = arf.run(ws, AR, Pd)
+    torch.cuda.synchronize()
+    ref = oracle.run(oracle.ALLREDUCE, P, dtype=oracle.BF16)
+    assert_parity(oracle.BF16, AR, (host_codes(out), None), ref, f"M={M} H={H} misaligned={misaligned}")
