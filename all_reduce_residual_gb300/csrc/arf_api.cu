@@ -611,7 +611,9 @@ arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t patt
         p.H = (int)H;
         p.W = W;
         p.eps = eps;
-        p.flat_ok = pattern == ARF_ALLREDUCE && !L.f32p && L.ldp == H && L.ldo == H && aligned16(out) ? 1 : 0;
+        const bool rms_flat = pattern == ARF_AR_RESIDUAL_RMSNORM && L.ldr == H && L.ldro == H && aligned16(residual) &&
+                              aligned16(residual_out);
+        p.flat_ok = (pattern == ARF_ALLREDUCE || rms_flat) && !L.f32p && L.ldp == H && L.ldo == H && aligned16(out) ? 1 : 0;
         const bool rms = pattern == ARF_AR_RESIDUAL_RMSNORM;
         e = bf ? arf::launch_elem_bf16(p, pl, rms, stream, L.f32p) : arf::launch_elem_fp16(p, pl, rms, stream, L.f32p);
         if (e != cudaSuccess) return cuda_fail(ws, e);

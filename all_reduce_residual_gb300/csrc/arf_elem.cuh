@@ -87,15 +87,79 @@ __global__ void __launch_bounds__(kMaxThreads) ar_elem_kernel(ElemParams p) {
     }
 }
 
+// One row of kARResidualRMSNorm on contiguous tensors whose bases are all
+// 16-byte aligned (flat_ok, partials checked by the caller): row r is the
+// flat range [r*H, (r+1)*H) of every tensor, split into a head of fewer than
+// 8 elements up to the first 16-byte boundary (threads 0..), whole 16-byte
+// chunks, and a tail of fewer than 8 elements (the last threads). gamma,
+// indexed from the row start, is read element by element from L1. Same
+// arithmetic as the elementwise rows; residual_out is re-read in the second
+// pass by the thread that wrote it.
+template <typename T>
+__device__ __forceinline__ void rms_flat_row(const ElemParams& p, const uint4* const* s_ptr, int64_t row, int it,
+                                             float (*s_warp)[kMaxThreads / 32]) {
+    const int64_t e0 = row * (int64_t)p.H, e1 = e0 + p.H;
+    int64_t hs = (e0 + 7) / 8 * 8;  // head [e0, hs)
+    if (hs > e1) hs = e1;
+    int64_t be = e1 / 8 * 8;        // chunks [hs/8, be/8), tail [be, e1)
+    if (be < hs) be = hs;
+    const int64_t c0 = hs / 8, c1 = be / 8;
+    const int B = blockDim.x, tid = threadIdx.x;
+    const int nh = (int)(hs - e0), nt = (int)(e1 - be);  // each < 8, and B >= 32
+    const int64_t my_e = tid < nh ? e0 + tid : (tid >= B - nt ? be + (tid - (B - nt)) : -1);
+    const uint4* res16 = reinterpret_cast<const uint4*>(p.residual);
+    uint4* ro16 = reinterpret_cast<uint4*>(p.residual_out);
+    uint4* out16 = reinterpret_cast<uint4*>(p.out);
+    float ss = 0.0f;
+    if (my_e >= 0) {
+        float acc = elem_rank_sum<T, false>(s_ptr, p.W, my_e);
+        acc = MixedAdd<T>::add(acc, p.residual[my_e]);
+        const unsigned short xs = narrow1<T>(acc);
+        p.residual_out[my_e] = xs;
+        const float x = widen1<T>(xs);
+        ss = fmaf(x, x, ss);
+    }
+    for (int64_t c = c0 + tid; c < c1; c += B) {
+        float acc[8];
+        rank_sum<T, 0, false>(acc, s_ptr, p.W, c);
+        (void)residual_chunk<T>(acc, ld_resid(res16 + c), ro16 + c, ss);
+    }
+    const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
+    if (my_e >= 0) {
+        const float x = widen1<T>(p.residual_out[my_e]);
+        const float g = widen1<T>(p.gamma[my_e - e0]);
+        p.out[my_e] = narrow1<T>(__fmul_rn(__fmul_rn(x, inv), g));
+    }
+    for (int64_t c = c0 + tid; c < c1; c += B) {
+        const unsigned short* gp = p.gamma + (c * 8 - e0);
+        uint4 gv;
+        gv.x = (uint32_t)__ldg(gp + 0) | ((uint32_t)__ldg(gp + 1) << 16);
+        gv.y = (uint32_t)__ldg(gp + 2) | ((uint32_t)__ldg(gp + 3) << 16);
+        gv.z = (uint32_t)__ldg(gp + 4) | ((uint32_t)__ldg(gp + 5) << 16);
+        gv.w = (uint32_t)__ldg(gp + 6) | ((uint32_t)__ldg(gp + 7) << 16);
+        normalise_chunk<T>(ro16[c], gv, inv, out16 + c);
+    }
+}
+
 // kARResidualRMSNorm: one CTA per row (rows grid-stride). The rounded
 // residual_out goes to memory in the first pass and is read back in the
-// second by the thread that wrote it.
+// second by the thread that wrote it. Contiguous, 16-byte aligned tensors
+// (flat_ok, and every partial pointer aligned) take rms_flat_row instead.
 template <typename T, bool F32P>
 __global__ void __launch_bounds__(kMaxThreads) rms_elem_kernel(ElemParams p) {
     __shared__ const uint4* s_ptr[ARF_MAX_W];
     __shared__ float s_warp[2][kMaxThreads / 32];
     prologue(s_ptr, p.lc, p.W);
     __syncthreads();
+    if constexpr (!F32P) {
+        bool vec = p.flat_ok != 0;
+        for (int r = 0; r < p.W && vec; ++r) vec = (reinterpret_cast<uintptr_t>(s_ptr[r]) & 15u) == 0;
+        if (vec) {  // the same answer in every thread of every CTA
+            int it = 0;
+            for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++it) rms_flat_row<T>(p, s_ptr, row, it, s_warp);
+            return;
+        }
+    }
     int it = 0;
     for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++it) {
         float ss = 0.0f;

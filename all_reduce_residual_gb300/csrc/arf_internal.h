@@ -88,10 +88,12 @@ struct ElemParams {
     int H;
     int W;
     float eps;
-    // kAllReduce: partials and out contiguous ([M,H], strides H) and out
-    // 16-byte aligned, so the whole tensor is one flat range of M*H
-    // elements; the kernel then takes 16-byte vectors if every partial
-    // pointer is 16-byte aligned too (it checks), with an elementwise tail.
+    // Every tensor contiguous ([M,H], strides H) and out (and, for the RMS
+    // pattern, residual and residual_out) 16-byte aligned: the tensors are
+    // one flat range of M*H elements. The kernels then take 16-byte vectors
+    // if every partial pointer is 16-byte aligned too (they check): the whole
+    // range with an elementwise tail (kAllReduce), or each row's aligned
+    // chunks with an elementwise head and tail (kARResidualRMSNorm).
     int flat_ok;
 };
 

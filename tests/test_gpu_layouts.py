@@ -161,15 +161,20 @@ def test_layout_argument_errors(ws):
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("M,H", [(5, 13), (64, 7170), (3, 1)])
+@pytest.mark.parametrize("M,H", [(5, 13), (64, 7170), (3, 1), (7, 1001), (2, 24579)])
 @pytest.mark.parametrize("misaligned", [False, True])
-def test_allreduce_odd_h_flat_range(ws, M, H, misaligned):
-    """kAllReduce on contiguous tensors with H % 8 != 0 takes the whole tensor as
-    one flat range (16-byte body, elementwise tail) when every partial pointer is
-    16-byte aligned, and stays elementwise when one is only 2-byte aligned."""
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_odd_h_flat_range(ws, pattern, M, H, misaligned):
+    """Contiguous tensors with H % 8 != 0: the whole tensor is one flat range
+    (kAllReduce: 16-byte body and elementwise tail; kARResidualRMSNorm: each
+    row's aligned chunks with an elementwise head and tail) when every partial
+    pointer is 16-byte aligned, and plain elementwise when one is only 2-byte
+    aligned. Both match the oracle."""
     W = 3
     rng = np.random.default_rng(M * 7 + H)
     P = [codes_of(rng, oracle.BF16, (M, H), 1.0) for _ in range(W)]
+    R = codes_of(rng, oracle.BF16, (M, H), 1.0)
+    G = pins.nearest_codes(oracle.BF16, 0.5 + rng.random(H))
     bufs = [torch.zeros(M * H + 8, dtype=torch.int16, device="cuda") for _ in range(W)]
     Pd = []
     for r, (b, p) in enumerate(zip(bufs, P)):
@@ -177,7 +182,11 @@ def test_allreduce_odd_h_flat_range(ws, M, H, misaligned):
         v = b[off:off + M * H].view(torch.bfloat16).view(M, H)
         v.copy_(wl.from_codes(p, "bf16").cuda())
         Pd.append(v)
-    out, _ = arf.run(ws, AR, Pd)
+    Rd = wl.from_codes(R, "bf16").cuda()
+    Gd = wl.from_codes(G, "bf16").cuda()
+    rms = pattern == RMS
+    out, ro = arf.run(ws, pattern, Pd, Rd if rms else None, Gd if rms else None, 1e-6)
     torch.cuda.synchronize()
-    ref = oracle.run(oracle.ALLREDUCE, P, dtype=oracle.BF16)
-    assert_parity(oracle.BF16, AR, (host_codes(out), None), ref, f"M={M} H={H} misaligned={misaligned}")
+    ref = oracle.run(OPAT[pattern], P, R if rms else None, G if rms else None, 1e-6, dtype=oracle.BF16)
+    got = (host_codes(out), host_codes(ro) if rms else None)
+    assert_parity(oracle.BF16, pattern, got, ref, f"M={M} H={H} misaligned={misaligned}")
