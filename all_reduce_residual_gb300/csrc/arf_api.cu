@@ -260,6 +260,17 @@ arf_plan_t elem_plan(const arf_device_caps_t& caps, arf_pattern_t pattern, int64
         const int64_t cap = (int64_t)caps.num_sms * (caps.max_threads_per_sm / 256 > 0 ? caps.max_threads_per_sm / 256 : 1);
         const int64_t g = tiles < cap ? tiles : cap;
         pl.grid = (int)(g > 0 ? g : 1);
+    } else if (M >= 3 * (int64_t)caps.num_sms && H >= 1024) {
+        // Many rows: narrower CTAs with several chunks per thread, more of
+        // them per SM, hide a row's two dependent passes behind other rows
+        // better than one wide CTA per row does. Measured on GB300 (cold,
+        // 512 -> chosen threads): W = 2, H = 4098, M = 456 14.4 -> 12.3 us
+        // (256), M = 4096 67.4 -> 43.1 us (128); W = 8, H = 7175, M = 456
+        // 22.3 -> 18.9 us (256); 256 and 128 tie near M = 1024.
+        const bool narrow = M >= 7 * (int64_t)caps.num_sms;
+        pl.threads = narrow ? 128 : 256;
+        const int64_t cap = (narrow ? 8 : 4) * (int64_t)caps.num_sms;
+        pl.grid = (int)(M < cap ? M : cap);
     } else {
         int64_t t = ceil_div(H, 32) * 32;
         if (t > kMaxThreads) t = kMaxThreads;
@@ -370,9 +381,17 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
         // row loop.
         if (one_row_grid_wanted(pl, W)) pl.grid = (int)(M < INT32_MAX ? M : INT32_MAX);
         const bool fp16_rows = dtype == ARF_FP16 && pl.vpt == 2 && W == 1 && M >= 2 * sms;
-        if (pl.path == ARF_PATH_ROW && W <= kBulkMaxRanks && (!arf::rms_prefetches(pl.w_spec, pl.vpt) || fp16_rows)) {
+        // Rows longer than one CTA holds (a cluster per row) once there are
+        // rows for half the SMs: the bulk ring, where its row buffer and two
+        // ring slots fit. Measured on GB300 (cold, cluster -> bulk): W = 2,
+        // H = 32776, M = 76 19.2 -> 15.8 us, M = 2048 280.7 -> 107.6 us; W = 8,
+        // M = 608 85.7 -> 77.1 us; W = 4, H = 65536, M = 152 31.6 -> 27.7 us,
+        // but M = 512 84.1 -> 92.8 us (one CTA per SM). Fewer rows keep the
+        // cluster (W = 4, H = 65536, M = 64: 16.5 vs 24.6 us).
+        const bool long_rows = pl.path == ARF_PATH_CLUSTER && C > kMaxThreads * 8 && 2 * M >= sms;
+        if ((pl.path == ARF_PATH_ROW && (!arf::rms_prefetches(pl.w_spec, pl.vpt) || fp16_rows)) || long_rows) {
             arf_plan_t b;
-            if (bulk_plan(*caps, w_spec, W, M, H, &b)) pl = b;
+            if (W <= kBulkMaxRanks && bulk_plan(*caps, w_spec, W, M, H, &b)) pl = b;
         }
         // The streaming kernel (ARF_PATH_ASYNC) is not chosen: measured on
         // GB300 it keeps fewer bytes in flight than the row kernel's register
@@ -611,10 +630,15 @@ arf_status_t launch(arf_workspace_t ws, const arf_plan_t& pl, arf_pattern_t patt
         p.H = (int)H;
         p.W = W;
         p.eps = eps;
-        const bool rms_flat = pattern == ARF_AR_RESIDUAL_RMSNORM && L.ldr == H && L.ldro == H && aligned16(residual) &&
-                              aligned16(residual_out);
-        p.flat_ok = (pattern == ARF_ALLREDUCE || rms_flat) && !L.f32p && L.ldp == H && L.ldo == H && aligned16(out) ? 1 : 0;
         const bool rms = pattern == ARF_AR_RESIDUAL_RMSNORM;
+        // 16-byte vectors need every tensor's row r to start at the same
+        // offset modulo 8 elements (strides congruent mod 8) from 16-byte
+        // aligned bases; contiguous tensors are also one flat range.
+        const int64_t res = ((L.ldp % 8) + 8) % 8;
+        bool vec = !L.f32p && aligned16(out) && L.ldo % 8 == res;
+        if (rms) vec = vec && aligned16(residual) && aligned16(residual_out) && L.ldr % 8 == res && L.ldro % 8 == res;
+        const bool contiguous = L.ldp == H && L.ldo == H && (!rms || (L.ldr == H && L.ldro == H));
+        p.flat_ok = !vec ? 0 : (contiguous ? 1 : 2);
         e = bf ? arf::launch_elem_bf16(p, pl, rms, stream, L.f32p) : arf::launch_elem_fp16(p, pl, rms, stream, L.f32p);
         if (e != cudaSuccess) return cuda_fail(ws, e);
         return ARF_OK;

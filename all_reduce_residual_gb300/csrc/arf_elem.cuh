@@ -1,7 +1,9 @@
 // arf_elem.cuh: elementwise kernels for layouts the 16-byte kernels cannot
 // take: H not a multiple of 8, row strides not a multiple of 8 elements, or
 // residual / gamma / outputs not 16-byte aligned (2-byte alignment suffices;
-// binary32 partials need 4). One element per thread per step, the same
+// binary32 partials need 4). One element per thread per step where the
+// rows of the tensors start at different offsets within a 16-byte vector,
+// else 16-byte vectors with per-row heads and tails; the same
 // arithmetic as the vector kernels: binary32 rank-order sum with one
 // round-to-nearest add per rank, the residual added to the unrounded sum,
 // one rounding, the statistic of the stored residual_out.
@@ -46,21 +48,46 @@ __device__ __forceinline__ float elem_rank_sum(const uint4* const* s_ptr, int W,
     return acc;
 }
 
+// The split of one row into 16-byte vectors. All tensors of the call start
+// row r at the same offset modulo 8 elements (flat_ok != 0), so one split
+// serves them all: nh head elements up to the first 16-byte boundary, nb
+// whole chunks, nt tail elements (nh, nt < 8).
+struct RowSplit {
+    int nh, nb, nt;
+};
+__device__ __forceinline__ RowSplit row_split(int64_t first_elem, int H) {
+    RowSplit r;
+    r.nh = (int)((8 - (first_elem & 7)) & 7);
+    if (r.nh > H) r.nh = H;
+    r.nb = (H - r.nh) / 8;
+    r.nt = H - r.nh - 8 * r.nb;
+    return r;
+}
+
+// Whether the vector forms apply: the host's layout verdict, and every
+// partial pointer 16-byte aligned (the same answer in every thread).
+__device__ __forceinline__ bool vector_layout(const ElemParams& p, const uint4* const* s_ptr) {
+    bool vec = p.flat_ok != 0;
+    for (int r = 0; r < p.W && vec; ++r) vec = (reinterpret_cast<uintptr_t>(s_ptr[r]) & 15u) == 0;
+    return vec;
+}
+
 // kAllReduce: tiles of blockDim.x elements, never crossing a row.
-// Contiguous tensors (p.flat_ok) whose partial pointers are all 16-byte
-// aligned are one flat range of M*H elements instead: 16-byte vectors over
-// the first (M*H)/8 chunks, then the last (M*H)%8 elements one by one. The
-// arithmetic is the same either way (rank-order mixed-precision adds, one
-// rounding per element).
+// Tensors whose rows share their 16-byte phase (flat_ok, partial pointers
+// aligned) take 16-byte vectors: contiguous ones as one flat range of M*H
+// elements (vectors over the first (M*H)/8 chunks, then the last (M*H)%8
+// elements one by one), strided ones a row per CTA (rows grid-stride; the
+// head and tail elements of a row one per thread, its whole chunks as
+// vectors). The arithmetic is the same in every form (rank-order
+// mixed-precision adds, one rounding per element). At most 64 registers, so
+// that 256-thread CTAs fit four to an SM.
 template <typename T, bool F32P>
-__global__ void __launch_bounds__(kMaxThreads) ar_elem_kernel(ElemParams p) {
+__global__ void __launch_bounds__(kMaxThreads, 2) ar_elem_kernel(ElemParams p) {
     __shared__ const uint4* s_ptr[ARF_MAX_W];
     prologue(s_ptr, p.lc, p.W);
     __syncthreads();
     if constexpr (!F32P) {
-        bool vec = p.flat_ok != 0;
-        for (int r = 0; r < p.W && vec; ++r) vec = (reinterpret_cast<uintptr_t>(s_ptr[r]) & 15u) == 0;
-        if (vec) {  // the same answer in every thread of every CTA
+        if (vector_layout(p, s_ptr) && p.flat_ok == 1) {
             const int64_t total = p.M * (int64_t)p.H, nch = total / 8;
             const int64_t stride = (int64_t)gridDim.x * blockDim.x;
             const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -72,6 +99,23 @@ __global__ void __launch_bounds__(kMaxThreads) ar_elem_kernel(ElemParams p) {
             }
             for (int64_t e = nch * 8 + first; e < total; e += stride)
                 p.out[e] = narrow1<T>(elem_rank_sum<T, false>(s_ptr, p.W, e));
+            return;
+        }
+        if (vector_layout(p, s_ptr)) {
+            const int B = blockDim.x, tid = threadIdx.x;  // B >= 32 > nh + nt
+            uint4* out16 = reinterpret_cast<uint4*>(p.out);
+            for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+                const int64_t op = row * p.ldp, oo = row * p.ldo;
+                const RowSplit sp = row_split(op, p.H);
+                const int k = tid < sp.nh ? tid : (tid >= B - sp.nt ? sp.nh + 8 * sp.nb + (tid - (B - sp.nt)) : -1);
+                if (k >= 0) p.out[oo + k] = narrow1<T>(elem_rank_sum<T, false>(s_ptr, p.W, op + k));
+                const int64_t cp = (op + sp.nh) / 8, co = (oo + sp.nh) / 8;
+                for (int j = tid; j < sp.nb; j += B) {
+                    float acc[8];
+                    rank_sum<T, 0, false>(acc, s_ptr, p.W, cp + j);
+                    st_out(out16 + co + j, Pack8<T>::narrow(acc));
+                }
+            }
             return;
         }
     }
@@ -87,64 +131,62 @@ __global__ void __launch_bounds__(kMaxThreads) ar_elem_kernel(ElemParams p) {
     }
 }
 
-// One row of kARResidualRMSNorm on contiguous tensors whose bases are all
-// 16-byte aligned (flat_ok, partials checked by the caller): row r is the
-// flat range [r*H, (r+1)*H) of every tensor, split into a head of fewer than
-// 8 elements up to the first 16-byte boundary (threads 0..), whole 16-byte
-// chunks, and a tail of fewer than 8 elements (the last threads). gamma,
-// indexed from the row start, is read element by element from L1. Same
-// arithmetic as the elementwise rows; residual_out is re-read in the second
-// pass by the thread that wrote it.
+// One row of kARResidualRMSNorm on tensors whose rows share their 16-byte
+// phase (flat_ok, partials checked by the caller): the row splits into a
+// head of fewer than 8 elements up to the first 16-byte boundary (threads
+// 0..), whole 16-byte chunks, and a tail of fewer than 8 elements (the last
+// threads), at each tensor's own row offset. gamma, indexed from the row
+// start, is read element by element from L1. Same arithmetic as the
+// elementwise rows; residual_out is re-read in the second pass by the
+// thread that wrote it.
 template <typename T>
 __device__ __forceinline__ void rms_flat_row(const ElemParams& p, const uint4* const* s_ptr, int64_t row, int it,
                                              float (*s_warp)[kMaxThreads / 32]) {
-    const int64_t e0 = row * (int64_t)p.H, e1 = e0 + p.H;
-    int64_t hs = (e0 + 7) / 8 * 8;  // head [e0, hs)
-    if (hs > e1) hs = e1;
-    int64_t be = e1 / 8 * 8;        // chunks [hs/8, be/8), tail [be, e1)
-    if (be < hs) be = hs;
-    const int64_t c0 = hs / 8, c1 = be / 8;
-    const int B = blockDim.x, tid = threadIdx.x;
-    const int nh = (int)(hs - e0), nt = (int)(e1 - be);  // each < 8, and B >= 32
-    const int64_t my_e = tid < nh ? e0 + tid : (tid >= B - nt ? be + (tid - (B - nt)) : -1);
+    const int64_t op = row * p.ldp, orr = row * p.ldr, oro = row * p.ldro, oo = row * p.ldo;
+    const RowSplit sp = row_split(op, p.H);
+    const int B = blockDim.x, tid = threadIdx.x;  // B >= 32 > nh + nt
+    const int k = tid < sp.nh ? tid : (tid >= B - sp.nt ? sp.nh + 8 * sp.nb + (tid - (B - sp.nt)) : -1);
+    // chunk j of the row in each tensor, as a 16-byte index
+    const int64_t cp = (op + sp.nh) / 8, cr = (orr + sp.nh) / 8, cro = (oro + sp.nh) / 8, co = (oo + sp.nh) / 8;
     const uint4* res16 = reinterpret_cast<const uint4*>(p.residual);
     uint4* ro16 = reinterpret_cast<uint4*>(p.residual_out);
     uint4* out16 = reinterpret_cast<uint4*>(p.out);
     float ss = 0.0f;
-    if (my_e >= 0) {
-        float acc = elem_rank_sum<T, false>(s_ptr, p.W, my_e);
-        acc = MixedAdd<T>::add(acc, p.residual[my_e]);
+    if (k >= 0) {
+        float acc = elem_rank_sum<T, false>(s_ptr, p.W, op + k);
+        acc = MixedAdd<T>::add(acc, p.residual[orr + k]);
         const unsigned short xs = narrow1<T>(acc);
-        p.residual_out[my_e] = xs;
+        p.residual_out[oro + k] = xs;
         const float x = widen1<T>(xs);
         ss = fmaf(x, x, ss);
     }
-    for (int64_t c = c0 + tid; c < c1; c += B) {
+    for (int j = tid; j < sp.nb; j += B) {
         float acc[8];
-        rank_sum<T, 0, false>(acc, s_ptr, p.W, c);
-        (void)residual_chunk<T>(acc, ld_resid(res16 + c), ro16 + c, ss);
+        rank_sum<T, 0, false>(acc, s_ptr, p.W, cp + j);
+        (void)residual_chunk<T>(acc, ld_resid(res16 + cr + j), ro16 + cro + j, ss);
     }
     const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
-    if (my_e >= 0) {
-        const float x = widen1<T>(p.residual_out[my_e]);
-        const float g = widen1<T>(p.gamma[my_e - e0]);
-        p.out[my_e] = narrow1<T>(__fmul_rn(__fmul_rn(x, inv), g));
+    if (k >= 0) {
+        const float x = widen1<T>(p.residual_out[oro + k]);
+        const float g = widen1<T>(p.gamma[k]);
+        p.out[oo + k] = narrow1<T>(__fmul_rn(__fmul_rn(x, inv), g));
     }
-    for (int64_t c = c0 + tid; c < c1; c += B) {
-        const unsigned short* gp = p.gamma + (c * 8 - e0);
+    for (int j = tid; j < sp.nb; j += B) {
+        const unsigned short* gp = p.gamma + sp.nh + 8 * j;
         uint4 gv;
         gv.x = (uint32_t)__ldg(gp + 0) | ((uint32_t)__ldg(gp + 1) << 16);
         gv.y = (uint32_t)__ldg(gp + 2) | ((uint32_t)__ldg(gp + 3) << 16);
         gv.z = (uint32_t)__ldg(gp + 4) | ((uint32_t)__ldg(gp + 5) << 16);
         gv.w = (uint32_t)__ldg(gp + 6) | ((uint32_t)__ldg(gp + 7) << 16);
-        normalise_chunk<T>(ro16[c], gv, inv, out16 + c);
+        normalise_chunk<T>(ro16[cro + j], gv, inv, out16 + co + j);
     }
 }
 
 // kARResidualRMSNorm: one CTA per row (rows grid-stride). The rounded
 // residual_out goes to memory in the first pass and is read back in the
-// second by the thread that wrote it. Contiguous, 16-byte aligned tensors
-// (flat_ok, and every partial pointer aligned) take rms_flat_row instead.
+// second by the thread that wrote it. Tensors whose rows share their
+// 16-byte phase (flat_ok, and every partial pointer aligned) take
+// rms_flat_row instead.
 template <typename T, bool F32P>
 __global__ void __launch_bounds__(kMaxThreads) rms_elem_kernel(ElemParams p) {
     __shared__ const uint4* s_ptr[ARF_MAX_W];
@@ -152,9 +194,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_elem_kernel(ElemParams p) {
     prologue(s_ptr, p.lc, p.W);
     __syncthreads();
     if constexpr (!F32P) {
-        bool vec = p.flat_ok != 0;
-        for (int r = 0; r < p.W && vec; ++r) vec = (reinterpret_cast<uintptr_t>(s_ptr[r]) & 15u) == 0;
-        if (vec) {  // the same answer in every thread of every CTA
+        if (vector_layout(p, s_ptr)) {  // the same answer in every thread of every CTA
             int it = 0;
             for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++it) rms_flat_row<T>(p, s_ptr, row, it, s_warp);
             return;

@@ -88,12 +88,15 @@ struct ElemParams {
     int H;
     int W;
     float eps;
-    // Every tensor contiguous ([M,H], strides H) and out (and, for the RMS
-    // pattern, residual and residual_out) 16-byte aligned: the tensors are
-    // one flat range of M*H elements. The kernels then take 16-byte vectors
-    // if every partial pointer is 16-byte aligned too (they check): the whole
-    // range with an elementwise tail (kAllReduce), or each row's aligned
-    // chunks with an elementwise head and tail (kARResidualRMSNorm).
+    // Whether 16-byte vectors can serve this layout: out (and, for the RMS
+    // pattern, residual and residual_out) 16-byte aligned and every row
+    // stride congruent to ldp modulo 8, so that row r of every tensor starts
+    // at the same offset within a 16-byte vector. 1: the tensors are also
+    // contiguous ([M,H], strides H), one flat range of M*H elements; 2: rows
+    // apart; 0: neither. The kernels then take vectors if every partial
+    // pointer is 16-byte aligned too (they check): per row, an elementwise
+    // head up to the first 16-byte boundary, whole chunks, an elementwise
+    // tail; kAllReduce on contiguous tensors runs the whole range as one.
     int flat_ok;
 };
 

@@ -195,18 +195,60 @@ def test_planner_uses_the_sm_count():
 @pytest.mark.parametrize("M", [1, 7, 300])
 def test_long_rows_split_over_clusters(H, M):
     """Rows longer than one CTA holds: kARResidualRMSNorm splits them over a
-    cluster (up to 16 CTAs); kAllReduce is flat and takes any H <= ARF_MAX_H."""
+    cluster (up to 16 CTAs), or, with rows for half the SMs, streams them
+    through the bulk ring where its row buffer fits; kAllReduce is flat and
+    takes any H <= ARF_MAX_H."""
     p = arf.Plan()
+    bulk = 2 * M >= 152 and (H // 8) * 16 + 1024 + 2 * 9 * 64 * 16 <= 232448
     assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
-    assert p.path == arf.ARF_PATH_CLUSTER and p.threads <= 512
-    assert p.threads * p.vpt * p.cluster >= H // 8
+    if bulk:
+        assert p.path == arf.ARF_PATH_BULK and p.threads <= 512
+    else:
+        assert p.path == arf.ARF_PATH_CLUSTER and p.threads <= 512
+        assert p.threads * p.vpt * p.cluster >= H // 8
     assert arf.arf_plan_check(GB300, p, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16) == arf.ARF_OK
     assert arf.arf_plan_for_caps(GB300, arf.ARF_ALLREDUCE, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
     # a device with 4-CTA clusters holds rows up to 4 x 32768; longer rows
     # take the elementwise kernel
     small = arf.DeviceCaps(152, 4, 2048, 232448)
     assert arf.arf_plan_for_caps(small, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
-    assert p.path == (arf.ARF_PATH_CLUSTER if H <= 4 * 32768 else arf.ARF_PATH_ELEM)
+    if H > 4 * 32768:
+        assert p.path == arf.ARF_PATH_ELEM
+    else:
+        assert p.path == (arf.ARF_PATH_BULK if bulk else arf.ARF_PATH_CLUSTER)
+
+
+def test_elementwise_rmsnorm_plan_shape():
+    """Rows with H % 8 != 0: one wide CTA per row while rows are few; from
+    3 x SMs rows 256-thread CTAs (at most four per SM), from 7 x SMs
+    128-thread CTAs (at most eight per SM)."""
+    p = arf.Plan()
+    for W, M, H in ((2, 4096, 4098), (4, 2048, 7170), (8, 608, 7175), (3, 128, 4097), (2, 455, 4098),
+                    (2, 456, 4098), (8, 1063, 7175), (8, 1064, 7175), (3, 5000, 1001)):
+        assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+        assert p.path == arf.ARF_PATH_ELEM
+        if M >= 7 * 152 and H >= 1024:
+            assert p.threads == 128 and p.grid == min(M, 8 * 152), (W, M, H, p)
+        elif M >= 3 * 152 and H >= 1024:
+            assert p.threads == 256 and p.grid == min(M, 4 * 152), (W, M, H, p)
+        else:
+            assert p.threads == min(512, -(-H // 32) * 32) and p.grid == min(M, 152 * (2048 // p.threads)), (W, M, H, p)
+        assert arf.arf_plan_check(GB300, p, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16) == arf.ARF_OK
+
+
+def test_long_rows_take_the_bulk_ring_when_rows_are_many():
+    """Rows of more than 4096 chunks: a cluster per row for fewer rows than
+    half the SMs, the bulk ring from there while its row buffer fits."""
+    p = arf.Plan()
+    for W, M, H in ((2, 16, 32776), (2, 76, 32776), (2, 2048, 32776), (8, 608, 32776), (4, 64, 65536),
+                    (4, 152, 65536), (12, 300, 40000), (13, 300, 40000), (2, 500, 131072)):
+        assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+        assert arf.arf_plan_check(GB300, p, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16) == arf.ARF_OK
+        fits = (H // 8) * 16 + 1024 + 2 * (W + 1) * 64 * 16 <= 232448
+        if 2 * M >= 152 and W <= 12 and fits:
+            assert p.path == arf.ARF_PATH_BULK, (W, M, H, p)
+        else:
+            assert p.path == arf.ARF_PATH_CLUSTER, (W, M, H, p)
 
 
 def test_long_row_limits():

@@ -42,7 +42,7 @@ def inputs(W, M, H, dtype, seed):
 @pytest.mark.parametrize("W,M,H,dtype", [(1, 9, 8, "bf16"), (2, 37, 1000, "bf16"), (3, 5, 7168, "fp16"),
                                          (8, 41, 7176, "bf16"), (16, 23, 7168, "fp16"), (16, 3, 4096, "bf16"),
                                          (17, 6, 2056, "fp16"), (64, 2, 256, "bf16"), (4, 300, 264, "fp16"),
-                                         (4, 2, 32768, "bf16")])
+                                         (4, 2, 32768, "bf16"), (2, 5, 32776, "bf16"), (8, 3, 65536, "fp16")])
 def test_bulk_plans(ws, W, M, H, dtype):
     inp = inputs(W, M, H, dtype, W * 131 + M)
     ref = oracle_run(RMS, inp)

@@ -88,6 +88,23 @@ def test_row_strides(ws, pattern, H, pads):
     run_case(ws, pattern, "bf16", 4, 37, H, pads=pads, seed=H)
 
 
+@pytest.mark.parametrize("H,pads", [(4098, (6, 6, 6, 6)), (1001, (4, 4, 4, 4)), (7170, (6, 14, 22, 30)),
+                                    (13, (8, 0, 0, 8)), (64, (3, 3, 3, 3)), (4096, (1, 9, 17, 1))])
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_strided_rows_vector_form(ws, pattern, H, pads):
+    """Row strides congruent modulo 8 (every tensor's row r starts at the same
+    offset within a 16-byte vector) take the elementwise kernels' 16-byte
+    form row by row, with heads that differ from row to row where the
+    stride is not a multiple of 8; padding stays untouched. Planner plans and
+    explicit ones with the narrowest and widest CTAs."""
+    for i, W in enumerate((1, 3, 8)):
+        dtype = "bf16" if i % 2 == 0 else "fp16"
+        run_case(ws, pattern, dtype, W, 37, H, pads=pads, seed=H + W)
+        for threads, grid in ((32, 5), (512, 64)):
+            plan = arf.Plan(path=arf.ARF_PATH_ELEM, threads=threads, vpt=1, cluster=1, grid=grid, w_spec=0)
+            run_case(ws, pattern, dtype, W, 37, H, pads=pads, plan=plan, seed=H + W + threads)
+
+
 @pytest.mark.parametrize("W", [1, 2, 3, 8, 17])
 @pytest.mark.parametrize("M,H", [(1, 8), (37, 4096), (300, 7168), (5, 13), (2, 65536)])
 @pytest.mark.parametrize("pattern", [AR, RMS])

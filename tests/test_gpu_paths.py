@@ -123,10 +123,12 @@ def test_generic_rank_counts(ws, W, pattern):
 
 
 @pytest.mark.parametrize("M,H", [(1, 8), (1, 32768), (2500, 64), (5000, 8), (3, 7176), (3, 32776), (2, 65536),
-                                 (40, 40960), (2, 262144), (1, 524288)])
+                                 (40, 40960), (80, 32776), (2, 262144), (1, 524288)])
 @pytest.mark.parametrize("pattern", [AR, RMS])
 def test_ragged_and_extreme_shapes(ws, M, H, pattern):
     check(ws, pattern, inputs(4, M, H), what=f"M={M} H={H}")
+    if pattern == RMS and M == 80:  # rows of 4097 chunks for half the SMs: the bulk ring
+        assert ws.plan(RMS, 4, M, H, torch.bfloat16).path == arf.ARF_PATH_BULK
 
 
 def test_zero_rows_launch_nothing(ws):
