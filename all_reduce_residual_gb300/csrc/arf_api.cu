@@ -387,11 +387,14 @@ extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pat
         // H = 32776, M = 76 19.2 -> 15.8 us, M = 2048 280.7 -> 107.6 us; W = 8,
         // M = 608 85.7 -> 77.1 us; W = 4, H = 65536, M = 152 31.6 -> 27.7 us,
         // but M = 512 84.1 -> 92.8 us (one CTA per SM). Fewer rows keep the
-        // cluster (W = 4, H = 65536, M = 64: 16.5 vs 24.6 us).
+        // cluster (W = 4, H = 65536, M = 64: 16.5 vs 24.6 us). Those figures
+        // are for blocks of 512 chunks; rows whose buffer leaves room only for
+        // blocks narrower than 256 chunks keep the cluster too.
         const bool long_rows = pl.path == ARF_PATH_CLUSTER && C > kMaxThreads * 8 && 2 * M >= sms;
         if ((pl.path == ARF_PATH_ROW && (!arf::rms_prefetches(pl.w_spec, pl.vpt) || fp16_rows)) || long_rows) {
             arf_plan_t b;
-            if (W <= kBulkMaxRanks && bulk_plan(*caps, w_spec, W, M, H, &b)) pl = b;
+            if (W <= kBulkMaxRanks && bulk_plan(*caps, w_spec, W, M, H, &b) && (!long_rows || b.threads >= 256))
+                pl = b;
         }
         // The streaming kernel (ARF_PATH_ASYNC) is not chosen: measured on
         // GB300 it keeps fewer bytes in flight than the row kernel's register

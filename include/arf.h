@@ -84,9 +84,12 @@ typedef enum arf_path {
                              256 threads per SM streams its rows in column
                              blocks of 256 chunks through a ring of `stages`
                              asynchronous shared-memory copies (cp.async) */
-    ARF_PATH_ELEM = 4,    /* either pattern, any layout: one element per thread
-                             per step (H not a multiple of 8, row strides not a
-                             multiple of 8, tensors only 2-byte aligned) */
+    ARF_PATH_ELEM = 4,    /* either pattern, any layout (H not a multiple of 8,
+                             row strides not a multiple of 8, tensors only 2-byte
+                             aligned): 16-byte vectors with per-row heads and
+                             tails where every tensor is 16-byte aligned and all
+                             row strides agree modulo 8, else one element per
+                             thread per step */
     ARF_PATH_BULK = 5     /* either pattern, 16-bit partials: each CTA walks
                              its rows in column blocks of `threads` chunks;
                              one thread keeps `stages` blocks in flight as TMA

@@ -199,7 +199,7 @@ def test_long_rows_split_over_clusters(H, M):
     through the bulk ring where its row buffer fits; kAllReduce is flat and
     takes any H <= ARF_MAX_H."""
     p = arf.Plan()
-    bulk = 2 * M >= 152 and (H // 8) * 16 + 1024 + 2 * 9 * 64 * 16 <= 232448
+    bulk = 2 * M >= 152 and (H // 8) * 16 + 1024 + 2 * 9 * 256 * 16 <= 232448
     assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
     if bulk:
         assert p.path == arf.ARF_PATH_BULK and p.threads <= 512
@@ -241,10 +241,11 @@ def test_long_rows_take_the_bulk_ring_when_rows_are_many():
     half the SMs, the bulk ring from there while its row buffer fits."""
     p = arf.Plan()
     for W, M, H in ((2, 16, 32776), (2, 76, 32776), (2, 2048, 32776), (8, 608, 32776), (4, 64, 65536),
-                    (4, 152, 65536), (12, 300, 40000), (13, 300, 40000), (2, 500, 131072)):
+                    (4, 152, 65536), (12, 300, 40000), (13, 300, 40000), (2, 500, 131072), (8, 500, 78848),
+                    (8, 500, 78856), (8, 500, 106496)):
         assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
         assert arf.arf_plan_check(GB300, p, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16) == arf.ARF_OK
-        fits = (H // 8) * 16 + 1024 + 2 * (W + 1) * 64 * 16 <= 232448
+        fits = (H // 8) * 16 + 1024 + 2 * (W + 1) * 256 * 16 <= 232448  # blocks of >= 256 chunks
         if 2 * M >= 152 and W <= 12 and fits:
             assert p.path == arf.ARF_PATH_BULK, (W, M, H, p)
         else:
