@@ -72,6 +72,43 @@ __device__ __forceinline__ bool vector_layout(const ElemParams& p, const uint4* 
     return vec;
 }
 
+// The vector forms' chunks per trip: two where the rank count is compiled in
+// (WS > 0) and a thread's loads for both fit the 64-register budget without
+// spilling (kAllReduce up to 8 vectors, W <= 4; kARResidualRMSNorm, which
+// also holds the residual, up to 6, W <= 2), else one.
+template <int WS, bool RMS>
+__host__ __device__ constexpr int elem_chunks_per_trip() {
+    return WS > 0 && 2 * (WS + (RMS ? 1 : 0)) <= (RMS ? 6 : 8) ? 2 : 1;
+}
+
+// acc[q] = the rank-order sum of the partials at chunk c[q], for each q < K
+// with ok[q]. WS > 0 (W == WS): every load of the K chunks is issued before
+// the first add; WS == 0: rank_sum's groups of run-time ranks, chunk by chunk.
+template <typename T, int WS, int K>
+__device__ __forceinline__ void rank_sum_chunks(float (&acc)[K][8], const uint4* const* s_ptr, int W,
+                                                const int64_t (&c)[K], const bool (&ok)[K]) {
+    if constexpr (WS > 0) {
+        uint4 v[K][WS];
+#pragma unroll
+        for (int q = 0; q < K; ++q)
+#pragma unroll
+            for (int r = 0; r < WS; ++r)
+                if (ok[q]) v[q][r] = ld_once(s_ptr[r] + c[q]);
+#pragma unroll
+        for (int q = 0; q < K; ++q) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[q][e] = 0.0f;
+#pragma unroll
+            for (int r = 0; r < WS; ++r)
+                if (ok[q]) accumulate<T>(acc[q], v[q][r]);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < K; ++q)
+            if (ok[q]) rank_sum<T, 0, false>(acc[q], s_ptr, W, c[q]);
+    }
+}
+
 // kAllReduce: tiles of blockDim.x elements, never crossing a row.
 // Tensors whose rows share their 16-byte phase (flat_ok, partial pointers
 // aligned) take 16-byte vectors: contiguous ones as one flat range of M*H
@@ -79,10 +116,13 @@ __device__ __forceinline__ bool vector_layout(const ElemParams& p, const uint4* 
 // elements one by one), strided ones a row per CTA (rows grid-stride; the
 // head and tail elements of a row one per thread, its whole chunks as
 // vectors). The arithmetic is the same in every form (rank-order
-// mixed-precision adds, one rounding per element). At most 64 registers, so
-// that 256-thread CTAs fit four to an SM.
-template <typename T, bool F32P>
+// mixed-precision adds, one rounding per element). WS > 0: W == WS compiled
+// in for the vector forms. At most 64 registers, so that 256-thread CTAs fit
+// four to an SM.
+template <typename T, bool F32P, int WS = 0>
 __global__ void __launch_bounds__(kMaxThreads, 2) ar_elem_kernel(ElemParams p) {
+    static_assert(!F32P || WS == 0, "binary32 partials use the run-time rank count");
+    constexpr int K = elem_chunks_per_trip<WS, false>();
     __shared__ const uint4* s_ptr[ARF_MAX_W];
     prologue(s_ptr, p.lc, p.W);
     __syncthreads();
@@ -92,10 +132,19 @@ __global__ void __launch_bounds__(kMaxThreads, 2) ar_elem_kernel(ElemParams p) {
             const int64_t stride = (int64_t)gridDim.x * blockDim.x;
             const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
             uint4* out16 = reinterpret_cast<uint4*>(p.out);
-            for (int64_t c = first; c < nch; c += stride) {
-                float acc[8];
-                rank_sum<T, 0, false>(acc, s_ptr, p.W, c);
-                st_out(out16 + c, Pack8<T>::narrow(acc));
+            for (int64_t c0 = first; c0 < nch; c0 += K * stride) {
+                int64_t c[K];
+                bool ok[K];
+#pragma unroll
+                for (int q = 0; q < K; ++q) {
+                    c[q] = c0 + q * stride;
+                    ok[q] = c[q] < nch;
+                }
+                float acc[K][8];
+                rank_sum_chunks<T, WS, K>(acc, s_ptr, p.W, c, ok);
+#pragma unroll
+                for (int q = 0; q < K; ++q)
+                    if (ok[q]) st_out(out16 + c[q], Pack8<T>::narrow(acc[q]));
             }
             for (int64_t e = nch * 8 + first; e < total; e += stride)
                 p.out[e] = narrow1<T>(elem_rank_sum<T, false>(s_ptr, p.W, e));
@@ -110,10 +159,19 @@ __global__ void __launch_bounds__(kMaxThreads, 2) ar_elem_kernel(ElemParams p) {
                 const int k = tid < sp.nh ? tid : (tid >= B - sp.nt ? sp.nh + 8 * sp.nb + (tid - (B - sp.nt)) : -1);
                 if (k >= 0) p.out[oo + k] = narrow1<T>(elem_rank_sum<T, false>(s_ptr, p.W, op + k));
                 const int64_t cp = (op + sp.nh) / 8, co = (oo + sp.nh) / 8;
-                for (int j = tid; j < sp.nb; j += B) {
-                    float acc[8];
-                    rank_sum<T, 0, false>(acc, s_ptr, p.W, cp + j);
-                    st_out(out16 + co + j, Pack8<T>::narrow(acc));
+                for (int j0 = tid; j0 < sp.nb; j0 += K * B) {
+                    int64_t c[K];
+                    bool ok[K];
+#pragma unroll
+                    for (int q = 0; q < K; ++q) {
+                        c[q] = cp + j0 + q * B;
+                        ok[q] = j0 + q * B < sp.nb;
+                    }
+                    float acc[K][8];
+                    rank_sum_chunks<T, WS, K>(acc, s_ptr, p.W, c, ok);
+#pragma unroll
+                    for (int q = 0; q < K; ++q)
+                        if (ok[q]) st_out(out16 + co + j0 + q * B, Pack8<T>::narrow(acc[q]));
                 }
             }
             return;
@@ -139,9 +197,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) ar_elem_kernel(ElemParams p) {
 // start, is read element by element from L1. Same arithmetic as the
 // elementwise rows; residual_out is re-read in the second pass by the
 // thread that wrote it.
-template <typename T>
+template <typename T, int WS>
 __device__ __forceinline__ void rms_flat_row(const ElemParams& p, const uint4* const* s_ptr, int64_t row, int it,
                                              float (*s_warp)[kMaxThreads / 32]) {
+    constexpr int K = elem_chunks_per_trip<WS, true>();
     const int64_t op = row * p.ldp, orr = row * p.ldr, oro = row * p.ldro, oo = row * p.ldo;
     const RowSplit sp = row_split(op, p.H);
     const int B = blockDim.x, tid = threadIdx.x;  // B >= 32 > nh + nt
@@ -160,10 +219,21 @@ __device__ __forceinline__ void rms_flat_row(const ElemParams& p, const uint4* c
         const float x = widen1<T>(xs);
         ss = fmaf(x, x, ss);
     }
-    for (int j = tid; j < sp.nb; j += B) {
-        float acc[8];
-        rank_sum<T, 0, false>(acc, s_ptr, p.W, cp + j);
-        (void)residual_chunk<T>(acc, ld_resid(res16 + cr + j), ro16 + cro + j, ss);
+    for (int j0 = tid; j0 < sp.nb; j0 += K * B) {
+        int64_t c[K];
+        bool ok[K];
+        uint4 rv[K];
+#pragma unroll
+        for (int q = 0; q < K; ++q) {
+            c[q] = cp + j0 + q * B;
+            ok[q] = j0 + q * B < sp.nb;
+            if (ok[q]) rv[q] = ld_resid(res16 + cr + j0 + q * B);
+        }
+        float acc[K][8];
+        rank_sum_chunks<T, WS, K>(acc, s_ptr, p.W, c, ok);
+#pragma unroll
+        for (int q = 0; q < K; ++q)
+            if (ok[q]) (void)residual_chunk<T>(acc[q], rv[q], ro16 + cro + j0 + q * B, ss);
     }
     const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
     if (k >= 0) {
@@ -187,8 +257,9 @@ __device__ __forceinline__ void rms_flat_row(const ElemParams& p, const uint4* c
 // second by the thread that wrote it. Tensors whose rows share their
 // 16-byte phase (flat_ok, and every partial pointer aligned) take
 // rms_flat_row instead.
-template <typename T, bool F32P>
-__global__ void __launch_bounds__(kMaxThreads) rms_elem_kernel(ElemParams p) {
+template <typename T, bool F32P, int WS = 0>
+__global__ void __launch_bounds__(kMaxThreads, 2) rms_elem_kernel(ElemParams p) {
+    static_assert(!F32P || WS == 0, "binary32 partials use the run-time rank count");
     __shared__ const uint4* s_ptr[ARF_MAX_W];
     __shared__ float s_warp[2][kMaxThreads / 32];
     prologue(s_ptr, p.lc, p.W);
@@ -196,7 +267,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_elem_kernel(ElemParams p) {
     if constexpr (!F32P) {
         if (vector_layout(p, s_ptr)) {  // the same answer in every thread of every CTA
             int it = 0;
-            for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++it) rms_flat_row<T>(p, s_ptr, row, it, s_warp);
+            for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++it) rms_flat_row<T, WS>(p, s_ptr, row, it, s_warp);
             return;
         }
     }

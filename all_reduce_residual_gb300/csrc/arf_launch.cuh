@@ -232,10 +232,24 @@ cudaError_t launch_rms_t(const RmsParams& p, const arf_plan_t& plan, cudaStream_
     return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
+// The elementwise instance for a call: binary32 partials, else the rank
+// count compiled in where there is one (1, 2, 4, 8; the plan's w_spec does
+// not apply to these kernels), else the run-time rank count.
+template <typename T>
+ElemFn elem_kernel_for(bool rms, bool f32p, int W) {
+    if (f32p) return rms ? rms_elem_kernel<T, true> : ar_elem_kernel<T, true>;
+    switch (W) {
+        case 1: return rms ? rms_elem_kernel<T, false, 1> : ar_elem_kernel<T, false, 1>;
+        case 2: return rms ? rms_elem_kernel<T, false, 2> : ar_elem_kernel<T, false, 2>;
+        case 4: return rms ? rms_elem_kernel<T, false, 4> : ar_elem_kernel<T, false, 4>;
+        case 8: return rms ? rms_elem_kernel<T, false, 8> : ar_elem_kernel<T, false, 8>;
+        default: return rms ? rms_elem_kernel<T, false> : ar_elem_kernel<T, false>;
+    }
+}
+
 template <typename T>
 cudaError_t launch_elem_t(const ElemParams& p, const arf_plan_t& plan, bool rms, cudaStream_t s, bool f32p) {
-    ElemFn fn = rms ? (f32p ? rms_elem_kernel<T, true> : rms_elem_kernel<T, false>)
-                    : (f32p ? ar_elem_kernel<T, true> : ar_elem_kernel<T, false>);
+    ElemFn fn = elem_kernel_for<T>(rms, f32p, p.W);
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.grid);

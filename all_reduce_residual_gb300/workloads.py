@@ -89,18 +89,22 @@ WORKLOADS = {
 # planner sends them to kernels the five do not reach: the bulk-copy kernel
 # for a rank count without a compiled kernel (W = 3 and W = 12), for fp16
 # rows of two chunks per thread with one rank and many rows, and for rows of
-# 32768 elements; and the row kernel's one-CTA-per-row grid for the 80 MiB
-# shape in fp16. Same input recipe.
+# 32768 elements and of 32776 (more than one CTA's row, many rows); the row
+# kernel's one-CTA-per-row grid for the 80 MiB shape in fp16; and the
+# elementwise kernels' 16-byte form for H not a multiple of 8. Same input
+# recipe.
 EXTRA_WORKLOADS = {
     "w3_generic": Workload("w3_generic", 6, 3, 2000, 7168, "bf16", 0.5, 1e-6, ("rmsnorm",)),
     "w12_generic": Workload("w12_generic", 7, 12, 585, 7168, "fp16", 0.1, 1e-6, ("rmsnorm",)),
     "tp4_80mib_fp16": Workload("tp4_80mib_fp16", 8, 4, 5851, 7168, "fp16", 1.0, 1e-6, ("rmsnorm",)),
     "h32768": Workload("h32768", 9, 4, 512, 32768, "bf16", 1.0, 1e-6, ("rmsnorm",)),
     "w1_fp16": Workload("w1_fp16", 10, 1, 4972, 7168, "fp16", 1.0, 1e-6, ("rmsnorm",)),
+    "h32776": Workload("h32776", 11, 2, 1024, 32776, "bf16", 1.0, 1e-6, ("rmsnorm",)),
+    "odd_h4098": Workload("odd_h4098", 12, 2, 4096, 4098, "bf16", 0.5, 1e-5, ("allreduce", "rmsnorm")),
 }
 # The kernel path the planner is expected to take for each extra shape.
 EXTRA_PATHS = {"w3_generic": "bulk", "w12_generic": "bulk", "tp4_80mib_fp16": "row, one CTA per row",
-               "h32768": "bulk", "w1_fp16": "bulk"}
+               "h32768": "bulk", "w1_fp16": "bulk", "h32776": "bulk", "odd_h4098": "elem"}
 
 
 def custom(W: int, M: int, H: int, dtype: str = "bf16", sigma: float = 1.0,

@@ -42,6 +42,7 @@ PATTERNS = ("allreduce", "rmsnorm")
 # the kARResidualRMSNorm kernel of each plan path (arf_path_t order)
 KERNEL_OF_PATH = {0: "ar_flat_kernel", 1: "rms_kernel", 2: "rms_kernel", 3: "rms_async_kernel", 4: "rms_elem_kernel",
                   5: "rms_bulk_kernel"}
+AR_KERNEL_OF_PATH = {0: "ar_flat_kernel", 4: "ar_elem_kernel", 5: "rms_bulk_kernel"}
 CSRC = os.path.join(ROOT, "all_reduce_residual_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
@@ -124,7 +125,8 @@ def measured_peak():
 
 def source_digests(kernel: str) -> dict:
     """SHA-256 of each source file that defines `kernel`."""
-    files = ["arf_kernels.cuh"] + (["arf_bulk.cuh"] if kernel == "rms_bulk_kernel" else [])
+    files = ["arf_kernels.cuh"] + (["arf_bulk.cuh"] if kernel == "rms_bulk_kernel" else []) + \
+        (["arf_elem.cuh"] if kernel.endswith("_elem_kernel") else [])
     return {f: hashlib.sha256(open(os.path.join(CSRC, f), "rb").read()).hexdigest() for f in files}
 
 
@@ -293,7 +295,7 @@ def run_arf(args):
     achieved = bytes_call[dom] / dom_s / 1e9
     dt_torch = torch.bfloat16 if w.dtype == "bf16" else torch.float16
     plans = {p: (plan if plan is not None else ws.plan(p, w.W, w.M, w.H, dt_torch)) for p in pats}
-    kname = KERNEL_OF_PATH[plans[dom].path] if dom == "rmsnorm" else "ar_flat_kernel"
+    kname = (KERNEL_OF_PATH if dom == "rmsnorm" else AR_KERNEL_OF_PATH)[plans[dom].path]
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kname, args.workload),
                 "kernel": kname, "algorithmic_bytes_per_launch": bytes_call[dom], "peak_source": peak_src,

@@ -97,7 +97,7 @@ def test_strided_rows_vector_form(ws, pattern, H, pads):
     form row by row, with heads that differ from row to row where the
     stride is not a multiple of 8; padding stays untouched. Planner plans and
     explicit ones with the narrowest and widest CTAs."""
-    for i, W in enumerate((1, 3, 8)):
+    for i, W in enumerate((1, 2, 3, 4, 8)):
         dtype = "bf16" if i % 2 == 0 else "fp16"
         run_case(ws, pattern, dtype, W, 37, H, pads=pads, seed=H + W)
         for threads, grid in ((32, 5), (512, 64)):
@@ -125,6 +125,19 @@ def test_explicit_elementwise_plans(ws, pattern, M, H):
         for grid in (1, 7, 300):
             plan = arf.Plan(path=arf.ARF_PATH_ELEM, threads=threads, vpt=1, cluster=1, grid=grid, w_spec=0)
             run_case(ws, pattern, "fp16", 3, M, H, plan=plan, seed=threads + grid)
+
+
+@pytest.mark.parametrize("W", [1, 2, 4, 8, 5])
+def test_odd_h_in_place(ws, W):
+    """residual_out == residual on the elementwise kernels' vector form (each
+    thread reads a chunk of the residual before it writes the same chunk,
+    two chunks per trip for W <= 2), against the oracle."""
+    from gpu_util import gpu_run, oracle_run, to_device
+    inp = wl.make_inputs(wl.custom(W, 300, 4098, "bf16" if W % 2 == 0 else "fp16", 0.7, 1e-6, config_id=4100 + W))
+    P, R, G = to_device(inp)
+    got = gpu_run(ws, RMS, P, R, G, inp.workload.eps, in_place=True)
+    assert_parity(DT[inp.workload.dtype], RMS, got, oracle_run(RMS, inp), f"W={W}")
+    assert ws.plan(RMS, W, 300, 4098, P[0].dtype).path == arf.ARF_PATH_ELEM
 
 
 def test_two_byte_aligned_tensors(ws):
@@ -178,17 +191,18 @@ def test_layout_argument_errors(ws):
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("W", [2, 3, 4])
 @pytest.mark.parametrize("M,H", [(5, 13), (64, 7170), (3, 1), (7, 1001), (2, 24579)])
 @pytest.mark.parametrize("misaligned", [False, True])
 @pytest.mark.parametrize("pattern", [AR, RMS])
-def test_odd_h_flat_range(ws, pattern, M, H, misaligned):
+def test_odd_h_flat_range(ws, pattern, M, H, misaligned, W):
     """Contiguous tensors with H % 8 != 0: the whole tensor is one flat range
     (kAllReduce: 16-byte body and elementwise tail; kARResidualRMSNorm: each
     row's aligned chunks with an elementwise head and tail) when every partial
     pointer is 16-byte aligned, and plain elementwise when one is only 2-byte
-    aligned. Both match the oracle."""
-    W = 3
-    rng = np.random.default_rng(M * 7 + H)
+    aligned. Both match the oracle, with the rank count compiled in (W = 2, 4)
+    or not (W = 3)."""
+    rng = np.random.default_rng(M * 7 + H + W)
     P = [codes_of(rng, oracle.BF16, (M, H), 1.0) for _ in range(W)]
     R = codes_of(rng, oracle.BF16, (M, H), 1.0)
     G = pins.nearest_codes(oracle.BF16, 0.5 + rng.random(H))

@@ -35,6 +35,8 @@ def test_workload_parity(ws, name, M, pattern):
         plan = ws.plan(pattern, len(P), M, inp.workload.H, P[0].dtype)
         if wl.EXTRA_PATHS[name] == "bulk":
             assert plan.path == arf.ARF_PATH_BULK, plan
+        elif wl.EXTRA_PATHS[name] == "elem":
+            assert plan.path == arf.ARF_PATH_ELEM, plan
         else:
             assert plan.path == arf.ARF_PATH_ROW and plan.grid == M, plan
     got = gpu_run(ws, pat, P, R, G, inp.workload.eps)
