@@ -134,7 +134,11 @@ constexpr size_t async_dyn_smem(int W, int stages, int C) {
 // static shared memory; its dynamic shared memory for W ranks, `stages`
 // slots of `threads` chunks per rank and rows of C chunks.
 constexpr int kBulkMaxStages = 16;
-constexpr int kBulkStaticSmem = 1024;  // upper bound, for the planner
+// Its __shared__ arrays: s_ptr (8 * ARF_MAX_W bytes), s_warp (2 * kMaxThreads
+// / 32 floats) and s_bar (8 * kBulkMaxStages bytes); the kAllReduce form
+// drops s_warp. With the 1 KB the SM reserves per CTA, this is what decides
+// whether two CTAs of long rows fit on one SM.
+constexpr int kBulkStaticSmem = 8 * ARF_MAX_W + 2 * (kMaxThreads / 32) * 4 + 8 * kBulkMaxStages;
 constexpr size_t bulk_dyn_smem(int W, int stages, int threads, int C) {
     return (size_t)stages * (size_t)(W + 1) * (size_t)threads * 16u + (size_t)C * 16u;
 }

@@ -14,6 +14,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "arf.h")
 
 GB300 = arf.DeviceCaps(num_sms=152, max_cluster=16, max_threads_per_sm=2048, max_smem_per_block=232448)
+# the bulk kernel's static shared memory: 64 partial pointers, 2 x 16 warp
+# sums, 16 mbarriers
+BULK_STATIC = 8 * 64 + 2 * 16 * 4 + 8 * 16
 K3_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048)
 SHAPES = [(2, 8, 1024), (2, 128, 4096), *[(8, m, 7168) for m in K3_M], (4, 5851, 7168), (16, 585, 7168),
           (1, 1, 8), (3, 7, 8), (64, 3, 32768), (5, 1000, 1000), (17, 200, 2048),
@@ -146,7 +149,7 @@ def test_planner_plans_are_legal(pattern, W, M, H):
             per_sm = caps.max_smem_per_block + 1024
 
             def fits(per, stages):
-                need = stages * (W + 1) * p.threads * 16 + C * 16 + 1024
+                need = stages * (W + 1) * p.threads * 16 + C * 16 + BULK_STATIC
                 room = per_sm // per - 1024 if per > 1 else caps.max_smem_per_block
                 return need <= room and per * p.threads <= caps.max_threads_per_sm
 
@@ -199,7 +202,7 @@ def test_long_rows_split_over_clusters(H, M):
     through the bulk ring where its row buffer fits; kAllReduce is flat and
     takes any H <= ARF_MAX_H."""
     p = arf.Plan()
-    bulk = 2 * M >= 152 and (H // 8) * 16 + 1024 + 2 * 9 * 256 * 16 <= 232448
+    bulk = 2 * M >= 152 and (H // 8) * 16 + BULK_STATIC + 2 * 9 * 256 * 16 <= 232448
     assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
     if bulk:
         assert p.path == arf.ARF_PATH_BULK and p.threads <= 512
@@ -241,13 +244,15 @@ def test_long_rows_take_the_bulk_ring_when_rows_are_many():
     half the SMs, the bulk ring from there while its row buffer fits."""
     p = arf.Plan()
     for W, M, H in ((2, 16, 32776), (2, 76, 32776), (2, 2048, 32776), (8, 608, 32776), (4, 64, 65536),
-                    (4, 152, 65536), (12, 300, 40000), (13, 300, 40000), (2, 500, 131072), (8, 500, 78848),
-                    (8, 500, 78856), (8, 500, 106496)):
+                    (4, 152, 65536), (12, 300, 40000), (13, 300, 40000), (2, 500, 131072), (8, 500, 78976),
+                    (8, 500, 78984), (8, 500, 106496), (2, 1024, 32776)):
         assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
         assert arf.arf_plan_check(GB300, p, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16) == arf.ARF_OK
-        fits = (H // 8) * 16 + 1024 + 2 * (W + 1) * 256 * 16 <= 232448  # blocks of >= 256 chunks
+        fits = (H // 8) * 16 + BULK_STATIC + 2 * (W + 1) * 256 * 16 <= 232448  # blocks of >= 256 chunks
         if 2 * M >= 152 and W <= 12 and fits:
             assert p.path == arf.ARF_PATH_BULK, (W, M, H, p)
+            if (W, H) == (2, 32776):  # 114 704 B of ring and row buffer: two CTAs per SM, 2 slots
+                assert p.threads == 512 and p.stages == 2 and p.grid == min(M, 304), p
         else:
             assert p.path == arf.ARF_PATH_CLUSTER, (W, M, H, p)
 
@@ -317,8 +322,8 @@ def test_plan_check_rejects_bad_plans():
 def test_bulk_plan_rules():
     """ARF_PATH_BULK: no cluster, vpt 1, 2..16 ring slots, and (W+1) x slots x
     threads x 16 bytes of ring plus the 16-byte row buffer (kAllReduce: W x
-    slots x threads x 16 bytes) must fit the opt-in shared memory (1 KiB kept
-    for static use)."""
+    slots x threads x 16 bytes) must fit the opt-in shared memory with the
+    kernel's static arrays."""
     rms16 = (arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7168, arf.ARF_FP16)
 
     def check(caps=GB300, args=rms16, **kw):
@@ -334,13 +339,13 @@ def test_bulk_plan_rules():
     assert check(stages=17) == arf.ARF_ERR_UNSUPPORTED
     assert check(vpt=2) == arf.ARF_ERR_UNSUPPORTED
     assert check(cluster=2, grid=304) == arf.ARF_ERR_UNSUPPORTED
-    # kAllReduce form: partials only, no row buffer: 16 x S x 128 x 16 + 1024 <= 232448  <=>  S <= 7
+    # kAllReduce form: partials only, no row buffer: 16 x S x 128 x 16 + 768 <= 232448  <=>  S <= 7
     ar16 = (arf.ARF_ALLREDUCE, 16, 585, 7168, arf.ARF_FP16)
     assert check(args=ar16, stages=7) == arf.ARF_OK
     assert check(args=ar16, stages=8) == arf.ARF_ERR_UNSUPPORTED
     assert check(args=(arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7170, arf.ARF_FP16)) == arf.ARF_ERR_UNSUPPORTED
-    # shared memory: 17 x S x 128 x 16 + 896 x 16 + 1024 <= 232448  <=>  S <= 6
-    ring = lambda s, t=128, w=16, c=896: (w + 1) * s * t * 16 + c * 16 + 1024  # noqa: E731
+    # shared memory: 17 x S x 128 x 16 + 896 x 16 + 768 <= 232448  <=>  S <= 6
+    ring = lambda s, t=128, w=16, c=896: (w + 1) * s * t * 16 + c * 16 + BULK_STATIC  # noqa: E731
     assert ring(6) <= GB300.max_smem_per_block < ring(7)
     assert check(stages=7) == arf.ARF_ERR_UNSUPPORTED
     assert check(threads=64, stages=12) == arf.ARF_OK and ring(12, 64) <= 232448 < ring(13, 64)
