@@ -241,13 +241,21 @@ __device__ __forceinline__ void rms_flat_row(const ElemParams& p, const uint4* c
         const float g = widen1<T>(p.gamma[k]);
         p.out[oo + k] = narrow1<T>(__fmul_rn(__fmul_rn(x, inv), g));
     }
+    // Second pass: gamma is one 16-byte load where the row's chunks start on
+    // a 16-byte boundary of an aligned gamma, else eight element loads.
+    const bool g_vec = sp.nh == 0 && (reinterpret_cast<uintptr_t>(p.gamma) & 15u) == 0;
+    const uint4* g16 = reinterpret_cast<const uint4*>(p.gamma);
     for (int j = tid; j < sp.nb; j += B) {
-        const unsigned short* gp = p.gamma + sp.nh + 8 * j;
         uint4 gv;
-        gv.x = (uint32_t)__ldg(gp + 0) | ((uint32_t)__ldg(gp + 1) << 16);
-        gv.y = (uint32_t)__ldg(gp + 2) | ((uint32_t)__ldg(gp + 3) << 16);
-        gv.z = (uint32_t)__ldg(gp + 4) | ((uint32_t)__ldg(gp + 5) << 16);
-        gv.w = (uint32_t)__ldg(gp + 6) | ((uint32_t)__ldg(gp + 7) << 16);
+        if (g_vec) {
+            gv = ld_keep(g16 + j);
+        } else {
+            const unsigned short* gp = p.gamma + sp.nh + 8 * j;
+            gv.x = (uint32_t)__ldg(gp + 0) | ((uint32_t)__ldg(gp + 1) << 16);
+            gv.y = (uint32_t)__ldg(gp + 2) | ((uint32_t)__ldg(gp + 3) << 16);
+            gv.z = (uint32_t)__ldg(gp + 4) | ((uint32_t)__ldg(gp + 5) << 16);
+            gv.w = (uint32_t)__ldg(gp + 6) | ((uint32_t)__ldg(gp + 7) << 16);
+        }
         normalise_chunk<T>(ro16[cro + j], gv, inv, out16 + co + j);
     }
 }

@@ -140,6 +140,32 @@ def test_odd_h_in_place(ws, W):
     assert ws.plan(RMS, W, 300, 4098, P[0].dtype).path == arf.ARF_PATH_ELEM
 
 
+@pytest.mark.parametrize("ld", [4098, 4104])
+@pytest.mark.parametrize("g_off", [0, 1])
+def test_vector_form_gamma_alignment(ws, ld, g_off):
+    """kARResidualRMSNorm's vector form with H = 4098: rows whose chunks start
+    on a 16-byte boundary (every row at ld = 4104, one in four contiguous)
+    load gamma as 16-byte vectors when gamma is aligned, element by element
+    when it sits at a 2-byte offset (g_off = 1); all match the oracle."""
+    M, H, W = 41, 4098, 2
+    rng = np.random.default_rng(ld + g_off)
+    P = [codes_of(rng, oracle.BF16, (M, H), 1.0) for _ in range(W)]
+    R = codes_of(rng, oracle.BF16, (M, H), 1.0)
+    G = pins.nearest_codes(oracle.BF16, 0.5 + rng.random(H))
+    pad = ld - H
+    Pd = [embed(p, pad, np.uint16(0x7FC1), "bf16")[0] for p in P]
+    Rd, _ = embed(R, pad, np.uint16(0x7FC1), "bf16")
+    Od, _ = embed(np.zeros((M, H), np.uint16), pad, np.uint16(0x1234), "bf16")
+    ROd, _ = embed(np.zeros((M, H), np.uint16), pad, np.uint16(0x1234), "bf16")
+    gbuf = torch.zeros(H + 8, dtype=torch.int16, device="cuda")
+    Gd = gbuf[g_off:g_off + H].view(torch.bfloat16)
+    Gd.copy_(wl.from_codes(G, "bf16").cuda())
+    arf.run(ws, RMS, Pd, Rd, Gd, 1e-6, out=Od, residual_out=ROd)
+    torch.cuda.synchronize()
+    ref = oracle.run_general(oracle.AR_RESIDUAL_RMSNORM, P, R, G, 1e-6, dtype=oracle.BF16)
+    assert_parity(oracle.BF16, RMS, (host_codes(Od), host_codes(ROd)), ref, f"ld={ld} g_off={g_off}")
+
+
 def test_two_byte_aligned_tensors(ws):
     """out / residual / gamma / residual_out at 2-byte (not 16-byte) offsets:
     the elementwise kernels; an odd address is refused."""
