@@ -193,10 +193,11 @@ __global__ void __launch_bounds__(kMaxThreads, 2) ar_elem_kernel(ElemParams p) {
 // phase (flat_ok, partials checked by the caller): the row splits into a
 // head of fewer than 8 elements up to the first 16-byte boundary (threads
 // 0..), whole 16-byte chunks, and a tail of fewer than 8 elements (the last
-// threads), at each tensor's own row offset. gamma, indexed from the row
-// start, is read element by element from L1. Same arithmetic as the
-// elementwise rows; residual_out is re-read in the second pass by the
-// thread that wrote it.
+// threads), at each tensor's own row offset. gamma is indexed from the row
+// start and read from L1, as 16-byte vectors where the row's chunks start
+// on a 16-byte boundary of an aligned gamma, else element by element. Same
+// arithmetic as the elementwise rows; residual_out is re-read in the second
+// pass by the thread that wrote it. WS > 0: W == WS compiled in.
 template <typename T, int WS>
 __device__ __forceinline__ void rms_flat_row(const ElemParams& p, const uint4* const* s_ptr, int64_t row, int it,
                                              float (*s_warp)[kMaxThreads / 32]) {
