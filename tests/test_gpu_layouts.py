@@ -105,6 +105,34 @@ def test_strided_rows_vector_form(ws, pattern, H, pads):
             run_case(ws, pattern, dtype, W, 37, H, pads=pads, plan=plan, seed=H + W + threads)
 
 
+@pytest.mark.parametrize("case", range(45))
+def test_fuzz_elementwise_layouts(ws, case):
+    """Seeded random layouts against the oracle: contiguous tensors, row
+    strides congruent modulo 8 (the vector forms) or arbitrary (one element
+    per thread), any H, compiled and run-time rank counts, and the planner's
+    plan or a random elementwise one."""
+    rng = np.random.default_rng(7000 + case)
+    W = int(rng.choice([1, 2, 3, 4, 5, 8, 16, 17]))
+    M = int(rng.choice([1, 2, 7, 33, 150]))
+    H = int(rng.integers(1, 9000))
+    H = max(1, min(H, 3_000_000 // (M * W)))
+    kind = case % 3
+    if kind == 0:
+        pads = (0, 0, 0, 0)
+    elif kind == 1:
+        base = int(rng.integers(0, 8))
+        pads = tuple(base + 8 * int(rng.integers(0, 3)) for _ in range(4))
+    else:
+        pads = tuple(int(rng.integers(0, 20)) for _ in range(4))
+    plan = None
+    if rng.random() < 0.5:
+        plan = arf.Plan(path=arf.ARF_PATH_ELEM, threads=32 * int(rng.integers(1, 17)), vpt=1, cluster=1,
+                        grid=int(rng.integers(1, 2000)), w_spec=0)
+    pattern = AR if rng.random() < 0.4 else RMS
+    dtype = "bf16" if rng.random() < 0.5 else "fp16"
+    run_case(ws, pattern, dtype, W, M, H, pads=pads, plan=plan, seed=7000 + case)
+
+
 @pytest.mark.parametrize("W", [1, 2, 3, 8, 17])
 @pytest.mark.parametrize("M,H", [(1, 8), (37, 4096), (300, 7168), (5, 13), (2, 65536)])
 @pytest.mark.parametrize("pattern", [AR, RMS])
