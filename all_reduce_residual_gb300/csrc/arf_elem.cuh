@@ -48,6 +48,24 @@ __device__ __forceinline__ float elem_rank_sum(const uint4* const* s_ptr, int W,
     return acc;
 }
 
+// elem_rank_sum for the vector forms' head and tail elements: with W == WS
+// compiled in, every partial's load is issued before the first add (the
+// run-time loop waits out one load latency per rank).
+template <typename T, int WS>
+__device__ __forceinline__ float elem_rank_sum_w(const uint4* const* s_ptr, int W, int64_t i) {
+    if constexpr (WS > 0) {
+        unsigned short v[WS];
+#pragma unroll
+        for (int r = 0; r < WS; ++r) v[r] = reinterpret_cast<const unsigned short*>(s_ptr[r])[i];
+        float acc = 0.0f;
+#pragma unroll
+        for (int r = 0; r < WS; ++r) acc = MixedAdd<T>::add(acc, v[r]);
+        return acc;
+    } else {
+        return elem_rank_sum<T, false>(s_ptr, W, i);
+    }
+}
+
 // The split of one row into 16-byte vectors. All tensors of the call start
 // row r at the same offset modulo 8 elements (flat_ok != 0), so one split
 // serves them all: nh head elements up to the first 16-byte boundary, nb
@@ -147,7 +165,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) ar_elem_kernel(ElemParams p) {
                     if (ok[q]) st_out(out16 + c[q], Pack8<T>::narrow(acc[q]));
             }
             for (int64_t e = nch * 8 + first; e < total; e += stride)
-                p.out[e] = narrow1<T>(elem_rank_sum<T, false>(s_ptr, p.W, e));
+                p.out[e] = narrow1<T>(elem_rank_sum_w<T, WS>(s_ptr, p.W, e));
             return;
         }
         if (vector_layout(p, s_ptr)) {
@@ -157,7 +175,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) ar_elem_kernel(ElemParams p) {
                 const int64_t op = row * p.ldp, oo = row * p.ldo;
                 const RowSplit sp = row_split(op, p.H);
                 const int k = tid < sp.nh ? tid : (tid >= B - sp.nt ? sp.nh + 8 * sp.nb + (tid - (B - sp.nt)) : -1);
-                if (k >= 0) p.out[oo + k] = narrow1<T>(elem_rank_sum<T, false>(s_ptr, p.W, op + k));
+                if (k >= 0) p.out[oo + k] = narrow1<T>(elem_rank_sum_w<T, WS>(s_ptr, p.W, op + k));
                 const int64_t cp = (op + sp.nh) / 8, co = (oo + sp.nh) / 8;
                 for (int j0 = tid; j0 < sp.nb; j0 += K * B) {
                     int64_t c[K];
@@ -213,8 +231,9 @@ __device__ __forceinline__ void rms_flat_row(const ElemParams& p, const uint4* c
     uint4* out16 = reinterpret_cast<uint4*>(p.out);
     float ss = 0.0f;
     if (k >= 0) {
-        float acc = elem_rank_sum<T, false>(s_ptr, p.W, op + k);
-        acc = MixedAdd<T>::add(acc, p.residual[orr + k]);
+        const unsigned short rk = p.residual[orr + k];  // read before residual_out (maybe the same) is written
+        float acc = elem_rank_sum_w<T, WS>(s_ptr, p.W, op + k);
+        acc = MixedAdd<T>::add(acc, rk);
         const unsigned short xs = narrow1<T>(acc);
         p.residual_out[oro + k] = xs;
         const float x = widen1<T>(xs);
