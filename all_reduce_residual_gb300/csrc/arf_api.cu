@@ -555,7 +555,7 @@ bool odd(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) != 0; }
 // and whether the 16-byte kernels can take the layout.
 arf_status_t check_call(arf_pattern_t pattern, const arf_run_opts_t* opts, bool by_value,
                         const void* const* partials, const void* residual, const void* gamma, float eps,
-                        const void* out, const void* residual_out, int64_t H, Layout* ly) {
+                        const void* out, const void* residual_out, int64_t M, int64_t H, Layout* ly) {
     if (!partials || !out) return ARF_ERR_INVALID_ARG;
     const bool rms = pattern == ARF_AR_RESIDUAL_RMSNORM;
     ly->ldp = opts && opts->ld_partials ? opts->ld_partials : H;
@@ -572,6 +572,11 @@ arf_status_t check_call(arf_pattern_t pattern, const arf_run_opts_t* opts, bool 
         if (residual == residual_out && ly->ldr != ly->ldro) return ARF_ERR_INVALID_ARG;
         if (odd(residual) || odd(gamma) || odd(residual_out)) return ARF_ERR_UNSUPPORTED;
     }
+    // every tensor's extent, M rows of its stride, stays inside the bound
+    // arf_supports puts on M*H, so that no index computation can overflow
+    const int64_t max_ld = ((int64_t)1 << 40) / (M > 0 ? M : 1);
+    if (ly->ldp > max_ld || ly->ldo > max_ld || (rms && (ly->ldr > max_ld || ly->ldro > max_ld)))
+        return ARF_ERR_UNSUPPORTED;
     if (odd(out)) return ARF_ERR_UNSUPPORTED;
     if (!by_value && (reinterpret_cast<uintptr_t>(partials) & 7u) != 0) return ARF_ERR_UNSUPPORTED;
     bool v = H % 8 == 0 && ly->ldp % 8 == 0 && ly->ldo % 8 == 0 && aligned16(out);
@@ -719,7 +724,7 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
     }
     if (M == 0) return ARF_OK;
     Layout L;
-    st = check_call(pattern, opts, by_value, partials, residual, gamma, eps, out, residual_out, H, &L);
+    st = check_call(pattern, opts, by_value, partials, residual, gamma, eps, out, residual_out, M, H, &L);
     if (st != ARF_OK) return st;
     if (forced && forced->path != ARF_PATH_ELEM) {
         // an explicit 16-byte plan needs a layout those kernels take; binary32

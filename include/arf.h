@@ -293,8 +293,10 @@ typedef struct arf_run_opts {
                                 what overlaps is launch latency. */
     int64_t ld_partials;     /* row strides in elements (0 = H, contiguous): of */
     int64_t ld_residual;     /* every partial, the residual, out and            */
-    int64_t ld_out;          /* residual_out. Each must be >= H. Strides that   */
-    int64_t ld_residual_out; /* are multiples of 8 keep the 16-byte kernels.    */
+    int64_t ld_out;          /* residual_out. Each must be >= H                 */
+    int64_t ld_residual_out; /* (ARF_ERR_INVALID_ARG) and M * stride <= 2^40
+                                (ARF_ERR_UNSUPPORTED). Strides that are
+                                multiples of 8 keep the 16-byte kernels. */
     int partials_f32;        /* 1: the partials are binary32 [M,H] tensors (the
                                 I/O dtype still applies to residual, gamma and
                                 the outputs); they enter the binary32 rank-order

@@ -235,6 +235,8 @@ def test_layout_argument_errors(ws):
                               out.data_ptr(), R.data_ptr(), M, H, arf.ARF_BF16, s)
 
     assert call(ld_partials=32) == arf.ARF_ERR_INVALID_ARG          # stride below H
+    assert call(ld_partials=(1 << 38) + 8) == arf.ARF_ERR_UNSUPPORTED  # M x stride above 2^40
+    assert call(ld_out=1 << 62) == arf.ARF_ERR_UNSUPPORTED
     assert call(ld_residual=72, ld_residual_out=80) == arf.ARF_ERR_INVALID_ARG  # in place, strides differ
     assert call() == arf.ARF_OK                                      # in place, equal strides
     plan = arf.Plan(path=arf.ARF_PATH_ROW, threads=32, vpt=2, cluster=1, grid=4, w_spec=2)
