@@ -417,3 +417,25 @@ def test_planner_bulk_choices():
         assert p.path == path, (W, M, H)
         if grid is not None:
             assert p.grid == grid, (W, M, H, p)
+
+
+def test_workload_tables_agree_with_the_planner():
+    """Every extra workload names the kernel path it exists to reach, and the
+    planner (on GB300's capabilities) sends each of its patterns there; the
+    benchmark can name the kernel of every plan any workload gets."""
+    import os
+    import sys
+    from all_reduce_residual_gb300 import workloads as wl
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    assert set(wl.EXTRA_PATHS) == set(wl.EXTRA_WORKLOADS)
+    want = {"bulk": arf.ARF_PATH_BULK, "elem": arf.ARF_PATH_ELEM, "row, one CTA per row": arf.ARF_PATH_ROW}
+    for name, w in {**wl.WORKLOADS, **wl.EXTRA_WORKLOADS}.items():
+        dt = arf.ARF_BF16 if w.dtype == "bf16" else arf.ARF_FP16
+        for pat in w.patterns:
+            p = arf.Plan()
+            assert arf.arf_plan_for_caps(GB300, arf.pattern_code(pat), w.W, w.M, w.H, dt, p) == arf.ARF_OK
+            table = bench.KERNEL_OF_PATH if pat == "rmsnorm" else bench.AR_KERNEL_OF_PATH
+            assert p.path in table, (name, pat, p)
+            if name in wl.EXTRA_PATHS:
+                assert p.path == want[wl.EXTRA_PATHS[name]], (name, pat, p)
