@@ -802,9 +802,19 @@ std::vector<arf_plan_t> tune_candidates(const arf_device_caps_t& caps, const arf
     };
     add(base);
     if (base.path == ARF_PATH_ELEM) {
+        // each CTA width with the base grid, and with as many of its CTAs as
+        // the SMs hold by thread count (capped at the rows, or kAllReduce's
+        // row tiles): the shapes that won the measured sweeps were of the
+        // second kind (128 x 8 SMs, 256 x 4 SMs, 512 x 2 SMs)
         for (int t : {64, 128, 256, 512}) {
             arf_plan_t p = base;
             p.threads = t;
+            add(p);
+            const int per_sm = caps.max_threads_per_sm / t > 0 ? caps.max_threads_per_sm / t : 1;
+            const int64_t full = (int64_t)caps.num_sms * per_sm;
+            const int64_t units = pattern == ARF_ALLREDUCE ? ceil_div(H, t) * M : M;
+            const int64_t g = units < full ? units : full;
+            p.grid = (int)(g > 0 ? g : 1);
             add(p);
         }
         return out;
