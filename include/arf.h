@@ -245,7 +245,9 @@ arf_status_t arf_run(arf_workspace_t ws, arf_pattern_t pattern, int W,
  * keep the fastest in the workspace: later arf_run calls of the same
  * (pattern, W, M, H, dtype) use it. Candidates: the planner's plan and its
  * neighbours (threads, chunks per thread, cluster size, compiled or run-time
- * rank count) that pass arf_plan_check and fit the device. Each runs `reps`
+ * rank count, bulk ring width and depth; for the elementwise path each CTA
+ * width with the planner's grid and with a device-full grid) that pass
+ * arf_plan_check and fit the device. Each runs `reps`
  * times (<= 0: 20) back to back on `stream`, timed with CUDA events after two
  * warm-up calls; the call synchronises the stream, so it cannot be captured.
  * Buffers and arguments are those of an arf_run call; the outputs are
