@@ -1,19 +1,20 @@
 """Benchmark of the all-reduce fusion epilogue on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl arf|reference]
-                    [--workload NAME] [--no-sweep]
+                    [--workload NAME] [--sweep-out FILE]
 
 One step = one pass of the whole hot path over one batch: a kAllReduce call
-and a kARResidualRMSNorm call on the workload's partials (default workload:
-Llama-3-8B-like TP2 decode, W=2, M=128, H=4096, bf16). The L2 is flushed
-before every step, outside the timed events: a write of twice its size, then
-a read of another buffer of twice its size. The read evicts the flush's own
-dirty lines, so their write-back to HBM is not charged to the timed kernels
-(a write-only flush adds 5-13 us of such write-backs to each call here); the
-sweep reports both.
+and a kARResidualRMSNorm call on the workload's partials. The default
+workload is the largest one-GPU configuration, the 80 MiB-per-partial TP4
+payload (W=4, M=5851, H=7168, bf16). The L2 is flushed before every step,
+outside the timed events: a write of twice its size, then a read of another
+buffer of twice its size. The read evicts the flush's own dirty lines, so
+their write-back to HBM is not charged to the timed kernels.
 Metric: achieved HBM GB/s = algorithmic bytes / device time, where the
 algorithmic bytes read every partial and the residual once, gamma once and
-write each output once. Rank 0 prints one JSON line.
+write each output once. Rank 0 prints one JSON line, the last line of
+standard output. --sweep-out writes the per-configuration table (every
+workload, pattern and K3 row count) to a JSON file instead.
 
 N > 1 (torchrun, one process per GPU): every rank runs its own replica of the
 workload (the path has no exchange step on one GPU); value = bytes of all
@@ -50,11 +51,12 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("arf", "reference"), default="arf")
-    ap.add_argument("--workload", default="llama_tp2")
-    ap.add_argument("--no-sweep", action="store_true", help="skip the per-config sweep table")
+    ap.add_argument("--workload", default="tp4_80mib")
+    ap.add_argument("--sweep-out", default=None,
+                    help="also time every workload, pattern and K3 row count and write the table to this JSON file")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--m", type=int, default=None, help="override the workload's row count M (for profiling)")
@@ -218,7 +220,7 @@ class L2Flush:
 
     def describe(self):
         mib = self.nbytes >> 20
-        return f"flushed before every step: write {mib} MiB, then read another {mib} MiB (L2 left clean)"
+        return f"flush before each step: write {mib} MiB, read another {mib} MiB"
 
 
 # ---------------------------------------------------------------------------
@@ -264,17 +266,20 @@ def run_arf(args):
         arf.run(ws, p, P, R, G, w.eps, out=outs[p], residual_out=ro if p == "rmsnorm" else None, ptrs=ptrs,
                 plan=plan)
 
-    for _ in range(args.warmup):
+    def step():
         flush.zero_()
         for p in pats:
             call(p)
-    torch.cuda.synchronize()
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(pats) + 1)] for _ in range(K)]
-    barrier(world)
-    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        t_timed = time.perf_counter()
         for k in range(K):
             flush.zero_()
             ev[k][0].record(stream)
@@ -282,7 +287,16 @@ def run_arf(args):
                 call(p)
                 ev[k][i + 1].record(stream)
         torch.cuda.synchronize()
-    barrier(world)
+        barrier(world)
+        t_timed = time.perf_counter() - t_timed
+        # nvidia-smi samples every 200 ms: a timed region shorter than a
+        # second is followed by untimed repetitions of the same step, so that
+        # the clock record holds samples taken under this load
+        t_extra = time.perf_counter()
+        while t_timed + (time.perf_counter() - t_extra) < 1.0:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
     per_call = {p: [ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)] for i, p in enumerate(pats)}
     step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
     total_s = sum(step_ms) / 1e3
@@ -296,10 +310,17 @@ def run_arf(args):
     dt_torch = torch.bfloat16 if w.dtype == "bf16" else torch.float16
     plans = {p: (plan if plan is not None else ws.plan(p, w.W, w.M, w.H, dt_torch)) for p in pats}
     kname = (KERNEL_OF_PATH if dom == "rmsnorm" else AR_KERNEL_OF_PATH)[plans[dom].path]
+    traffic = recorded_traffic(kname, w.name if args.m is None else None)
+    steady_us = steady_state_us(lambda: call(dom), dev, stream)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kname, args.workload),
-                "kernel": kname, "algorithmic_bytes_per_launch": bytes_call[dom], "peak_source": peak_src,
-                "timing": "mean CUDA-event time per launch, L2 flushed before each step"}
+                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kname,
+                "algorithmic_bytes_per_launch": bytes_call[dom],
+                "peak_source": f"{peak_src} hbm_gbs (copy)",
+                "frac_basis": "cold: mean event time per launch in the timed steps",
+                "steady_frac": round(bytes_call[dom] / (steady_us * 1e-6) / 1e9 / peak, 4),
+                "steady_us": round(steady_us, 3),
+                "steady_basis": "graph of 20 back-to-back launches; each pays the L2 write-backs of the last",
+                "dram_over_algorithmic": round(traffic / bytes_call[dom], 4) if traffic else None}
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -308,25 +329,29 @@ def run_arf(args):
         "data": "synthetic (seeded N(0,s) partials, residual N(0,1), gamma U(0.5,1.5), rounded to the I/O dtype)",
         "config": {"workload": f"{w.name}: W={w.W} M={w.M} H={w.H} {w.dtype}, one {' + one '.join(pats)} call per step",
                    "W": w.W, "M": w.M, "H": w.H, "io_dtype": w.dtype, "accumulate": "f32",
-                   "patterns": list(pats), "bytes_per_step": step_bytes,
-                   "l2": flush.describe(),
-                   "parallelism": f"replicas x{world}",
-                   "plans": {p: plans[p].as_dict() for p in pats},
+                   "bytes_per_step": step_bytes, "l2": flush.describe(), "parallelism": f"replicas x{world}",
+                   "plans": {p: plan_str(plans[p]) for p in pats},
                    "plan_source": "explicit (--plan)" if plan is not None else "planner"},
         "us_per_call": {p: round(statistics.mean(v) * 1e3, 3) for p, v in per_call.items()},
+        "frac_per_call": {p: round(bytes_call[p] / (statistics.mean(v) * 1e-3) / 1e9 / peak, 4)
+                          for p, v in per_call.items()},
         "roofline": roofline,
         "gpu_launches": len(pats) * K,
-        "clocks": clk.summary(),
+        "clocks": {**clk.summary(),
+                   "window": "warm-up and timed steps" + (", then untimed steps to 1 s" if t_timed < 1.0 else "")},
     }
     if not args.no_e2e:
         result["e2e"] = e2e_leg(ws, w, inp, pats, flush, dev, K, world)
     result["roofline_context"] = roofline_context(ws, dev, flush, w, dom, per_call[dom])
-    if not args.no_sweep and world == 1:  # the scaling runs (N > 1) time the headline only
-        result["sweep"] = sweep(ws, dev, flush, peak)
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(w, inp, budget_s=10.0)
+    if args.sweep_out and world == 1:  # the scaling runs (N > 1) time the headline only
+        rows = sweep(ws, dev, flush, peak)
+        with open(args.sweep_out, "w") as f:
+            json.dump({"peak_gbs": peak, "peak_source": peak_src, "clocks": result["clocks"], "rows": rows}, f,
+                      indent=1)
     if rank == 0:
-        print(json.dumps(result), flush=True)
+        print(json.dumps(result, separators=(",", ":")), flush=True)
     ws.close()
     if world > 1:
         import torch.distributed as dist
@@ -334,15 +359,57 @@ def run_arf(args):
         dist.destroy_process_group()
 
 
+def plan_str(p) -> str:
+    """A launch plan in one short string: path threads x chunks per thread
+    (bulk: ring slots), cluster, grid."""
+    names = {0: "flat", 1: "row", 2: "cluster", 3: "async", 4: "elem", 5: "bulk"}
+    s = f"{names.get(p.path, p.path)} {p.threads}x{p.vpt}"
+    if p.cluster > 1:
+        s += f" c{p.cluster}"
+    if p.stages:
+        s += f" s{p.stages}"
+    return s + f" g{p.grid} w{p.w_spec}"
+
+
+def steady_state_us(fn, dev, stream, n=20):
+    """Per-call time of fn in a CUDA graph of n back-to-back calls, fastest of
+    5 replays: the sustained rate, where each call also pays the write-backs
+    the previous one left in L2."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(stream)
+    with torch.cuda.stream(s):
+        fn()  # plan made outside the capture
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(n):
+                fn()
+    stream.wait_stream(s)
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        b.synchronize()
+        t = a.elapsed_time(b) * 1e3 / n
+        best = t if best is None else min(best, t)
+    del g
+    return best
+
+
 def e2e_leg(ws, w, inp, pats, flush, dev, K, world):
-    """The same step on host (page-locked) buffers, inputs and outputs in
-    host memory, all data movement inside the timed events: zero-copy (the
-    kernels read and write the host buffers over NVLink-C2C; the headline
-    e2e) and staged (arf_run_host: copies in, kernels, copies out)."""
-    zc = _e2e(ws, w, inp, pats, flush, dev, K, world, zero_copy=True)
+    """The same step on page-locked host buffers, all data movement inside
+    the timed events. Headline: arf_run_host (copies of the step's inputs in,
+    the kernels, copies of its outputs back). Beside it, zero-copy: arf_run on
+    the host buffers themselves, the kernels reading and writing host memory
+    over NVLink-C2C."""
     st = _e2e(ws, w, inp, pats, flush, dev, K, world, zero_copy=False)
-    zc["staged"] = {k: st[k] for k in ("value", "ms_per_step", "api")}
-    return zc
+    zc = _e2e(ws, w, inp, pats, flush, dev, K, world, zero_copy=True)
+    st["zero_copy"] = {k: zc[k] for k in ("value", "ms_per_step", "api")}
+    return st
 
 
 def _e2e(ws, w, inp, pats, flush, dev, K, world, zero_copy):
@@ -382,9 +449,8 @@ def _e2e(ws, w, inp, pats, flush, dev, K, world, zero_copy):
     plane = w.M * w.H * 2
     h2d = sum((w.W * plane) + ((plane + w.H * 2) if p == "rmsnorm" else 0) for p in pats)
     d2h = sum(plane * (2 if p == "rmsnorm" else 1) for p in pats)
-    api = ("arf_run on page-locked host buffers (zero-copy: the kernels read the inputs from and write the "
-           "outputs to host memory over NVLink-C2C, inside the events)" if zero_copy else
-           "arf_run_host (page-locked host buffers; H2D copies + kernels + D2H copies inside the events)")
+    api = ("arf_run on pinned host buffers, no copies" if zero_copy else
+           "arf_run_host: H2D copies, kernels, D2H copies")
     return {"value": round(units / slowest / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": round(statistics.mean(times) * 1e3, 4),
             "api": api}
@@ -434,9 +500,7 @@ def roofline_context(ws, dev, flush, w, pattern, call_ms):
     call_us = statistics.mean(call_ms) * 1e3
     return {"pattern": pattern, "call_us": round(call_us, 3), "copy_same_bytes_us": round(copy_us, 3),
             "read_only_pass_same_reads_us": round(read_us, 3),
-            "call_over_read_only": round(call_us / read_us, 3),
-            "note": "the call's time against a device copy of its bytes and a read-only pass over its reads, "
-                    "all cold (L2 flushed) and event-timed"}
+            "call_over_read_only": round(call_us / read_us, 3)}
 
 
 def sweep(ws, dev, flush, peak):
