@@ -100,6 +100,7 @@ _SIGNATURES = {
     "arf_read_pass": (_c.c_int, [_vp, _vp, _i64, _vp]),
     "arf_run_host_static": (_c.c_int, [_vp, _c.c_int, _c.c_int, _c.POINTER(_vp), _vp, _vp, _c.c_float, _vp, _vp,
                                        _i64, _i64, _c.c_int, _vp]),
+    "arf_static_staging_bytes": (_c.c_size_t, []),
 }
 
 _lib = None
@@ -236,3 +237,7 @@ def arf_run_host_static(ws, pattern, W, partials_host, residual_host, gamma_host
     arr = (ctypes.c_void_p * W)(*partials_host)
     return load().arf_run_host_static(ws, pattern, W, arr, residual_host, gamma_host, eps, out_host,
                                       residual_out_host, M, H, dtype, stream)
+
+
+def arf_static_staging_bytes() -> int:
+    return load().arf_static_staging_bytes()

@@ -23,6 +23,11 @@ struct arf_workspace {
     std::map<std::tuple<int, int, int64_t, int64_t, int>, arf_plan_t> plans;
     std::atomic<int> last_err{0};
     unsigned int* wait_timeouts = nullptr;  // device counter of the bulk kernel's given-up waits
+    // Device address of the staging array of arf_run_host_static on this
+    // workspace's device, looked up at creation (arf_static.cu), or the
+    // error the lookup returned.
+    void* static_staging = nullptr;
+    cudaError_t static_staging_err = cudaErrorInvalidValue;
 };
 
 namespace {
@@ -193,6 +198,22 @@ extern "C" arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out
             (void)cudaGetLastError();
         }
     }
+    {
+        // The built-in staging array of arf_run_host_static: its address on
+        // this device, with the device current. Under lazy module loading this
+        // lookup is what loads the array, so the array is taken here, at
+        // set-up, and not inside a later call. A failure only disables that
+        // entry point (it then returns ARF_ERR_CUDA with this error).
+        void* addr = nullptr;
+        const cudaError_t se = arf::static_staging_address(&addr);
+        if (se == cudaSuccess) {
+            ws->static_staging = addr;
+            ws->static_staging_err = cudaSuccess;
+        } else {
+            ws->static_staging_err = se;
+            (void)cudaGetLastError();
+        }
+    }
     const char* lg = std::getenv("ARF_LOG");
     ws->log = lg && lg[0] == '1';
     if (ws->log)
@@ -238,6 +259,12 @@ extern "C" arf_status_t arf_workspace_caps(arf_workspace_t ws, arf_device_caps_t
 }
 
 extern "C" int arf_last_cuda_error(arf_workspace_t ws) { return ws ? ws->last_err.load() : 0; }
+
+cudaError_t arf::workspace_static_staging(arf_workspace_t ws, void** out) {
+    if (!ws->static_staging) return ws->static_staging_err;
+    *out = ws->static_staging;
+    return cudaSuccess;
+}
 
 // ---------------------------------------------------------------------------
 // capability and planning
@@ -473,7 +500,8 @@ cudaError_t max_active_blocks(arf_dtype_t dt, const arf_plan_t& pl, int64_t H, i
 // The planner's plan, with the cluster size lowered until the cluster kernel
 // instance can actually be made resident on this device. During stream
 // capture no occupancy query is made: the plan then rests on the cluster
-// limit probed at workspace creation.
+// limit probed at workspace creation, and it is not cached, so the next call
+// outside a capture makes the checked plan for the same key.
 arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64_t M, int64_t H,
                          arf_dtype_t dtype, arf_plan_t* out, bool capturing = false) {
     const auto key = std::make_tuple((int)pattern, W, M, H, (int)dtype);
@@ -536,8 +564,10 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
         std::fprintf(stderr, "[arf] plan %s W=%d M=%lld H=%lld %s: path=%s threads=%d vpt=%d cluster=%d grid=%d w_spec=%d stages=%d\n",
                      pattern_name(pattern), W, (long long)M, (long long)H, dtype == ARF_BF16 ? "bf16" : "fp16",
                      path_name(pl.path), pl.threads, pl.vpt, pl.cluster, pl.grid, pl.w_spec, pl.stages);
-    std::lock_guard<std::mutex> lk(ws->mu);
-    ws->plans[key] = pl;
+    if (!capturing) {
+        std::lock_guard<std::mutex> lk(ws->mu);
+        ws->plans[key] = pl;
+    }
     *out = pl;
     return ARF_OK;
 }

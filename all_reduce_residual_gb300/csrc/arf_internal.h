@@ -161,6 +161,12 @@ cudaError_t rms_max_active_blocks_fp16(const arf_plan_t& plan, int C, int W, int
 // Record a CUDA error as the workspace's last one (arf_last_cuda_error).
 void note_cuda_error(arf_workspace_t ws, cudaError_t e);
 
+// The staging array of arf_run_host_static (arf_static.cu): its device
+// address on the current device (cudaGetSymbolAddress), and the address a
+// workspace looked up at creation (or the error that lookup returned).
+cudaError_t static_staging_address(void** out);
+cudaError_t workspace_static_staging(arf_workspace_t ws, void** out);
+
 // The read-only measurement pass (arf_measure.cu): `grid` CTAs of 512 threads.
 cudaError_t launch_read_pass(const void* buf, int64_t bytes, int grid, unsigned int* sink, cudaStream_t s);
 

@@ -10,13 +10,15 @@
 // a caller cannot provide the device staging buffer that arf_run_host needs.
 //
 // Here that staging buffer is a file-scope device array compiled into the
-// library, ARF_STATIC_STAGING_BYTES bytes, which every GPU that loads the
-// library keeps until the process exits. Host code cannot use the array's
-// name as a device address (on the host it is only a stand-in symbol), so the
-// address is obtained with cudaGetSymbolAddress once per device, with that
-// device current, on the first call made on that device.
-#include <mutex>
-
+// library, ARF_STATIC_STAGING_BYTES bytes. Host code cannot use the array's
+// name as a device address (on the host it is only a stand-in symbol), so
+// arf_workspace_create looks the address up with cudaGetSymbolAddress, with
+// the workspace's device current, and the workspace keeps it. Under CUDA's
+// lazy module loading (the default) that lookup is also what loads the array
+// onto the device, so the array is taken when the first workspace on a device
+// is created, never inside a call of this entry point; it stays until the
+// process exits. A workspace lives in one CUDA context: after a device reset
+// it must be destroyed and created again, which looks the address up anew.
 #include "arf.h"
 #include "arf_internal.h"
 
@@ -24,26 +26,15 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_staging[ARF_STATIC_STAGING_BYTES];
 
-constexpr int kMaxDevices = 64;
-
-std::mutex g_setup_mu;
-void* g_staging_addr[kMaxDevices] = {};
-
-// Device address of g_static_staging on the current device `device`,
-// looked up once per device.
-cudaError_t staging_address(int device, void** out) {
-    std::lock_guard<std::mutex> lk(g_setup_mu);
-    if (!g_staging_addr[device]) {
-        void* p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_static_staging);
-        if (e != cudaSuccess) return e;
-        g_staging_addr[device] = p;
-    }
-    *out = g_staging_addr[device];
-    return cudaSuccess;
-}
-
 }  // namespace
+
+namespace arf {
+
+cudaError_t static_staging_address(void** out) { return cudaGetSymbolAddress(out, g_static_staging); }
+
+}  // namespace arf
+
+extern "C" size_t arf_static_staging_bytes(void) { return (size_t)ARF_STATIC_STAGING_BYTES; }
 
 extern "C" arf_status_t arf_run_host_static(arf_workspace_t ws, arf_pattern_t pattern, int W,
                                             const void* const* partials_host, const void* residual_host,
@@ -56,16 +47,15 @@ extern "C" arf_status_t arf_run_host_static(arf_workspace_t ws, arf_pattern_t pa
     if (M == 0) return ARF_OK;
     if (arf_host_staging_bytes(pattern, W, M, H, dtype) > (size_t)ARF_STATIC_STAGING_BYTES)
         return ARF_ERR_UNSUPPORTED;  // larger than the built-in staging array
-    int device = -1;
-    cudaError_t e = cudaGetDevice(&device);
-    if (e == cudaSuccess && (device < 0 || device >= kMaxDevices)) e = cudaErrorInvalidDevice;
+    // the address the workspace looked up on its device at creation
     void* staging = nullptr;
-    if (e == cudaSuccess) e = staging_address(device, &staging);
+    const cudaError_t e = arf::workspace_static_staging(ws, &staging);
     if (e != cudaSuccess) {
         arf::note_cuda_error(ws, e);
         return ARF_ERR_CUDA;
     }
-    // The rest is arf_run_host on the built-in array: device checks, copies
+    // The rest is arf_run_host on the built-in array: device checks (the
+    // current device must be the workspace's, whose array this is), copies
     // in, the kernel, copies out. Every region the kernels read is written
     // earlier in the same call, so nothing in the array has to start at zero.
     return arf_run_host(ws, pattern, W, partials_host, residual_host, gamma_host, eps, out_host,

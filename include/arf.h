@@ -306,10 +306,13 @@ typedef struct arf_run_opts {
     int64_t wait_limit_cycles; /* bulk path: SM cycles a wait on a ring slot
                                   may take before the CTA gives up (0 = the
                                   default, 2^31, about a second) */
-    int hold_first_copy;     /* bulk path, for testing the bounded waits only:
-                                1 = every CTA leaves its first ring slot
-                                unfilled, so its first wait runs out; the call
-                                then produces no complete output */
+    int hold_first_copy;     /* TESTING ONLY; leave 0 in production code.
+                                Bulk path: 1 = every CTA leaves its first ring
+                                slot unfilled, so its first wait runs out (see
+                                arf_workspace_wait_timeouts); the call then
+                                produces NO complete output. It exists so that
+                                a test can make a bounded wait give up without
+                                faulting anything. */
 } arf_run_opts_t;
 
 /* arf_run with per-call options (NULL opts = arf_run). Same semantics,
@@ -354,6 +357,10 @@ arf_status_t arf_run_host(arf_workspace_t ws, arf_pattern_t pattern, int W,
 /* Size of the staging array built into the library for arf_run_host_static. */
 #define ARF_STATIC_STAGING_BYTES (16u << 20) /* 16 MiB */
 
+/* ARF_STATIC_STAGING_BYTES as the built library has it (for bindings that do
+ * not read this header). No counterpart on the source pages. */
+size_t arf_static_staging_bytes(void);
+
 /* arf_run_host for callers that cannot allocate device memory. There is no
  * counterpart on the source pages: it exists for callers such as a plugin
  * inside a framework or serving engine whose allocator owns the device
@@ -361,19 +368,28 @@ arf_status_t arf_run_host(arf_workspace_t ws, arf_pattern_t pattern, int W,
  * implicit synchronisation, neither of which can hand arf_run_host a staging
  * buffer. It allocates nothing (no cudaMalloc, no cudaFree, no allocating
  * library call): the staging lives in a file-scope device array of
- * ARF_STATIC_STAGING_BYTES bytes compiled into the library, which every GPU
- * that loads the library holds until the process exits.
+ * ARF_STATIC_STAGING_BYTES bytes compiled into the library.
+ *
+ * When the array is taken: arf_workspace_create looks up its device address
+ * (cudaGetSymbolAddress, with the workspace's device current) and keeps it in
+ * the workspace. Under CUDA's lazy module loading (the default since CUDA
+ * 12.2) that lookup loads the array, so its 16 MiB are taken on a device when
+ * the first workspace there is created; with eager loading, when the library
+ * is loaded. Either way never inside a call of this entry point, and the
+ * array stays until the process exits. A workspace belongs to one CUDA
+ * context: after cudaDeviceReset destroy it and create a new one. If the
+ * lookup failed (for example the device had no memory left for the array)
+ * this entry point returns ARF_ERR_CUDA with that error in
+ * arf_last_cuda_error; the workspace's other entry points are unaffected.
  *
  * Arguments, results and errors are those of arf_run_host without the staging
- * arguments; sizes whose staging (arf_host_staging_bytes) exceeds
- * ARF_STATIC_STAGING_BYTES are rejected with ARF_ERR_UNSUPPORTED before
- * anything is enqueued. The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress, with that device current); make that
- * first call before any stream capture. Every call on a device shares the one
- * array, which keeps the last call's contents (no call relies on it starting
- * at zero: each call writes every byte it reads). Calls whose GPU work can
- * overlap (other streams, other threads) race on the array: serialise them,
- * for example on one stream. */
+ * arguments; the current device must be the workspace's. Sizes whose staging
+ * (arf_host_staging_bytes) exceeds ARF_STATIC_STAGING_BYTES are rejected with
+ * ARF_ERR_UNSUPPORTED before anything is enqueued. Every call on a device
+ * shares the one array, which keeps the last call's contents (no call relies
+ * on it starting at zero: each call writes every byte it reads). Calls whose
+ * GPU work can overlap (other streams, other threads, other workspaces on the
+ * same device) race on the array: serialise them, for example on one stream. */
 arf_status_t arf_run_host_static(arf_workspace_t ws, arf_pattern_t pattern, int W,
                                  const void* const* partials_host,
                                  const void* residual_host, const void* gamma_host, float eps,

@@ -76,6 +76,13 @@ def test_binding_constants_match_the_header():
     assert not missing, missing
 
 
+def test_static_staging_size_is_the_headers():
+    """The library reports the staging size arf.h declares, and the binding's
+    copy of the constant agrees with both."""
+    assert arf.arf_static_staging_bytes() == header_constants()["ARF_STATIC_STAGING_BYTES"]
+    assert arf.arf_static_staging_bytes() == _binding.ARF_STATIC_STAGING_BYTES
+
+
 def test_read_pass_argument_errors():
     """arf_read_pass checks its arguments before touching a device."""
     assert arf.arf_read_pass(None, 256, 1024, None) == arf.ARF_ERR_INVALID_ARG
