@@ -16,8 +16,9 @@
 //
 // Waits are bounded: a thread that has not seen its slot fill within
 // p.spin_limit SM cycles reports it, the whole CTA stops at the next block
-// barrier, thread 0 waits (bounded again) for the copies it issued and has
-// not seen land, counts the event in *p.status, and the CTA returns.
+// barrier, thread 0 waits (bounded again, by at least the default limit) for
+// the copies it issued and has not seen land, counts the event in *p.status,
+// and the CTA returns.
 #pragma once
 
 #include "arf_kernels.cuh"
@@ -166,15 +167,19 @@ __global__ void __launch_bounds__(kMaxThreads) rms_bulk_kernel(RmsParams p) {
         }
         if (failed) break;
         if constexpr (RMS) {
-            const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
+            const float inv = rsqrtf(cta_sum_squares(ss, s_warp, it) / (float)p.H + p.eps);
             for (int c = tid; c < C; c += B) normalise_chunk<T>(xrow[c], ld_keep(p.gamma + c), inv, p.out + ob + c);
         }
     }
     if (failed && tid == 0) {
-        // leave with no copy in flight into this CTA's shared memory
+        // Leave with no copy in flight into this CTA's shared memory. The
+        // drain waits at least the default limit, however short the caller's
+        // limit was: a copy that has not landed by then is lost, and this CTA
+        // may exit with it still in flight.
+        const long long drain = limit > kBulkSpinLimit ? limit : kBulkSpinLimit;
         for (int64_t j = consumed; j < issued; ++j) {
             if (p.hold_first && j == 0) continue;  // never issued
-            (void)mbar_wait_bounded(bar0 + 8u * (uint32_t)(j % S), (uint32_t)((j / S) & 1), limit);
+            (void)mbar_wait_bounded(bar0 + 8u * (uint32_t)(j % S), (uint32_t)((j / S) & 1), drain);
         }
         atomicAdd(p.status, 1u);
     }

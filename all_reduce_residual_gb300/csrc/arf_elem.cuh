@@ -255,7 +255,7 @@ __device__ __forceinline__ void rms_flat_row(const ElemParams& p, const uint4* c
         for (int q = 0; q < K; ++q)
             if (ok[q]) (void)residual_chunk<T>(acc[q], rv[q], ro16 + cro + j0 + q * B, ss);
     }
-    const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
+    const float inv = rsqrtf(cta_sum_squares(ss, s_warp, it) / (float)p.H + p.eps);
     if (k >= 0) {
         const float x = widen1<T>(p.residual_out[oro + k]);
         const float g = widen1<T>(p.gamma[k]);
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) rms_elem_kernel(ElemParams p) 
             const float x = widen1<T>(xs);
             ss = fmaf(x, x, ss);
         }
-        const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
+        const float inv = rsqrtf(cta_sum_squares(ss, s_warp, it) / (float)p.H + p.eps);
         for (int64_t e = threadIdx.x; e < p.H; e += blockDim.x) {
             const float x = widen1<T>(p.residual_out[row * p.ldro + e]);
             const float g = widen1<T>(p.gamma[e]);

@@ -395,24 +395,60 @@ __device__ __forceinline__ void issue_row(uint4 (&L)[VPT][WS + 1], const uint4* 
     }
 }
 
-// Row statistic: butterfly in the warp, warps in index order, then (cluster)
-// CTAs in rank order; every thread of every CTA of the cluster ends with the
-// same value. Shared slots alternate with the row parity `it`.
-__device__ __forceinline__ float row_sum_squares(float ss, float (*s_warp)[kMaxThreads / 32], float* s_cta,
-                                                 int cs, int it) {
+// Largest cluster the row-split kernels are launched with.
+constexpr int kMaxCluster = 16;
+
+// Cluster barrier halves (PTX barrier.cluster). The kernels arrive once at
+// the start (relaxed: it only tells the peers this CTA is running) and wait
+// before their first access to a peer's shared memory.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// The CTA's part of a row statistic: butterfly in the warp, then the warps'
+// sums in warp-index order (unrolled and predicated, so the shared-memory
+// reads issue together; the additions keep their order). Every thread ends
+// with the same value. Shared slots alternate with the row parity `it`.
+__device__ __forceinline__ float cta_sum_squares(float ss, float (*s_warp)[kMaxThreads / 32], int it) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) s_warp[it & 1][warp] = ss;
     __syncthreads();
     float tot = 0.0f;
-    for (int w = 0; w < nwarps; ++w) tot += s_warp[it & 1][w];
+#pragma unroll
+    for (int w = 0; w < kMaxThreads / 32; ++w)
+        if (w < nwarps) tot += s_warp[it & 1][w];
+    return tot;
+}
+
+// Row statistic over a cluster of cs CTAs; this CTA is rank q. Each CTA
+// pushes its part into slot q of every CTA's s_cta (itself included: threads
+// 0..cs-1 store one value each through distributed shared memory), one
+// cluster barrier (release / acquire) makes the stores visible, and every
+// CTA adds its own slots in CTA-rank order. Nobody reads a peer's shared
+// memory, so a CTA may exit as soon as it is done. Slots alternate with the
+// row parity: a CTA writes parity it & 1 again only after the next row's
+// barrier, which every peer reaches after reading this row's slots.
+// *wait_pending: this CTA still has to wait on its start arrival before the
+// first store into a peer.
+__device__ __forceinline__ float row_sum_squares(float ss, float (*s_warp)[kMaxThreads / 32],
+                                                 float (*s_cta)[kMaxCluster], int cs, int q, int it,
+                                                 bool* wait_pending) {
+    float tot = cta_sum_squares(ss, s_warp, it);
     if (cs > 1) {
+        if (*wait_pending) {
+            cluster_wait();  // every peer is running
+            *wait_pending = false;
+        }
         cg::cluster_group cluster = cg::this_cluster();
-        if (threadIdx.x == 0) s_cta[it & 1] = tot;
+        if ((int)threadIdx.x < cs) *cluster.map_shared_rank(&s_cta[it & 1][q], (int)threadIdx.x) = tot;
         cluster.sync();
         tot = 0.0f;
-        for (int r = 0; r < cs; ++r) tot += *cluster.map_shared_rank(&s_cta[it & 1], r);
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+            if (r < cs) tot += s_cta[it & 1][r];
     }
     return tot;
 }
@@ -448,7 +484,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
     static_assert(!ONE_ROW || Shape::kPrefetch, "the one-row form is the prefetching form without its row loop");
     __shared__ const uint4* s_ptr[ARF_MAX_W];
     __shared__ float s_warp[2][kMaxThreads / 32];  // per-warp partial sums, by row parity
-    __shared__ float s_cta[2];                     // this CTA's partial, read by its peers
+    __shared__ float s_cta[2][kMaxCluster];        // the cluster's CTA partials, by row parity
 
     prologue(s_ptr, p.lc, p.W);
 
@@ -468,6 +504,8 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
         }
     }
     __syncthreads();
+    bool wait_pending = cs > 1;
+    if (cs > 1) cluster_arrive_relaxed();
 
     if constexpr (ONE_ROW) {
         // Every cluster owns at most one row (grid >= rows): the same work as
@@ -492,7 +530,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
                     xs[k] = residual_chunk<T>(acc, L[k][WS], p.residual_out + rob + c, ss);
                 }
             }
-            const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, 0) / (float)p.H + p.eps);
+            const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, q, 0, &wait_pending) / (float)p.H + p.eps);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int c = c0 + warp_run_chunk<VPT>(k);
@@ -526,7 +564,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
             }
             const int64_t next = row + nclusters;
             if (next < p.M) issue_row<WS, VPT>(L, s_ptr, p.residual, next * p.ly.ldp, next * p.ly.ldr, c0, c1);
-            const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, it) / (float)p.H + p.eps);
+            const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, q, it, &wait_pending) / (float)p.H + p.eps);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int c = c0 + warp_run_chunk<VPT>(k);
@@ -554,7 +592,7 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
                     xs[k] = residual_chunk<T>(acc, rv, p.residual_out + rob + c, ss);
                 }
             }
-            const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, it) / (float)p.H + p.eps);
+            const float inv = rsqrtf(row_sum_squares(ss, s_warp, s_cta, cs, q, it, &wait_pending) / (float)p.H + p.eps);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int c = c0 + warp_run_chunk<VPT>(k);
@@ -567,8 +605,9 @@ __global__ void __launch_bounds__(kMaxThreads) rms_kernel(RmsParams p) {
             }
         }
     }
-    // A peer may still be reading this CTA's s_cta: leave together.
-    if (cs > 1) cg::this_cluster().sync();
+    // A cluster without rows never waited on its start arrival: complete
+    // that barrier phase before leaving.
+    if (wait_pending) cluster_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -674,7 +713,7 @@ __global__ void __launch_bounds__(kAsyncThreads, 1) rms_async_kernel(RmsParams p
             if (++slot_i == S) slot_i = 0;
         }
         // the row is complete: normalise it
-        const float inv = rsqrtf(row_sum_squares(ss, s_warp, nullptr, 1, it) / (float)p.H + p.eps);
+        const float inv = rsqrtf(cta_sum_squares(ss, s_warp, it) / (float)p.H + p.eps);
         for (int b = 0; b < nb; ++b) {
             const int c = b * kAsyncThreads + tid;
             if (c < C) normalise_chunk<T>(xrow[c], ld_keep(p.gamma + c), inv, p.out + ob + c);
