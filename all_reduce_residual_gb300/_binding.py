@@ -83,6 +83,8 @@ _SIGNATURES = {
     "arf_supports": (_c.c_int, [_vp, _c.c_int, _c.c_int, _i64, _i64, _c.c_int]),
     "arf_plan_for_caps": (_c.c_int, [_c.POINTER(DeviceCaps), _c.c_int, _c.c_int, _i64, _i64, _c.c_int,
                                      _c.POINTER(Plan)]),
+    "arf_plan_rules": (_c.c_int, [_c.POINTER(DeviceCaps), _c.c_int, _c.c_int, _i64, _i64, _c.c_int,
+                                  _c.POINTER(Plan)]),
     "arf_workspace_plan": (_c.c_int, [_vp, _c.c_int, _c.c_int, _i64, _i64, _c.c_int, _c.POINTER(Plan)]),
     "arf_plan_check": (_c.c_int, [_c.POINTER(DeviceCaps), _c.POINTER(Plan), _c.c_int, _c.c_int, _i64, _i64,
                                   _c.c_int]),
@@ -174,6 +176,10 @@ def arf_supports(ws, pattern: int, W: int, M: int, H: int, dtype: int) -> int:
 
 def arf_plan_for_caps(caps: DeviceCaps, pattern: int, W: int, M: int, H: int, dtype: int, plan_out: Plan) -> int:
     return load().arf_plan_for_caps(ctypes.byref(caps), pattern, W, M, H, dtype, ctypes.byref(plan_out))
+
+
+def arf_plan_rules(caps: DeviceCaps, pattern: int, W: int, M: int, H: int, dtype: int, plan_out: Plan) -> int:
+    return load().arf_plan_rules(ctypes.byref(caps), pattern, W, M, H, dtype, ctypes.byref(plan_out))
 
 
 def arf_workspace_plan(ws, pattern: int, W: int, M: int, H: int, dtype: int, plan_out: Plan) -> int:

@@ -323,8 +323,100 @@ extern "C" arf_status_t arf_supports(arf_workspace_t ws, arf_pattern_t pattern, 
     return ARF_OK;
 }
 
+namespace {
+
+// The measured plan table (arf_plan_table.inc, written by plan_table.py
+// from cold timings on one device): for a device with exactly these
+// capabilities, a pattern, dtype, W, H and a range of M, a plan shape and a
+// rule for its grid. Threads per block, cluster size and grid come from the
+// device (flashinfer PR #1507 "update allreduce to match trtllm",
+// Highlights), chosen per shape from measurements (vLLM PR #53318 "Tune
+// FlashInfer all-reduce selection on SM103", Scope).
+struct PlanTableRow {
+    int num_sms, max_cluster, max_threads_per_sm, max_smem_per_block;
+    int pattern, dtype, W;
+    int64_t H, m_lo, m_hi;
+    int path, threads, vpt, cluster, w_spec, stages;
+    int grid_rule;  // PlanGridRule
+    int per_sm;     // CTAs per SM (resident and tiles rules)
+};
+
+enum PlanGridRule {
+    kGridRows = 0,      // M * cluster: one CTA (or cluster) per row
+    kGridResident = 1,  // min(M, per_sm * SMs / cluster) * cluster
+    kGridChunks = 2,    // ceil(M * H / 8 / (threads * vpt)): flat kAllReduce
+    kGridTiles = 3,     // min(ceil(H / threads) * M, per_sm * SMs): elementwise kAllReduce
+};
+
+const PlanTableRow kPlanTable[] = {
+#include "arf_plan_table.inc"
+    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0},  // end
+};
+
+// The table's plan for this call, if a row covers it and its plan passes
+// arf_plan_check.
+bool table_plan(const arf_device_caps_t& caps, arf_pattern_t pattern, int W, int64_t M, int64_t H,
+                arf_dtype_t dtype, arf_plan_t* out) {
+    for (const PlanTableRow& r : kPlanTable) {
+        if (r.num_sms == 0) break;
+        if (r.num_sms != caps.num_sms || r.max_cluster != caps.max_cluster ||
+            r.max_threads_per_sm != caps.max_threads_per_sm || r.max_smem_per_block != caps.max_smem_per_block)
+            continue;
+        if (r.pattern != (int)pattern || r.dtype != (int)dtype || r.W != W || r.H != H || M < r.m_lo || M > r.m_hi)
+            continue;
+        arf_plan_t pl = {};
+        pl.path = r.path;
+        pl.threads = r.threads;
+        pl.vpt = r.vpt;
+        pl.cluster = r.cluster;
+        pl.w_spec = r.w_spec;
+        pl.stages = r.stages;
+        const int64_t cs = r.cluster > 0 ? r.cluster : 1;
+        int64_t g;
+        switch (r.grid_rule) {
+            case kGridRows: g = M * cs; break;
+            case kGridResident: {
+                int64_t n = (int64_t)r.per_sm * caps.num_sms / cs;
+                if (n < 1) n = 1;
+                g = (M < n ? M : n) * cs;
+                break;
+            }
+            case kGridChunks: g = ceil_div(M * H / 8, (int64_t)r.threads * r.vpt); break;
+            case kGridTiles: {
+                g = ceil_div(H, r.threads) * M;
+                const int64_t cap = (int64_t)r.per_sm * caps.num_sms;
+                if (g > cap) g = cap;
+                break;
+            }
+            default: return false;
+        }
+        const int64_t gmax = (int64_t)(INT32_MAX / cs) * cs;
+        if (g < 1) g = 1;
+        if (g > gmax) g = gmax;
+        pl.grid = (int)g;
+        if (arf_plan_check(&caps, &pl, pattern, W, M, H, dtype) != ARF_OK) return false;
+        *out = pl;
+        return true;
+    }
+    return false;
+}
+
+}  // namespace
+
 extern "C" arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pattern_t pattern, int W,
                                           int64_t M, int64_t H, arf_dtype_t dtype, arf_plan_t* plan_out) {
+    if (!caps || !plan_out) return ARF_ERR_INVALID_ARG;
+    arf_status_t st = arf_supports(nullptr, pattern, W, M, H, dtype);
+    if (st != ARF_OK) return st;
+    if (caps->num_sms < 1 || caps->max_threads_per_sm < 32 || caps->max_cluster < 1) return ARF_ERR_INVALID_ARG;
+    // A measured plan for this device and shape, where the table has one;
+    // else the closed-form rules.
+    if (table_plan(*caps, pattern, W, M, H, dtype, plan_out)) return ARF_OK;
+    return arf_plan_rules(caps, pattern, W, M, H, dtype, plan_out);
+}
+
+extern "C" arf_status_t arf_plan_rules(const arf_device_caps_t* caps, arf_pattern_t pattern, int W, int64_t M,
+                                       int64_t H, arf_dtype_t dtype, arf_plan_t* plan_out) {
     if (!caps || !plan_out) return ARF_ERR_INVALID_ARG;
     arf_status_t st = arf_supports(nullptr, pattern, W, M, H, dtype);
     if (st != ARF_OK) return st;
@@ -516,7 +608,11 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
     arf_plan_t pl;
     arf_status_t st = arf_plan_for_caps(&ws->caps, pattern, W, M, H, dtype, &pl);
     if (st != ARF_OK) return st;
-    if (!capturing && pl.path == ARF_PATH_ASYNC) {
+    // A plan from the measured table was timed as it stands on a device with
+    // these capabilities: it is used without the refinements below.
+    arf_plan_t tp;
+    const bool refine = !capturing && !table_plan(ws->caps, pattern, W, M, H, dtype, &tp);
+    if (refine && pl.path == ARF_PATH_ASYNC) {
         int b = 0;
         cudaError_t e = max_active_blocks(dtype, pl, H, W, &b);
         if (e != cudaSuccess || b < 1) {  // the ring does not fit: one CTA per row instead
@@ -524,7 +620,7 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
             pl = row_plan(ws->caps, pl.w_spec, M, H);
         }
     }
-    if (!capturing && pl.path == ARF_PATH_BULK) {
+    if (refine && pl.path == ARF_PATH_BULK) {
         int b = 0;
         cudaError_t e = max_active_blocks(dtype, pl, H, W, &b);
         if (e == cudaSuccess && b > 0) {
@@ -535,7 +631,7 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
             pl = row_plan(ws->caps, pl.w_spec, M, H);
         }
     }
-    while (!capturing && pl.path == ARF_PATH_CLUSTER) {
+    while (refine && pl.path == ARF_PATH_CLUSTER) {
         int n = 0;
         cudaError_t e = max_active_clusters(dtype, pl, &n);
         if (e == cudaSuccess && n > 0) {
@@ -550,7 +646,7 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
     // only smaller clusters) is refused rather than launched
     st = arf_plan_check(&ws->caps, &pl, pattern, W, M, H, dtype);
     if (st != ARF_OK) return st;
-    if (!capturing && pl.path == ARF_PATH_ROW && !one_row_grid_wanted(pl, W)) {
+    if (refine && pl.path == ARF_PATH_ROW && !one_row_grid_wanted(pl, W)) {
         int b = 0;
         cudaError_t e = max_active_blocks(dtype, pl, H, W, &b);
         if (e == cudaSuccess && b > 0) {
@@ -1112,10 +1208,9 @@ extern "C" arf_status_t arf_read_pass(arf_workspace_t ws, const void* buf, int64
     if (!ws || bytes < 0 || bytes % 16 != 0) return ARF_ERR_INVALID_ARG;
     if (bytes == 0) return ARF_OK;
     if (!buf || !aligned16(buf)) return ARF_ERR_INVALID_ARG;
-    // two CTAs of 512 threads per SM, grid-stride (measured the fastest
-    // shape for a plain read on GB300); the sink is a spare word of the
-    // workspace's device allocation, past the wait-timeout counter
-    cudaError_t e = arf::launch_read_pass(buf, bytes, 2 * ws->caps.num_sms, ws->wait_timeouts + 32,
+    // the sink is a spare word of the workspace's device allocation, past
+    // the wait-timeout counter
+    cudaError_t e = arf::launch_read_pass(buf, bytes, ws->caps.num_sms, ws->wait_timeouts + 32,
                                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(ws, e);
     return ARF_OK;

@@ -102,9 +102,11 @@ EXTRA_WORKLOADS = {
     "h32776": Workload("h32776", 11, 2, 1024, 32776, "bf16", 1.0, 1e-6, ("rmsnorm",)),
     "odd_h4098": Workload("odd_h4098", 12, 2, 4096, 4098, "bf16", 0.5, 1e-5, ("allreduce", "rmsnorm")),
 }
-# The kernel path the planner is expected to take for each extra shape.
+# The kernel path the planner takes for each extra shape on GB300 (from its
+# measured plan table; the closed-form rules send h32768 and w1_fp16 to the
+# bulk kernel instead).
 EXTRA_PATHS = {"w3_generic": "bulk", "w12_generic": "bulk", "tp4_80mib_fp16": "row, one CTA per row",
-               "h32768": "bulk", "w1_fp16": "bulk", "h32776": "bulk", "odd_h4098": "elem"}
+               "h32768": "row", "w1_fp16": "row, one CTA per row", "h32776": "bulk", "odd_h4098": "elem"}
 
 
 def custom(W: int, M: int, H: int, dtype: str = "bf16", sigma: float = 1.0,

@@ -182,10 +182,25 @@ arf_status_t arf_supports(arf_workspace_t ws, arf_pattern_t pattern, int W,
                           int64_t M, int64_t H, arf_dtype_t dtype);
 
 /* The plan the library picks for these sizes on a device with `caps`.
- * Pure function of its arguments. */
+ * Pure function of its arguments. Threads per block, cluster size and grid
+ * follow from the device (flashinfer PR #1507 "update allreduce to match
+ * trtllm", Highlights), chosen per shape (vLLM PR #53318 "Tune FlashInfer
+ * all-reduce selection on SM103", Scope): first from the library's measured
+ * plan table, whose rows hold the fastest plan timed cold (L2 flushed) for
+ * a device with exactly these capabilities, a pattern, dtype, W, H and a
+ * range of M; for shapes and devices the table does not cover, from the
+ * closed-form rules of arf_plan_rules. */
 arf_status_t arf_plan_for_caps(const arf_device_caps_t* caps, arf_pattern_t pattern,
                                int W, int64_t M, int64_t H, arf_dtype_t dtype,
                                arf_plan_t* plan_out);
+
+/* The closed-form planning rules alone, without the measured table: the plan
+ * arf_plan_for_caps returns where the table has no row. Same arguments,
+ * results and errors. No counterpart on the pages beyond the launch-
+ * configuration remark cited above. */
+arf_status_t arf_plan_rules(const arf_device_caps_t* caps, arf_pattern_t pattern,
+                            int W, int64_t M, int64_t H, arf_dtype_t dtype,
+                            arf_plan_t* plan_out);
 
 /* The plan arf_run would use on this workspace (memoised per shape). */
 arf_status_t arf_workspace_plan(arf_workspace_t ws, arf_pattern_t pattern, int W,

@@ -127,7 +127,7 @@ def test_planner_plans_are_legal(pattern, W, M, H):
     for caps in (GB300, arf.DeviceCaps(148, 8, 2048, 232448), arf.DeviceCaps(132, 1, 2048, 101376),
                  arf.DeviceCaps(1, 1, 1024, 49152)):
         p = arf.Plan()
-        assert arf.arf_plan_for_caps(caps, pattern, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+        assert arf.arf_plan_rules(caps, pattern, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
         assert arf.arf_plan_check(caps, p, pattern, W, M, H, arf.ARF_BF16) == arf.ARF_OK, p
         assert p.grid % p.cluster == 0 and p.threads % 32 == 0
         assert p.w_spec in (0, W)
@@ -186,18 +186,18 @@ def test_planner_plans_are_legal(pattern, W, M, H):
 def test_planner_uses_the_sm_count():
     """Few wide rows spread over several SMs; large M fills the device."""
     p = arf.Plan()
-    arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 1, 7168, arf.ARF_BF16, p)
+    arf.arf_plan_rules(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 1, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_CLUSTER and p.cluster == 8 and p.threads == 128
-    arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 128, 7168, arf.ARF_BF16, p)
+    arf.arf_plan_rules(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 128, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and (p.threads, p.vpt, p.grid) == (448, 2, 128)
-    arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 2048, 7168, arf.ARF_BF16, p)
+    arf.arf_plan_rules(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 2048, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and (p.threads, p.vpt) == (448, 2) and p.grid % 152 == 0
-    arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 4, 5851, 7168, arf.ARF_BF16, p)
+    arf.arf_plan_rules(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 4, 5851, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and p.vpt * (4 + 1) <= 18 and p.grid == 5851  # one CTA per row
-    arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7168, arf.ARF_BF16, p)
+    arf.arf_plan_rules(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 16, 585, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and (p.threads, p.vpt) == (448, 2)  # 896 chunks > 512 threads
     no_cluster = arf.DeviceCaps(152, 1, 2048, 232448)
-    arf.arf_plan_for_caps(no_cluster, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 1, 7168, arf.ARF_BF16, p)
+    arf.arf_plan_rules(no_cluster, arf.ARF_AR_RESIDUAL_RMSNORM, 8, 1, 7168, arf.ARF_BF16, p)
     assert p.path == arf.ARF_PATH_ROW and p.grid == 1
 
 
@@ -210,18 +210,18 @@ def test_long_rows_split_over_clusters(H, M):
     takes any H <= ARF_MAX_H."""
     p = arf.Plan()
     bulk = 2 * M >= 152 and (H // 8) * 16 + BULK_STATIC + 2 * 9 * 256 * 16 <= 232448
-    assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+    assert arf.arf_plan_rules(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
     if bulk:
         assert p.path == arf.ARF_PATH_BULK and p.threads <= 512
     else:
         assert p.path == arf.ARF_PATH_CLUSTER and p.threads <= 512
         assert p.threads * p.vpt * p.cluster >= H // 8
     assert arf.arf_plan_check(GB300, p, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16) == arf.ARF_OK
-    assert arf.arf_plan_for_caps(GB300, arf.ARF_ALLREDUCE, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+    assert arf.arf_plan_rules(GB300, arf.ARF_ALLREDUCE, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
     # a device with 4-CTA clusters holds rows up to 4 x 32768; longer rows
     # take the elementwise kernel
     small = arf.DeviceCaps(152, 4, 2048, 232448)
-    assert arf.arf_plan_for_caps(small, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+    assert arf.arf_plan_rules(small, arf.ARF_AR_RESIDUAL_RMSNORM, 8, M, H, arf.ARF_BF16, p) == arf.ARF_OK
     if H > 4 * 32768:
         assert p.path == arf.ARF_PATH_ELEM
     else:
@@ -235,7 +235,7 @@ def test_elementwise_rmsnorm_plan_shape():
     p = arf.Plan()
     for W, M, H in ((2, 4096, 4098), (4, 2048, 7170), (8, 608, 7175), (3, 128, 4097), (2, 455, 4098),
                     (2, 456, 4098), (8, 1063, 7175), (8, 1064, 7175), (3, 5000, 1001)):
-        assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+        assert arf.arf_plan_rules(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
         assert p.path == arf.ARF_PATH_ELEM
         if M >= 7 * 152 and H >= 1024:
             assert p.threads == 128 and p.grid == min(M, 8 * 152), (W, M, H, p)
@@ -253,7 +253,7 @@ def test_long_rows_take_the_bulk_ring_when_rows_are_many():
     for W, M, H in ((2, 16, 32776), (2, 76, 32776), (2, 2048, 32776), (8, 608, 32776), (4, 64, 65536),
                     (4, 152, 65536), (12, 300, 40000), (13, 300, 40000), (2, 500, 131072), (8, 500, 78976),
                     (8, 500, 78984), (8, 500, 106496), (2, 1024, 32776)):
-        assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+        assert arf.arf_plan_rules(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
         assert arf.arf_plan_check(GB300, p, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16) == arf.ARF_OK
         fits = (H // 8) * 16 + BULK_STATIC + 2 * (W + 1) * 256 * 16 <= 232448  # blocks of >= 256 chunks
         if 2 * M >= 152 and W <= 12 and fits:
@@ -271,15 +271,15 @@ def test_long_row_limits():
     assert S(None, arf.ARF_ALLREDUCE, 2, 1, 524296, arf.ARF_BF16) == arf.ARF_ERR_UNSUPPORTED
     no_cluster = arf.DeviceCaps(152, 1, 2048, 232448)
     p = arf.Plan()
-    assert arf.arf_plan_for_caps(no_cluster, arf.ARF_AR_RESIDUAL_RMSNORM, 2, 1, 32776, arf.ARF_BF16, p) == arf.ARF_OK
+    assert arf.arf_plan_rules(no_cluster, arf.ARF_AR_RESIDUAL_RMSNORM, 2, 1, 32776, arf.ARF_BF16, p) == arf.ARF_OK
     assert p.path == arf.ARF_PATH_ELEM and p.threads == 512
-    assert arf.arf_plan_for_caps(no_cluster, arf.ARF_ALLREDUCE, 2, 1, 524288, arf.ARF_BF16, p) == arf.ARF_OK
+    assert arf.arf_plan_rules(no_cluster, arf.ARF_ALLREDUCE, 2, 1, 524288, arf.ARF_BF16, p) == arf.ARF_OK
 
 
 def test_plan_check_rejects_bad_plans():
     good = arf.Plan()
     args = (arf.ARF_AR_RESIDUAL_RMSNORM, 8, 64, 7168, arf.ARF_BF16)
-    assert arf.arf_plan_for_caps(GB300, *args, good) == arf.ARF_OK
+    assert arf.arf_plan_rules(GB300, *args, good) == arf.ARF_OK
 
     def with_(**kw):
         p = arf.Plan(**good.as_dict())
@@ -400,7 +400,7 @@ def test_planner_bulk_choices():
     wide rows (cluster path) and wider rank counts keep their kernels."""
     def plan(W, M, H):
         p = arf.Plan()
-        assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
+        assert arf.arf_plan_rules(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_BF16, p) == arf.ARF_OK
         return p
 
     p = plan(3, 2000, 7168)  # rank count not compiled in: 2 x 4 x 8 KiB slots, 2 CTAs per SM
@@ -420,7 +420,7 @@ def test_planner_bulk_choices():
                                 (8, 1024, 7168, arf.ARF_PATH_ROW, None), (2, 128, 7168, arf.ARF_PATH_ROW, 128),
                                 (2, 8192, 4096, arf.ARF_PATH_ROW, None), (4, 304, 7168, arf.ARF_PATH_ROW, 304)):
         p = arf.Plan()
-        assert arf.arf_plan_for_caps(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_FP16, p) == arf.ARF_OK
+        assert arf.arf_plan_rules(GB300, arf.ARF_AR_RESIDUAL_RMSNORM, W, M, H, arf.ARF_FP16, p) == arf.ARF_OK
         assert p.path == path, (W, M, H)
         if grid is not None:
             assert p.grid == grid, (W, M, H, p)
@@ -436,7 +436,8 @@ def test_workload_tables_agree_with_the_planner():
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     import bench
     assert set(wl.EXTRA_PATHS) == set(wl.EXTRA_WORKLOADS)
-    want = {"bulk": arf.ARF_PATH_BULK, "elem": arf.ARF_PATH_ELEM, "row, one CTA per row": arf.ARF_PATH_ROW}
+    want = {"bulk": arf.ARF_PATH_BULK, "elem": arf.ARF_PATH_ELEM, "row, one CTA per row": arf.ARF_PATH_ROW,
+            "row": arf.ARF_PATH_ROW}
     for name, w in {**wl.WORKLOADS, **wl.EXTRA_WORKLOADS}.items():
         dt = arf.ARF_BF16 if w.dtype == "bf16" else arf.ARF_FP16
         for pat in w.patterns:
@@ -446,3 +447,5 @@ def test_workload_tables_agree_with_the_planner():
             assert p.path in table, (name, pat, p)
             if name in wl.EXTRA_PATHS:
                 assert p.path == want[wl.EXTRA_PATHS[name]], (name, pat, p)
+                if wl.EXTRA_PATHS[name] == "row, one CTA per row":
+                    assert p.grid == w.M, (name, pat, p)

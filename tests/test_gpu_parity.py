@@ -37,6 +37,8 @@ def test_workload_parity(ws, name, M, pattern):
             assert plan.path == arf.ARF_PATH_BULK, plan
         elif wl.EXTRA_PATHS[name] == "elem":
             assert plan.path == arf.ARF_PATH_ELEM, plan
+        elif wl.EXTRA_PATHS[name] == "row":
+            assert plan.path == arf.ARF_PATH_ROW, plan
         else:
             assert plan.path == arf.ARF_PATH_ROW and plan.grid == M, plan
     got = gpu_run(ws, pat, P, R, G, inp.workload.eps)
