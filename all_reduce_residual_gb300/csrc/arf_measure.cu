@@ -9,23 +9,39 @@
 
 namespace arf {
 
-// Every thread reads 16-byte vectors at a grid stride and folds them into a
+// Every thread reads four 16-byte vectors per trip (issued together) over
+// tiles of 4 x blockDim.x vectors at a grid stride, and folds them into a
 // register; one store, under a condition the data cannot be shown to avoid,
-// keeps the loads alive.
-__global__ void __launch_bounds__(512) read_pass_kernel(const uint4* a, int64_t n, unsigned int* sink) {
+// keeps the loads alive. Four CTAs of 256 threads per SM: on GB300 this
+// shape read fastest among those measured (136 MiB in 28.3 us and 2 GiB in
+// 311 us cold, against 30.8 and 347 us with one vector per trip and two
+// 512-thread CTAs per SM).
+constexpr int kReadUnroll = 4;
+constexpr int kReadThreads = 256;
+
+__global__ void __launch_bounds__(kReadThreads) read_pass_kernel(const uint4* a, int64_t n, unsigned int* sink) {
     unsigned int x = 0;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        uint4 v;
-        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                     : "l"(a + i));
-        x ^= v.x ^ v.y ^ v.z ^ v.w;
+    const int64_t tile = (int64_t)blockDim.x * kReadUnroll;
+    for (int64_t t0 = (int64_t)blockIdx.x * tile; t0 < n; t0 += (int64_t)gridDim.x * tile) {
+        uint4 v[kReadUnroll];
+#pragma unroll
+        for (int k = 0; k < kReadUnroll; ++k) {
+            const int64_t i = t0 + (int64_t)k * blockDim.x + threadIdx.x;
+            if (i < n)
+                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(v[k].x), "=r"(v[k].y), "=r"(v[k].z), "=r"(v[k].w)
+                             : "l"(a + i));
+            else
+                v[k] = make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < kReadUnroll; ++k) x ^= v[k].x ^ v[k].y ^ v[k].z ^ v[k].w;
     }
     if (x == 0x9e3779b9u) *sink = x;
 }
 
-cudaError_t launch_read_pass(const void* buf, int64_t bytes, int grid, unsigned int* sink, cudaStream_t s) {
-    read_pass_kernel<<<grid, 512, 0, s>>>(static_cast<const uint4*>(buf), bytes / 16, sink);
+cudaError_t launch_read_pass(const void* buf, int64_t bytes, int num_sms, unsigned int* sink, cudaStream_t s) {
+    read_pass_kernel<<<4 * num_sms, kReadThreads, 0, s>>>(static_cast<const uint4*>(buf), bytes / 16, sink);
     return cudaGetLastError();
 }
 
