@@ -5,8 +5,9 @@
 Runs on one GPU. For every (pattern, dtype, W, H) of the table's shape list
 and a ladder of row counts M, it times candidate launch plans cold, the way
 the benchmark times a call: the L2 is flushed clean before each call (a write
-of twice its size, then a read of another buffer of that size) and the call
-is timed with CUDA events on its stream. The fastest plan at each measured M
+of twice its size, then a read of another buffer of that size, then a spin of
+random length so that the call starts at a random phase of the event clock)
+and the call is timed with CUDA events on its stream. The fastest plan at each measured M
 is kept. Neighbouring row counts with the same winner merge into one range,
 and the ranges split at the geometric mean of the measured row counts. The
 result is written as C initialisers to ``csrc/arf_plan_table.inc``, which the
@@ -31,6 +32,7 @@ from __future__ import annotations
 import argparse
 import math
 import os
+import random
 import statistics
 import sys
 import time
@@ -109,9 +111,9 @@ def candidates(caps, pattern, W, H):
     def threads_for(chunks, vpt):
         return max(32, -(-(-(-chunks // vpt)) // 32) * 32)
 
-    # one CTA per row: the fewest chunks per thread that fit 512 threads, and twice that
+    # one CTA per row: the fewest chunks per thread that fit 512 threads, and two and four times that
     v0 = next((v for v in (1, 2, 4, 8) if threads_for(C, v) <= MAX_THREADS), None)
-    for vpt in ((v0, 2 * v0) if v0 and v0 < 8 else ((v0,) if v0 else ())):
+    for vpt in sorted({v for v in ((v0, 2 * v0, 4 * v0) if v0 else ()) if v <= 8}):
         t = threads_for(C, vpt)
         out.append((PATH_ROW, t, vpt, 1, ws, 0, GRID_ROWS, 0))
         for per in (1, 2, 3, 4):
@@ -160,9 +162,15 @@ def main():
     fw = torch.empty(nflush, dtype=torch.uint8, device=dev)
     fr = torch.zeros(nflush // 4, dtype=torch.int32, device=dev)
 
+    rng = random.Random(4321)
+
     def flush():
+        # then a spin of a random 0-4095 SM cycles: the timed call starts at a
+        # random phase of the event clock (which advances in steps of about
+        # 2 us), so that means of many cold timings are unbiased
         fw.zero_()
         torch.amax(fr)
+        torch.cuda._sleep(rng.randrange(4096))
 
     def time_cold(fn, n):
         ts = []

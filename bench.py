@@ -202,14 +202,24 @@ class L2Flush:
     """Leaves the L2 holding none of the benchmark's data: write `nbytes`
     (twice the L2), then read another `nbytes` so that the L2 ends up full
     of clean lines (no write-back pending when the timed kernels start).
-    zero_(dirty_only=True) skips the read: the plain write flush."""
+    zero_(dirty_only=True) skips the read: the plain write flush.
 
-    def __init__(self, nbytes, dev):
+    It ends with a spin of a random 0-4095 SM cycles (under 2 us, touching
+    no memory). The GPU's event clock advances in steps of about 2 us and
+    the flush takes a fixed time, so without it the timed call would start at
+    nearly the same phase of that clock every time and the mean of many
+    timings would carry up to a step of bias; with it the phase is random
+    and the mean is unbiased."""
+
+    def __init__(self, nbytes, dev, seed=12345):
+        import random
+
         import torch
 
         self.w = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.r = torch.zeros(nbytes // 4, dtype=torch.int32, device=dev)
         self.nbytes = nbytes
+        self.rng = random.Random(seed)
 
     def zero_(self, dirty_only=False):
         import torch
@@ -217,10 +227,11 @@ class L2Flush:
         self.w.zero_()
         if not dirty_only:
             self.sink = torch.amax(self.r)  # one read pass, no temporary
+        torch.cuda._sleep(self.rng.randrange(4096))
 
     def describe(self):
         mib = self.nbytes >> 20
-        return f"flush before each step: write {mib} MiB, read another {mib} MiB"
+        return f"flush before each step: write {mib} MiB, read another {mib} MiB, random 0-2 us spin"
 
 
 # ---------------------------------------------------------------------------
