@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--workload", default="tp4_80mib")
     ap.add_argument("--sweep-out", default=None,
                     help="also time every workload, pattern and K3 row count and write the table to this JSON file")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="accepted for older command lines; the sweep runs only with --sweep-out")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--m", type=int, default=None, help="override the workload's row count M (for profiling)")
