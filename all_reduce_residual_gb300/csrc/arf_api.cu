@@ -538,7 +538,12 @@ extern "C" arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_
         if (pl->cluster != 1 || pl->vpt != 1 || pl->stages != 0 || pl->w_spec != 0) return ARF_ERR_UNSUPPORTED;
         return ARF_OK;
     }
-    if (H % 8 != 0) return ARF_ERR_UNSUPPORTED;  // the 16-byte kernels need whole chunks
+    // The 16-byte kernels need whole chunks. kAllReduce is elementwise, so
+    // the flat kernel also takes H % 8 != 0 when M * H is a multiple of 8:
+    // contiguous tensors are then one range of whole chunks (the call checks
+    // the layout and takes the elementwise kernel otherwise).
+    const bool flat_range = pattern == ARF_ALLREDUCE && pl->path == ARF_PATH_FLAT && (M * H) % 8 == 0;
+    if (H % 8 != 0 && !flat_range) return ARF_ERR_UNSUPPORTED;
     if (pl->path == ARF_PATH_ASYNC) {
         if (pattern != ARF_AR_RESIDUAL_RMSNORM || pl->w_spec == 0 || pl->w_spec != W) return ARF_ERR_UNSUPPORTED;
         if (pl->threads != arf::kAsyncCtaThreads || pl->cluster != 1 || pl->vpt != 1) return ARF_ERR_UNSUPPORTED;
@@ -672,7 +677,9 @@ arf_status_t device_plan(arf_workspace_t ws, arf_pattern_t pattern, int W, int64
 struct Layout {
     int64_t ldp, ldr, ldo, ldro;
     bool f32p;
-    bool vec_ok;  // the 16-byte kernels can take it
+    bool vec_ok;    // the 16-byte kernels can take it
+    bool range_ok;  // kAllReduce: contiguous 16-bit tensors, M*H a multiple of 8 and out
+                    // 16-byte aligned, so the flat kernel can run one range of chunks
 };
 
 bool odd(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) != 0; }
@@ -709,7 +716,16 @@ arf_status_t check_call(arf_pattern_t pattern, const arf_run_opts_t* opts, bool 
     if (rms) v = v && ly->ldr % 8 == 0 && ly->ldro % 8 == 0 && aligned16(residual) && aligned16(gamma) &&
                  aligned16(residual_out);
     ly->vec_ok = v;
+    ly->range_ok = !rms && !ly->f32p && ly->ldp == H && ly->ldo == H && (M * H) % 8 == 0 && aligned16(out);
     return ARF_OK;
+}
+
+// Whether the 16-byte kernel of plan `pl` can take this call's layout: the
+// flat kAllReduce kernel on rows of H % 8 != 0 runs the whole contiguous
+// [M,H] as one range; every other 16-byte kernel needs 16-byte rows.
+bool layout_fits(const arf_plan_t& pl, arf_pattern_t pattern, int64_t H, const Layout& L) {
+    if (pattern == ARF_ALLREDUCE && pl.path == ARF_PATH_FLAT && H % 8 != 0) return L.range_ok;
+    return L.vec_ok;
 }
 
 // Current device and stream device must be the workspace's. While `stream`
@@ -855,7 +871,7 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
     if (forced && forced->path != ARF_PATH_ELEM) {
         // an explicit 16-byte plan needs a layout those kernels take; binary32
         // partials exist only in the run-time-W instances of the row/flat kernels
-        if (!L.vec_ok) return ARF_ERR_UNSUPPORTED;
+        if (!layout_fits(*forced, pattern, H, L)) return ARF_ERR_UNSUPPORTED;
         if (L.f32p && (forced->w_spec != 0 || forced->path == ARF_PATH_ASYNC || forced->path == ARF_PATH_BULK))
             return ARF_ERR_UNSUPPORTED;
     }
@@ -890,7 +906,7 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
         st = device_plan(ws, pattern, W, M, H, dtype, &pl, capturing);
         if (st != ARF_OK) return st;
         if (pl.path != ARF_PATH_ELEM) {
-            if (!L.vec_ok) {
+            if (!layout_fits(pl, pattern, H, L)) {
                 pl = elem_plan(ws->caps, pattern, M, H);  // strides or alignment the vectors cannot take
             } else if (L.f32p) {
                 // binary32 partials: the run-time W instances of the row and
@@ -1210,8 +1226,7 @@ extern "C" arf_status_t arf_read_pass(arf_workspace_t ws, const void* buf, int64
     if (!buf || !aligned16(buf)) return ARF_ERR_INVALID_ARG;
     // the sink is a spare word of the workspace's device allocation, past
     // the wait-timeout counter
-    cudaError_t e = arf::launch_read_pass(buf, bytes, ws->caps.num_sms, ws->wait_timeouts + 32,
-                                          static_cast<cudaStream_t>(stream));
+    cudaError_t e = arf::launch_read_pass(buf, bytes, ws->wait_timeouts + 32, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(ws, e);
     return ARF_OK;
 }

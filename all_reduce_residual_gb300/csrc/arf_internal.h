@@ -167,8 +167,8 @@ void note_cuda_error(arf_workspace_t ws, cudaError_t e);
 cudaError_t static_staging_address(void** out);
 cudaError_t workspace_static_staging(arf_workspace_t ws, void** out);
 
-// The read-only measurement pass (arf_measure.cu), sized from the SM count.
-cudaError_t launch_read_pass(const void* buf, int64_t bytes, int num_sms, unsigned int* sink, cudaStream_t s);
+// The read-only measurement pass (arf_measure.cu): a CTA per 16 KiB tile.
+cudaError_t launch_read_pass(const void* buf, int64_t bytes, unsigned int* sink, cudaStream_t s);
 
 // Host-buffer helper kernel launcher (arf_api.cu).
 cudaError_t launch_fill_pointer_array(const void** array, const char* first, int64_t stride, int W,

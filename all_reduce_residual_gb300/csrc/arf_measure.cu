@@ -9,39 +9,45 @@
 
 namespace arf {
 
-// Every thread reads four 16-byte vectors per trip (issued together) over
-// tiles of 4 x blockDim.x vectors at a grid stride, and folds them into a
-// register; one store, under a condition the data cannot be shown to avoid,
-// keeps the loads alive. Four CTAs of 256 threads per SM: on GB300 this
-// shape read fastest among those measured (136 MiB in 28.3 us and 2 GiB in
-// 311 us cold, against 30.8 and 347 us with one vector per trip and two
-// 512-thread CTAs per SM).
+// One tile of 4 x 256 16-byte vectors per CTA: every thread issues its four
+// loads together, folds them into a register and exits, and the grid has a
+// CTA per tile, so the hardware block scheduler hands the tiles to whichever
+// SM has room. On GB300 SMs do not all stream at the same rate; a fixed
+// share of the buffer per CTA (a resident grid walking it at a grid stride)
+// waits for the slowest SMs: 136 MiB cold took 28.6 us that way, with the
+// CTAs finishing over 18.8-24.2 us, against 26.2 us with a CTA per tile
+// (512 MiB: 88.7 against 77.2 us). Larger tiles per CTA measured slower
+// (8, 16 and 64 vectors per thread: 31.9, 32.8 and 38.9 us at 136 MiB). One
+// store, under a condition the data cannot be shown to avoid, keeps the
+// loads alive.
 constexpr int kReadUnroll = 4;
 constexpr int kReadThreads = 256;
 
 __global__ void __launch_bounds__(kReadThreads) read_pass_kernel(const uint4* a, int64_t n, unsigned int* sink) {
-    unsigned int x = 0;
-    const int64_t tile = (int64_t)blockDim.x * kReadUnroll;
-    for (int64_t t0 = (int64_t)blockIdx.x * tile; t0 < n; t0 += (int64_t)gridDim.x * tile) {
-        uint4 v[kReadUnroll];
+    const int64_t base = (int64_t)blockIdx.x * (kReadThreads * kReadUnroll) + threadIdx.x;
+    uint4 v[kReadUnroll];
 #pragma unroll
-        for (int k = 0; k < kReadUnroll; ++k) {
-            const int64_t i = t0 + (int64_t)k * blockDim.x + threadIdx.x;
-            if (i < n)
-                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(v[k].x), "=r"(v[k].y), "=r"(v[k].z), "=r"(v[k].w)
-                             : "l"(a + i));
-            else
-                v[k] = make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int k = 0; k < kReadUnroll; ++k) x ^= v[k].x ^ v[k].y ^ v[k].z ^ v[k].w;
+    for (int k = 0; k < kReadUnroll; ++k) {
+        const int64_t i = base + (int64_t)k * kReadThreads;
+        if (i < n)
+            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[k].x), "=r"(v[k].y), "=r"(v[k].z), "=r"(v[k].w)
+                         : "l"(a + i));
+        else
+            v[k] = make_uint4(0u, 0u, 0u, 0u);
     }
+    unsigned int x = 0;
+#pragma unroll
+    for (int k = 0; k < kReadUnroll; ++k) x ^= v[k].x ^ v[k].y ^ v[k].z ^ v[k].w;
     if (x == 0x9e3779b9u) *sink = x;
 }
 
-cudaError_t launch_read_pass(const void* buf, int64_t bytes, int num_sms, unsigned int* sink, cudaStream_t s) {
-    read_pass_kernel<<<4 * num_sms, kReadThreads, 0, s>>>(static_cast<const uint4*>(buf), bytes / 16, sink);
+cudaError_t launch_read_pass(const void* buf, int64_t bytes, unsigned int* sink, cudaStream_t s) {
+    const int64_t n = bytes / 16;
+    const int64_t tile = (int64_t)kReadThreads * kReadUnroll;
+    const int64_t grid = (n + tile - 1) / tile;
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    read_pass_kernel<<<(unsigned)grid, kReadThreads, 0, s>>>(static_cast<const uint4*>(buf), n, sink);
     return cudaGetLastError();
 }
 

@@ -89,6 +89,13 @@ def candidates(caps, pattern, W, H):
     out = []
     ws = W if W in COMPILED_W else 0  # the compiled rank count where there is one
     if H % 8 != 0:
+        if pattern == "allreduce":
+            # the flat kernel over the contiguous [M,H] as one range of chunks
+            # (arf_plan_check admits it where M * H is a multiple of 8)
+            for t in (128, 256, 512):
+                for u in (1, 2, 4):
+                    if u == 1 or (u == 2 and ws <= 8) or (u == 4 and ws <= 4):
+                        out.append((PATH_FLAT, t, u, 1, ws, 0, GRID_CHUNKS, 0))
         for t in (64, 128, 256, 512):
             if pattern == "allreduce":
                 for per in (2, 4, 8):
@@ -143,7 +150,9 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=OUT_DEFAULT)
     ap.add_argument("--reps", type=int, default=80, help="cold timings per finalist")
-    ap.add_argument("--keys", default=None, help="comma-separated key indices (default: all)")
+    ap.add_argument("--keys", default=None,
+                    help="comma-separated indices into KEYS: measure only these shapes and keep the other rows "
+                         "of the existing table (default: measure all and write a new table)")
     args = ap.parse_args()
 
     import torch
@@ -247,7 +256,13 @@ def main():
                       f"library plan {lp} {lib_us:8.3f} us  [{time.time() - t_start:6.0f} s]", flush=True)
             del inp, P, R, G, ptrs, out, ro
             torch.cuda.empty_cache()
-    write_table(args.out, caps, rows, torch.cuda.get_device_name(dev))
+    keep = []
+    if args.keys is not None and os.path.exists(args.out):
+        measured = {(0 if k[3] == "allreduce" else 1, 0 if k[2] == "bf16" else 1, k[0], k[1])
+                    for W, H, dts, pats in keys for k in [(W, H, dts, p) for p in pats]}
+        keep = [ln for ln in open(args.out) if ln.startswith("{") and
+                tuple(int(x) for x in ln[1:ln.index("}")].split(",")[4:8]) not in measured]
+    write_table(args.out, caps, rows, torch.cuda.get_device_name(dev), keep)
     ws.close()
 
 
@@ -299,8 +314,9 @@ def fmt(c):
     return f"{names[path]} {t}x{vpt} c{cs} w{wsp} s{st} {kinds[kind]}{per if kind in (1, 3) else ''}"
 
 
-def write_table(path, caps, rows, device_name):
-    """Merge the measured points into M ranges and write the C initialisers."""
+def write_table(path, caps, rows, device_name, keep=()):
+    """Merge the measured points into M ranges and write the C initialisers
+    (after `keep`: rows of an earlier table for shapes not measured now)."""
     by_key = {}
     for r in rows:
         by_key.setdefault((r[0], r[1], r[2], r[3]), []).append(r)
@@ -312,7 +328,7 @@ def write_table(path, caps, rows, device_name):
         "// dtype, W, H, M_lo, M_hi, path, threads, vpt, cluster, w_spec, stages, grid rule,",
         "// CTAs per SM (resident and tiles rules). Comments: the measured row counts,",
         "// the winner's time and the time of the plan the library chose before.",
-    ]
+    ] + [ln.rstrip("\n") for ln in keep]
     for (pattern, dts, W, H), pts in sorted(by_key.items()):
         pts.sort(key=lambda r: r[4])
         m_max = (1 << 40) // H

@@ -102,11 +102,19 @@ EXTRA_WORKLOADS = {
     "h32776": Workload("h32776", 11, 2, 1024, 32776, "bf16", 1.0, 1e-6, ("rmsnorm",)),
     "odd_h4098": Workload("odd_h4098", 12, 2, 4096, 4098, "bf16", 0.5, 1e-5, ("allreduce", "rmsnorm")),
 }
-# The kernel path the planner takes for each extra shape on GB300 (from its
-# measured plan table; the closed-form rules send h32768 and w1_fp16 to the
-# bulk kernel instead).
+# The kernel path the planner takes for each extra shape on GB300, from its
+# measured plan table (the closed-form rules send h32768 and w1_fp16 to the
+# bulk kernel, and odd_h4098's kAllReduce to the elementwise kernel). A dict
+# gives the path per pattern.
 EXTRA_PATHS = {"w3_generic": "bulk", "w12_generic": "bulk", "tp4_80mib_fp16": "row, one CTA per row",
-               "h32768": "row", "w1_fp16": "row, one CTA per row", "h32776": "bulk", "odd_h4098": "elem"}
+               "h32768": "row", "w1_fp16": "row, one CTA per row", "h32776": "bulk",
+               "odd_h4098": {"allreduce": "flat", "rmsnorm": "elem"}}
+
+
+def extra_path(name: str, pattern: str) -> str:
+    """The kernel path EXTRA_PATHS names for one pattern of an extra shape."""
+    v = EXTRA_PATHS[name]
+    return v[pattern] if isinstance(v, dict) else v
 
 
 def custom(W: int, M: int, H: int, dtype: str = "bf16", sigma: float = 1.0,

@@ -413,12 +413,14 @@ arf_status_t arf_run_host_static(arf_workspace_t ws, arf_pattern_t pattern, int 
 
 /* ---- measurement ----------------------------------------------------- */
 
-/* Read `bytes` bytes at `buf` once, in 16-byte vectors from every SM, and
- * discard them (nothing is written but, with vanishing probability, one word
- * of the workspace's own device memory). No counterpart on the source pages:
- * it is the roofline reference for calls that mostly read. On GB300 reads
- * alone stream slower than a copy's mix of reads and writes at the sizes the
- * epilogue runs at, so such a call is bounded by this pass over its reads.
+/* Read `bytes` bytes at `buf` once, in 16-byte vectors, and discard them
+ * (nothing is written but, with vanishing probability, one word of the
+ * workspace's own device memory). A CTA per 16 KiB tile, each thread issuing
+ * its four loads together, so the hardware block scheduler balances the SMs.
+ * No counterpart on the source pages: it is the roofline reference for calls
+ * that mostly read. On GB300 reads alone stream slower than a copy's mix of
+ * reads and writes at the sizes the epilogue runs at (the copy's writes stay
+ * in L2), so such a call is bounded by this pass over its reads.
  * Asynchronous on `stream`; time it with events.
  *   buf    device (or device-addressable host) memory, 16-byte aligned
  *   bytes  a multiple of 16; 0 launches nothing

@@ -437,7 +437,7 @@ def test_workload_tables_agree_with_the_planner():
     import bench
     assert set(wl.EXTRA_PATHS) == set(wl.EXTRA_WORKLOADS)
     want = {"bulk": arf.ARF_PATH_BULK, "elem": arf.ARF_PATH_ELEM, "row, one CTA per row": arf.ARF_PATH_ROW,
-            "row": arf.ARF_PATH_ROW}
+            "row": arf.ARF_PATH_ROW, "flat": arf.ARF_PATH_FLAT}
     for name, w in {**wl.WORKLOADS, **wl.EXTRA_WORKLOADS}.items():
         dt = arf.ARF_BF16 if w.dtype == "bf16" else arf.ARF_FP16
         for pat in w.patterns:
@@ -446,6 +446,6 @@ def test_workload_tables_agree_with_the_planner():
             table = bench.KERNEL_OF_PATH if pat == "rmsnorm" else bench.AR_KERNEL_OF_PATH
             assert p.path in table, (name, pat, p)
             if name in wl.EXTRA_PATHS:
-                assert p.path == want[wl.EXTRA_PATHS[name]], (name, pat, p)
-                if wl.EXTRA_PATHS[name] == "row, one CTA per row":
+                assert p.path == want[wl.extra_path(name, pat)], (name, pat, p)
+                if wl.extra_path(name, pat) == "row, one CTA per row":
                     assert p.grid == w.M, (name, pat, p)

@@ -277,3 +277,33 @@ def test_odd_h_flat_range(ws, pattern, M, H, misaligned, W):
     ref = oracle.run(OPAT[pattern], P, R if rms else None, G if rms else None, 1e-6, dtype=oracle.BF16)
     got = (host_codes(out), host_codes(ro) if rms else None)
     assert_parity(oracle.BF16, pattern, got, ref, f"M={M} H={H} misaligned={misaligned}")
+
+
+@pytest.mark.parametrize("W,M,H", [(2, 4096, 4098), (2, 4, 4098), (4, 8, 7175), (1, 16, 1001), (3, 8, 7170),
+                                   (16, 8, 13), (8, 24, 7171)])
+def test_flat_range_for_h_not_multiple_of_8(ws, W, M, H):
+    """kAllReduce with H % 8 != 0 on the 16-byte flat kernel: contiguous
+    tensors whose M * H is a multiple of 8 run as one range of chunks."""
+    assert (M * H) % 8 == 0
+    wspec = W if W in (1, 2, 4, 8, 16) else 0
+    for t, u in ((128, 1), (256, 2), (512, 4)):
+        if (u == 2 and wspec > 8) or (u == 4 and wspec > 4):
+            continue
+        grid = -(-(M * H // 8) // (t * u))
+        plan = arf.Plan(path=arf.ARF_PATH_FLAT, threads=t, vpt=u, cluster=1, grid=grid, w_spec=wspec, stages=0)
+        assert arf.arf_plan_check(ws.caps, plan, AR, W, M, H, arf.ARF_BF16) == arf.ARF_OK
+        run_case(ws, AR, "bf16", W, M, H, plan=plan, seed=M + t)
+
+
+def test_flat_range_needs_contiguous_rows_and_whole_chunks(ws):
+    """The flat range is refused where M * H is not a multiple of 8, and on
+    strided rows (an explicit plan is rejected; the planner's own plan falls
+    back to the elementwise kernel)."""
+    caps = ws.caps
+    plan = arf.Plan(path=arf.ARF_PATH_FLAT, threads=128, vpt=1, cluster=1, grid=11, w_spec=2, stages=0)
+    assert arf.arf_plan_check(caps, plan, AR, 2, 3, 4098, arf.ARF_BF16) == arf.ARF_ERR_UNSUPPORTED
+    assert arf.arf_plan_check(caps, plan, AR, 2, 4, 4098, arf.ARF_BF16) == arf.ARF_OK
+    with pytest.raises(arf.ArfError) as e:
+        run_case(ws, AR, "bf16", 2, 4, 4098, pads=(8, 0, 8, 0), plan=plan)
+    assert e.value.status == arf.ARF_ERR_UNSUPPORTED
+    run_case(ws, AR, "bf16", 2, 4, 4098, pads=(8, 0, 8, 0))  # the planner's plan on the strided rows

@@ -33,11 +33,14 @@ def test_workload_parity(ws, name, M, pattern):
     pat = PAT[pattern]
     if name in wl.EXTRA_WORKLOADS:  # these shapes exist to reach particular kernel paths
         plan = ws.plan(pattern, len(P), M, inp.workload.H, P[0].dtype)
-        if wl.EXTRA_PATHS[name] == "bulk":
+        want = wl.extra_path(name, pattern)
+        if want == "bulk":
             assert plan.path == arf.ARF_PATH_BULK, plan
-        elif wl.EXTRA_PATHS[name] == "elem":
+        elif want == "elem":
             assert plan.path == arf.ARF_PATH_ELEM, plan
-        elif wl.EXTRA_PATHS[name] == "row":
+        elif want == "flat":
+            assert plan.path == arf.ARF_PATH_FLAT, plan
+        elif want == "row":
             assert plan.path == arf.ARF_PATH_ROW, plan
         else:
             assert plan.path == arf.ARF_PATH_ROW and plan.grid == M, plan

@@ -47,8 +47,10 @@ def test_table_plan_matches_oracle(ws, row, M):
     dts = "bf16" if row["dtype"] == arf.ARF_BF16 else "fp16"
     W, H, pattern = row["W"], row["H"], row["pattern"]
     plan = ws.plan(pattern, W, M, H, wl.TORCH_DTYPE[dts])
-    assert (plan.path, plan.threads, plan.vpt, plan.cluster, plan.grid, plan.w_spec, plan.stages) == \
-        pt.row_plan_fields(row, M)
+    row_plan = arf.Plan(*pt.row_plan_fields(row, M))
+    if arf.arf_plan_check(caps, row_plan, pattern, W, M, H, row["dtype"]) == arf.ARF_OK:
+        assert (plan.path, plan.threads, plan.vpt, plan.cluster, plan.grid, plan.w_spec, plan.stages) == \
+            pt.row_plan_fields(row, M)
     w = wl.custom(W, M, H, dts, 0.5, 1e-6, config_id=960 + (M % 17))
     dev = wl.make_inputs(w, device="cuda")  # drawn on the GPU; the oracle gets the same bytes
     out, ro = arf.run(ws, pattern, dev.partials, dev.residual, dev.gamma, w.eps)

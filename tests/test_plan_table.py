@@ -31,15 +31,31 @@ def test_ranges_are_disjoint_and_contiguous():
             assert b_lo == a_hi + 1, (key, rs)
 
 
+def _fields(p):
+    return (p.path, p.threads, p.vpt, p.cluster, p.grid, p.w_spec, p.stages)
+
+
 def test_planner_returns_each_row_plan():
+    """At both ends of each row's range (and inside it) the planner returns the
+    row's plan; where that plan is not legal for the M (the flat kAllReduce
+    range of rows with H % 8 != 0 needs M * H to be a multiple of 8) it
+    returns the closed-form rules' plan instead."""
     for r in pt.read_table():
         caps = _caps(r)
-        for M in sorted({r["m_lo"], min(r["m_hi"], 4 * r["m_lo"]), r["m_hi"]}):
-            want = pt.row_plan_fields(r, M)
+        for M in sorted({r["m_lo"], r["m_lo"] + 1, min(r["m_hi"], 4 * r["m_lo"]), r["m_hi"]} - {r["m_hi"] + 1}):
+            if M > r["m_hi"]:
+                continue
+            row = arf.Plan(*pt.row_plan_fields(r, M))
+            legal = arf.arf_plan_check(caps, row, r["pattern"], r["W"], M, r["H"], r["dtype"]) == arf.ARF_OK
+            want = arf.Plan()
+            if legal:
+                want = row
+            else:
+                assert arf.arf_plan_rules(caps, r["pattern"], r["W"], M, r["H"], r["dtype"], want) == arf.ARF_OK
             got = arf.Plan()
             st = arf.arf_plan_for_caps(caps, r["pattern"], r["W"], M, r["H"], r["dtype"], got)
             assert st == arf.ARF_OK, (r, M)
-            assert (got.path, got.threads, got.vpt, got.cluster, got.grid, got.w_spec, got.stages) == want, (r, M, got)
+            assert _fields(got) == _fields(want), (r, M, got)
             assert arf.arf_plan_check(caps, got, r["pattern"], r["W"], M, r["H"], r["dtype"]) == arf.ARF_OK
 
 
