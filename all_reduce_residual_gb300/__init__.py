@@ -13,7 +13,7 @@ from ._binding import (  # noqa: F401  (re-exported C-ABI names)
     ARF_AR_RESIDUAL_RMSNORM, ARF_ALLREDUCE, ARF_BF16, ARF_ERR_CUDA, ARF_ERR_DEVICE_MISMATCH,
     ARF_ERR_INVALID_ARG, ARF_ERR_UNSUPPORTED, ARF_FP16, ARF_MAX_H, ARF_MAX_H_PER_CTA, ARF_MAX_W, ARF_OK,
     ARF_PATH_ASYNC, ARF_PATH_BULK, ARF_PATH_CLUSTER, ARF_PATH_ELEM, ARF_PATH_FLAT, ARF_PATH_ROW,
-    ARF_STATIC_STAGING_BYTES, ArfError, DeviceCaps, Plan, RunOpts,
+    ARF_STATIC_STAGING_BYTES, COMPILED_W, ArfError, DeviceCaps, Plan, RunOpts,
     arf_host_staging_bytes, arf_last_cuda_error, arf_plan_check, arf_plan_for_caps, arf_plan_rules, arf_read_pass,
     arf_run,
     arf_run_ex,

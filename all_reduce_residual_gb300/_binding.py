@@ -37,6 +37,8 @@ ARF_MAX_W = 64
 ARF_MAX_H = 524288
 ARF_MAX_H_PER_CTA = 32768
 ARF_STATIC_STAGING_BYTES = 16 << 20
+# Rank counts with kernels specialised at compile time (w_spec values other than 0).
+COMPILED_W = (1, 2, 4, 8, 12, 16)
 
 STATUS_NAMES = {0: "ARF_OK", 1: "ARF_ERR_INVALID_ARG", 2: "ARF_ERR_UNSUPPORTED", 3: "ARF_ERR_CUDA",
                 4: "ARF_ERR_DEVICE_MISMATCH"}

@@ -11,9 +11,10 @@ namespace arf {
 // Every kernel is compiled for at most this many threads per CTA.
 constexpr int kMaxThreads = 512;
 
-// Rank counts with a kernel specialised at compile time (0 = generic).
+// Rank counts with a kernel specialised at compile time (0 = generic): the
+// pages' tensor-parallel sizes up to 16, TP12 included.
 constexpr bool w_spec_compiled(int ws) {
-    return ws == 0 || ws == 1 || ws == 2 || ws == 4 || ws == 8 || ws == 16;
+    return ws == 0 || ws == 1 || ws == 2 || ws == 4 || ws == 8 || ws == 12 || ws == 16;
 }
 // Flat-kernel unroll factors compiled per rank count (registers: U*W vectors).
 constexpr bool flat_unroll_compiled(int ws, int u) {

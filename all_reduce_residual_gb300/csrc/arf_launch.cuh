@@ -38,6 +38,7 @@ FlatFn flat_kernel_for(int ws, int u, bool f32p = false) {
         case 2: return flat_by_unroll<T, 2>(u);
         case 4: return flat_by_unroll<T, 4>(u);
         case 8: return flat_by_unroll<T, 8>(u);
+        case 12: return flat_by_unroll<T, 12>(u);
         case 16: return flat_by_unroll<T, 16>(u);
         default: return nullptr;
     }
@@ -72,6 +73,7 @@ RmsFn rms_kernel_for(int ws, int vpt, bool f32p = false) {
         case 2: return rms_by_vpt<T, 2>(vpt);
         case 4: return rms_by_vpt<T, 4>(vpt);
         case 8: return rms_by_vpt<T, 8>(vpt);
+        case 12: return rms_by_vpt<T, 12>(vpt);
         case 16: return rms_by_vpt<T, 16>(vpt);
         default: return nullptr;
     }
@@ -96,6 +98,7 @@ RmsFn one_row_kernel_for(int ws, int vpt) {
         case 2: return one_row_by_vpt<T, 2>(vpt);
         case 4: return one_row_by_vpt<T, 4>(vpt);
         case 8: return one_row_by_vpt<T, 8>(vpt);
+        case 12: return one_row_by_vpt<T, 12>(vpt);
         case 16: return one_row_by_vpt<T, 16>(vpt);
         default: return nullptr;
     }
@@ -108,6 +111,7 @@ RmsFn async_kernel_for(int ws) {
         case 2: return rms_async_kernel<T, 2>;
         case 4: return rms_async_kernel<T, 4>;
         case 8: return rms_async_kernel<T, 8>;
+        case 12: return rms_async_kernel<T, 12>;
         case 16: return rms_async_kernel<T, 16>;
         default: return nullptr;
     }
@@ -121,6 +125,7 @@ RmsFn bulk_kernel_for(int ws) {
         case 2: return rms_bulk_kernel<T, 2>;
         case 4: return rms_bulk_kernel<T, 4>;
         case 8: return rms_bulk_kernel<T, 8>;
+        case 12: return rms_bulk_kernel<T, 12>;
         case 16: return rms_bulk_kernel<T, 16>;
         default: return nullptr;
     }
@@ -134,6 +139,7 @@ RmsFn bulk_ar_kernel_for(int ws) {
         case 2: return rms_bulk_kernel<T, 2, false>;
         case 4: return rms_bulk_kernel<T, 4, false>;
         case 8: return rms_bulk_kernel<T, 8, false>;
+        case 12: return rms_bulk_kernel<T, 12, false>;
         case 16: return rms_bulk_kernel<T, 16, false>;
         default: return nullptr;
     }
@@ -266,7 +272,7 @@ cudaError_t launch_elem_t(const ElemParams& p, const arf_plan_t& plan, bool rms,
 
 template <typename T>
 cudaError_t configure_kernels_t(bool clusters, int max_dyn_smem) {
-    const int ws_list[] = {0, 1, 2, 4, 8, 16};
+    const int ws_list[] = {0, 1, 2, 4, 8, 12, 16};
     const int vpt_list[] = {1, 2, 4, 8};
     if (clusters)
         for (int ws : ws_list)

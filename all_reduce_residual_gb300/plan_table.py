@@ -45,7 +45,7 @@ OUT_DEFAULT = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc", "
 
 GRID_ROWS, GRID_RESIDENT, GRID_CHUNKS, GRID_TILES = 0, 1, 2, 3
 PATH_FLAT, PATH_ROW, PATH_CLUSTER, PATH_ASYNC, PATH_ELEM, PATH_BULK = 0, 1, 2, 3, 4, 5
-COMPILED_W = (1, 2, 4, 8, 16)
+COMPILED_W = (1, 2, 4, 8, 12, 16)
 MAX_THREADS = 512
 
 # (W, H, dtype, patterns): the five benchmark workloads' shapes and the extra
@@ -138,9 +138,10 @@ def candidates(caps, pattern, W, H):
             for per in (1, 2, 4):
                 if per * t <= caps.max_threads_per_sm:
                     out.append((PATH_CLUSTER, t, vpt, cs, ws, 0, GRID_RESIDENT, per))
-    # the bulk-copy ring
+    # the bulk-copy ring: a resident grid walking the rows, or one CTA per row
     for t in (128, 256, 512):
         for st in (2, 3, 4):
+            out.append((PATH_BULK, t, 1, 1, ws, st, GRID_ROWS, 0))
             for per in (1, 2):
                 out.append((PATH_BULK, t, 1, 1, ws, st, GRID_RESIDENT, per))
     return out

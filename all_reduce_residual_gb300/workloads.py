@@ -103,10 +103,10 @@ EXTRA_WORKLOADS = {
     "odd_h4098": Workload("odd_h4098", 12, 2, 4096, 4098, "bf16", 0.5, 1e-5, ("allreduce", "rmsnorm")),
 }
 # The kernel path the planner takes for each extra shape on GB300, from its
-# measured plan table (the closed-form rules send h32768 and w1_fp16 to the
-# bulk kernel, and odd_h4098's kAllReduce to the elementwise kernel). A dict
-# gives the path per pattern.
-EXTRA_PATHS = {"w3_generic": "bulk", "w12_generic": "bulk", "tp4_80mib_fp16": "row, one CTA per row",
+# measured plan table (the closed-form rules send w12_generic, h32768 and
+# w1_fp16 to the bulk kernel, and odd_h4098's kAllReduce to the elementwise
+# kernel). A dict gives the path per pattern.
+EXTRA_PATHS = {"w3_generic": "bulk", "w12_generic": "cluster", "tp4_80mib_fp16": "row, one CTA per row",
                "h32768": "row", "w1_fp16": "row, one CTA per row", "h32776": "bulk",
                "odd_h4098": {"allreduce": "flat", "rmsnorm": "elem"}}
 

@@ -76,6 +76,17 @@ def test_binding_constants_match_the_header():
     assert not missing, missing
 
 
+def test_compiled_rank_counts_match_the_library():
+    """arf_plan_check accepts a plan with the rank count compiled in exactly
+    for the rank counts COMPILED_W lists."""
+    accepted = []
+    for W in range(1, arf.ARF_MAX_W + 1):
+        p = arf.Plan(path=arf.ARF_PATH_FLAT, threads=128, vpt=1, cluster=1, grid=7, w_spec=W, stages=0)
+        if arf.arf_plan_check(GB300, p, arf.ARF_ALLREDUCE, W, 1, 7168, arf.ARF_BF16) == arf.ARF_OK:
+            accepted.append(W)
+    assert tuple(accepted) == arf.COMPILED_W
+
+
 def test_static_staging_size_is_the_headers():
     """The library reports the staging size arf.h declares, and the binding's
     copy of the constant agrees with both."""
@@ -137,7 +148,7 @@ def test_planner_plans_are_legal(pattern, W, M, H):
             continue
         if p.path == arf.ARF_PATH_ASYNC:
             # many rows, compile-time W: one streaming CTA per SM, ring of >= 3 blocks in shared memory
-            assert M >= caps.num_sms and W in (1, 2, 4, 8, 16) and p.grid == caps.num_sms
+            assert M >= caps.num_sms and W in arf.COMPILED_W and p.grid == caps.num_sms
             ring = p.stages * (W + 1) * 256 * 16 + (H // 8) * 16
             assert 3 <= p.stages <= 8 and ring + 1024 <= caps.max_smem_per_block
             continue
@@ -146,7 +157,7 @@ def test_planner_plans_are_legal(pattern, W, M, H):
         vpt = 1
         while vpt < 8 and -(-C // vpt) > 512:
             vpt *= 2
-        prefetch = W in (1, 2, 4, 8, 16) and vpt * (W + 1) <= 18
+        prefetch = W in arf.COMPILED_W and vpt * (W + 1) <= 18
         if p.path == arf.ARF_PATH_BULK:
             # one CTA per row would run without the register prefetch: the bulk ring instead
             assert pattern == arf.ARF_AR_RESIDUAL_RMSNORM and W <= 12 and not prefetch and C <= 4096
@@ -437,7 +448,7 @@ def test_workload_tables_agree_with_the_planner():
     import bench
     assert set(wl.EXTRA_PATHS) == set(wl.EXTRA_WORKLOADS)
     want = {"bulk": arf.ARF_PATH_BULK, "elem": arf.ARF_PATH_ELEM, "row, one CTA per row": arf.ARF_PATH_ROW,
-            "row": arf.ARF_PATH_ROW, "flat": arf.ARF_PATH_FLAT}
+            "row": arf.ARF_PATH_ROW, "flat": arf.ARF_PATH_FLAT, "cluster": arf.ARF_PATH_CLUSTER}
     for name, w in {**wl.WORKLOADS, **wl.EXTRA_WORKLOADS}.items():
         dt = arf.ARF_BF16 if w.dtype == "bf16" else arf.ARF_FP16
         for pat in w.patterns:

@@ -42,12 +42,13 @@ def inputs(W, M, H, dtype, seed):
 @pytest.mark.parametrize("W,M,H,dtype", [(1, 9, 8, "bf16"), (2, 37, 1000, "bf16"), (3, 5, 7168, "fp16"),
                                          (8, 41, 7176, "bf16"), (16, 23, 7168, "fp16"), (16, 3, 4096, "bf16"),
                                          (17, 6, 2056, "fp16"), (64, 2, 256, "bf16"), (4, 300, 264, "fp16"),
-                                         (4, 2, 32768, "bf16"), (2, 5, 32776, "bf16"), (8, 3, 65536, "fp16")])
+                                         (4, 2, 32768, "bf16"), (2, 5, 32776, "bf16"), (8, 3, 65536, "fp16"),
+                                         (12, 11, 7168, "fp16")])
 def test_bulk_plans(ws, W, M, H, dtype):
     inp = inputs(W, M, H, dtype, W * 131 + M)
     ref = oracle_run(RMS, inp)
     P, R, G = to_device(inp)
-    w_specs = sorted({0, W if W in (1, 2, 4, 8, 16) else 0})
+    w_specs = sorted({0, W if W in arf.COMPILED_W else 0})
     ran = 0
     for threads in (32, 128, 256, 512):
         for stages in (2, 3, 6, 16):
@@ -167,7 +168,7 @@ def test_bulk_fuzz(ws, case):
     inp = wl.make_inputs(wl.custom(W, M, H, dtype, float(rng.choice([0.01, 1.0, 30.0])), 1e-6, config_id=6000 + case))
     for _ in range(100):
         plan = bulk(int(rng.choice([32, 64, 96, 128, 256, 384, 512])), int(rng.integers(2, 17)),
-                    int(rng.integers(1, 700)), int(rng.choice([0, W])) if W in (1, 2, 4, 8, 16) else 0)
+                    int(rng.integers(1, 700)), int(rng.choice([0, W])) if W in arf.COMPILED_W else 0)
         if legal(ws, plan, W, M, H, dtype):
             break
     else:
@@ -240,7 +241,7 @@ def test_bulk_pdl_chain(ws):
 
 @pytest.mark.parametrize("W,M,H,dtype", [(1, 9, 8, "bf16"), (2, 37, 1000, "fp16"), (3, 5, 7168, "bf16"),
                                          (8, 41, 7176, "bf16"), (16, 23, 7168, "fp16"), (64, 2, 256, "bf16"),
-                                         (4, 300, 264, "fp16")])
+                                         (4, 300, 264, "fp16"), (12, 7, 1000, "bf16")])
 def test_bulk_allreduce_plans(ws, W, M, H, dtype):
     """The kAllReduce form of the bulk kernel: bitwise equal to the oracle for
     every block width, ring depth and grid drawn."""
@@ -251,7 +252,7 @@ def test_bulk_allreduce_plans(ws, W, M, H, dtype):
     for threads in (32, 128, 512):
         for stages in (2, 5, 16):
             for grid in sorted({1, 7, M, 2 * M + 1}):
-                for w_spec in sorted({0, W if W in (1, 2, 4, 8, 16) else 0}):
+                for w_spec in sorted({0, W if W in arf.COMPILED_W else 0}):
                     plan = bulk(threads, stages, grid, w_spec)
                     if arf.arf_plan_check(ws.caps, plan, AR, W, M, H, arf.dtype_code(wl.TORCH_DTYPE[dtype])) != 0:
                         continue

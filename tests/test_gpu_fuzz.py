@@ -26,7 +26,7 @@ def random_plan(rng, ws, pattern, W, M, H, dtype):
     caps = ws.caps
     if rng.random() < 0.4:
         return None
-    ws_choices = [0] + ([W] if W in (1, 2, 4, 8, 16) else [])
+    ws_choices = [0] + ([W] if W in arf.COMPILED_W else [])
     for _ in range(50):
         w_spec = int(rng.choice(ws_choices))
         if pattern == AR:
@@ -39,7 +39,7 @@ def random_plan(rng, ws, pattern, W, M, H, dtype):
                 p = arf.Plan(path=arf.ARF_PATH_BULK, threads=int(rng.choice([32, 64, 128, 256, 512])), vpt=1,
                              cluster=1, grid=int(rng.integers(1, 600)), w_spec=w_spec,
                              stages=int(rng.integers(2, 17)))
-            elif kind == 2 and W in (1, 2, 4, 8, 16):
+            elif kind == 2 and W in arf.COMPILED_W:
                 p = arf.Plan(path=arf.ARF_PATH_ASYNC, threads=256, vpt=1, cluster=1,
                              grid=int(rng.integers(1, 200)), w_spec=W, stages=int(rng.integers(2, 9)))
             else:

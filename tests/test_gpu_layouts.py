@@ -285,7 +285,7 @@ def test_flat_range_for_h_not_multiple_of_8(ws, W, M, H):
     """kAllReduce with H % 8 != 0 on the 16-byte flat kernel: contiguous
     tensors whose M * H is a multiple of 8 run as one range of chunks."""
     assert (M * H) % 8 == 0
-    wspec = W if W in (1, 2, 4, 8, 16) else 0
+    wspec = W if W in arf.COMPILED_W else 0
     for t, u in ((128, 1), (256, 2), (512, 4)):
         if (u == 2 and wspec > 8) or (u == 4 and wspec > 4):
             continue

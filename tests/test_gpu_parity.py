@@ -40,6 +40,8 @@ def test_workload_parity(ws, name, M, pattern):
             assert plan.path == arf.ARF_PATH_ELEM, plan
         elif want == "flat":
             assert plan.path == arf.ARF_PATH_FLAT, plan
+        elif want == "cluster":
+            assert plan.path == arf.ARF_PATH_CLUSTER, plan
         elif want == "row":
             assert plan.path == arf.ARF_PATH_ROW, plan
         else:

@@ -58,12 +58,12 @@ def rms_plans(ws, W, M, H, grids=("full", 1)):
                 continue
             for g in grids:
                 nclus = min(M, 2 * caps.num_sms) if g == "full" else g
-                for w_spec in {0, W if W in (1, 2, 4, 8, 16) else 0}:
+                for w_spec in {0, W if W in arf.COMPILED_W else 0}:
                     p = arf.Plan(path=arf.ARF_PATH_ROW if cs == 1 else arf.ARF_PATH_CLUSTER, threads=threads,
                                  vpt=vpt, cluster=cs, grid=max(1, nclus) * cs, w_spec=w_spec)
                     assert arf.arf_plan_check(caps, p, RMS, W, M, H, arf.ARF_BF16) == arf.ARF_OK, p
                     plans.append(p)
-    if W in (1, 2, 4, 8, 16):  # the streaming kernel, every ring depth that fits
+    if W in arf.COMPILED_W:  # the streaming kernel, every ring depth that fits
         for stages in range(2, 9):
             for g in ("full", 1, 3):
                 grid = min(M, caps.num_sms) if g == "full" else g
@@ -77,7 +77,8 @@ def rms_plans(ws, W, M, H, grids=("full", 1)):
 @pytest.mark.parametrize("W,M,H,dtype", [(3, 37, 1000, "bf16"), (8, 5, 7168, "bf16"), (16, 3, 4096, "fp16"),
                                          (1, 9, 8, "bf16"), (64, 2, 256, "fp16"), (5, 4, 32768, "bf16"),
                                          (2, 19, 2056, "bf16"), (4, 41, 7176, "bf16"), (16, 23, 7168, "fp16"),
-                                         (8, 13, 32768, "bf16"), (1, 300, 264, "fp16")])
+                                         (8, 13, 32768, "bf16"), (1, 300, 264, "fp16"), (12, 7, 7168, "fp16"),
+                                         (12, 3, 1000, "bf16")])
 def test_every_rms_plan(ws, W, M, H, dtype):
     inp = inputs(W, M, H, dtype)
     ref = oracle_run(RMS, inp)
@@ -99,12 +100,13 @@ def test_every_rms_plan(ws, W, M, H, dtype):
 
 
 @pytest.mark.parametrize("W,M,H,dtype", [(3, 37, 1000, "bf16"), (2, 1, 8, "bf16"), (16, 11, 2056, "fp16"),
-                                         (8, 3, 7168, "bf16"), (4, 5, 264, "fp16"), (1, 7, 24, "bf16")])
+                                         (8, 3, 7168, "bf16"), (4, 5, 264, "fp16"), (1, 7, 24, "bf16"),
+                                         (12, 9, 7168, "fp16")])
 def test_every_flat_plan(ws, W, M, H, dtype):
     inp = inputs(W, M, H, dtype)
     ref = oracle_run(AR, inp)
     P, R, G = to_device(inp)
-    specs = {0, W if W in (1, 2, 4, 8, 16) else 0}
+    specs = {0, W if W in arf.COMPILED_W else 0}
     for w_spec in specs:
         for u in (1, 2, 4):
             for threads in (32, 256, 512):
