@@ -138,14 +138,16 @@ def _check_operand(t, name, shape, dtype, device):
 
 def run(ws: Workspace, pattern, partials, residual=None, gamma=None, eps: float = 0.0, out=None,
         residual_out=None, stream=None, plan: Plan | None = None, ptrs=None, by_value: bool = False,
-        pdl: bool = False):
+        pdl=None):
     """Run one pattern on CUDA tensors.
 
     partials: list of W [M,H] tensors (rank order). ``ptrs`` may be passed
     instead of building the pointer array here (for CUDA-graph capture, keep
     it alive and stable). out / residual_out are allocated when None.
     by_value / pdl / plan: the options of arf_run_ex (partials passed in the
-    launch, programmatic dependent launch, an explicit launch plan).
+    launch, programmatic dependent launch, an explicit launch plan). pdl:
+    None = the library's choice (on for latency-bound launches), True =
+    always, False = never.
     Returns (out, residual_out); residual_out is None for kAllReduce.
     """
     torch = _torch()
@@ -184,9 +186,10 @@ def run(ws: Workspace, pattern, partials, residual=None, gamma=None, eps: float 
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     tail = (r_ptr, g_ptr, float(eps), out.data_ptr(), ro_ptr, M, H, dtype_code(dt), s.cuda_stream)
     general = f32p or (ldp, ldr, ldo, ldro) != (H, H, H, H)
-    if by_value or pdl or general:
+    pdl_code = 0 if pdl is None else (1 if pdl else 2)  # arf_run_opts_t.pdl: 0 auto, 1 always, 2 never
+    if by_value or pdl is not None or general:
         opts = RunOpts(plan=ctypes.pointer(plan) if plan is not None else None, partials_by_value=int(by_value),
-                       pdl=int(pdl), ld_partials=ldp, ld_residual=ldr, ld_out=ldo, ld_residual_out=ldro,
+                       pdl=pdl_code, ld_partials=ldp, ld_residual=ldr, ld_out=ldo, ld_residual_out=ldro,
                        partials_f32=int(f32p))
         if by_value:
             parts = [p.data_ptr() for p in P]

@@ -864,7 +864,8 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
     if (!ws) return ARF_ERR_INVALID_ARG;
     const arf_plan_t* forced = opts ? opts->plan : nullptr;
     const bool by_value = opts && opts->partials_by_value;
-    const bool pdl = opts && opts->pdl;
+    const int pdl_opt = opts ? opts->pdl : 0;
+    if (pdl_opt < 0 || pdl_opt > 2) return ARF_ERR_INVALID_ARG;
     arf_status_t st = arf_supports(ws, pattern, W, M, H, dtype);
     if (st != ARF_OK) return st;
     if (forced) {
@@ -930,6 +931,12 @@ arf_status_t run_impl(arf_workspace_t ws, const arf_run_opts_t* opts, arf_patter
             }
         }
     }
+    // Programmatic dependent launch: by default for latency-bound launches
+    // (grid x threads at most 1/16 of the device's resident threads), where
+    // overlapping this launch with the previous kernel's tail is the gain;
+    // larger grids would hold SM slots with waiting CTAs.
+    const bool pdl = pdl_opt == 1 || (pdl_opt == 0 && (int64_t)pl.grid * pl.threads * 16 <=
+                                                          (int64_t)ws->caps.num_sms * ws->caps.max_threads_per_sm);
     return launch(ws, pl, pattern, W, partials, by_value, pdl, residual, gamma, eps, out, residual_out, M, H, dtype,
                   L, stream, opts);
 }

@@ -593,7 +593,7 @@ def sweep(ws, dev, flush, peak):
 
                 def call(opt=False, wsx=None):
                     arf.run(wsx or ws, pat, P, R, G, w.eps, out=out, residual_out=ro if pat == "rmsnorm" else None,
-                            ptrs=ptrs, by_value=opt, pdl=opt)
+                            ptrs=ptrs, by_value=opt, pdl=True if opt else None)
 
                 def cold_us(opt, dirty=False):
                     for _ in range(10):

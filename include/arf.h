@@ -307,12 +307,21 @@ typedef struct arf_run_opts {
                                 round trip less); a captured graph keeps the
                                 values, and the host array may be reused as
                                 soon as the call returns. */
-    int pdl;                 /* 1: launch as a programmatic dependent launch:
-                                the kernel may be scheduled while the previous
-                                kernel in the stream still runs, and waits
+    int pdl;                 /* programmatic dependent launch: the kernel may
+                                be scheduled while the previous kernel in the
+                                stream still runs, and waits
                                 (griddepcontrol.wait) for it to complete before
                                 it touches any memory, so results are the same;
-                                what overlaps is launch latency. */
+                                what overlaps is launch latency.
+                                0 = the library's choice (the default, also for
+                                arf_run): on for latency-bound launches, whose
+                                grid x threads is at most 1/16 of the threads
+                                the device holds (decode sizes; measured on
+                                GB300 in CUDA graphs: k3 TP8 M = 1..8
+                                kARResidualRMSNorm 2.6-2.7 -> 2.2-2.4 us per
+                                call), off for larger ones, where waiting CTAs
+                                would hold SM slots; 1 = always; 2 = never.
+                                Other values -> ARF_ERR_INVALID_ARG. */
     int64_t ld_partials;     /* row strides in elements (0 = H, contiguous): of */
     int64_t ld_residual;     /* every partial, the residual, out and            */
     int64_t ld_out;          /* residual_out. Each must be >= H                 */

@@ -557,3 +557,38 @@ def test_read_pass(ws):
     assert arf.arf_read_pass(ws.handle, buf.data_ptr(), 1000, s) == arf.ARF_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.equal(buf, keep)
+
+
+@pytest.mark.parametrize("code", [0, 1, 2])
+def test_pdl_codes_in_graph(ws, code):
+    """arf_run_opts_t.pdl: 0 (the library's choice: on for this decode-size
+    call), 1 (always), 2 (never); each, replayed in a CUDA graph, matches the
+    oracle; other values are refused."""
+    inp = inputs(8, 4, 7168, "bf16")
+    P, R, G = to_device(inp)
+    ptrs = arf.pointer_array(P)
+    out, ro = torch.empty_like(R), torch.empty_like(R)
+    opts = arf.RunOpts(plan=None, partials_by_value=0, pdl=code)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def call():
+        st = arf.arf_run_ex(ws.handle, opts, RMS, 8, ptrs.data_ptr(), R.data_ptr(), G.data_ptr(), 1e-6,
+                            out.data_ptr(), ro.data_ptr(), 4, 7168, arf.ARF_BF16, s.cuda_stream)
+        assert st == arf.ARF_OK, arf.arf_status_string(st)
+
+    with torch.cuda.stream(s):
+        call()  # plan made outside the capture
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(3):
+                call()
+    out.zero_()
+    ro.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert_parity(DT["bf16"], RMS, (wl.codes(out.cpu()), wl.codes(ro.cpu())), oracle_run(RMS, inp), f"pdl={code}")
+    bad = arf.RunOpts(plan=None, partials_by_value=0, pdl=3)
+    st = arf.arf_run_ex(ws.handle, bad, RMS, 8, ptrs.data_ptr(), R.data_ptr(), G.data_ptr(), 1e-6, out.data_ptr(),
+                        ro.data_ptr(), 4, 7168, arf.ARF_BF16, torch.cuda.current_stream().cuda_stream)
+    assert st == arf.ARF_ERR_INVALID_ARG
