@@ -535,14 +535,7 @@ extern "C" arf_status_t arf_plan_check(const arf_device_caps_t* caps, const arf_
     if (pl->threads < 32 || pl->threads > kMaxThreads || pl->threads % 32 != 0) return ARF_ERR_UNSUPPORTED;
     if (pl->cluster < 1 || pl->grid < 1 || pl->grid % pl->cluster != 0) return ARF_ERR_UNSUPPORTED;
     if (pl->path == ARF_PATH_ELEM) {
-        if (pl->cluster != 1 || pl->stages != 0) return ARF_ERR_UNSUPPORTED;
-        if (pl->vpt == 1) return pl->w_spec == 0 ? ARF_OK : ARF_ERR_UNSUPPORTED;
-        // vpt > 1: kARResidualRMSNorm's register row kernel, W compiled in,
-        // enough threads for a row at any phase, gamma in shared memory
-        if (pattern != ARF_AR_RESIDUAL_RMSNORM || pl->w_spec != W || !arf::vrow_compiled(W, pl->vpt))
-            return ARF_ERR_UNSUPPORTED;
-        if ((int64_t)pl->threads * pl->vpt < arf::vrow_max_vectors(H)) return ARF_ERR_UNSUPPORTED;
-        if (arf::vrow_smem(H) + arf::kVrowStaticSmem > (size_t)caps->max_smem_per_block) return ARF_ERR_UNSUPPORTED;
+        if (pl->cluster != 1 || pl->vpt != 1 || pl->stages != 0 || pl->w_spec != 0) return ARF_ERR_UNSUPPORTED;
         return ARF_OK;
     }
     // The 16-byte kernels need whole chunks. kAllReduce is elementwise, so

@@ -280,12 +280,25 @@ __device__ __forceinline__ void rms_flat_row(const ElemParams& p, const uint4* c
     }
 }
 
-// kARResidualRMSNorm one element per thread per step, rows grid-stride (one
-// CTA per row): any layout. The rounded residual_out goes to memory in the
-// first pass and is read back in the second by the thread that wrote it.
-template <typename T, bool F32P>
-__device__ __forceinline__ void rms_elem_rows(const ElemParams& p, const uint4* const* s_ptr,
-                                              float (*s_warp)[kMaxThreads / 32]) {
+// kARResidualRMSNorm: one CTA per row (rows grid-stride). The rounded
+// residual_out goes to memory in the first pass and is read back in the
+// second by the thread that wrote it. Tensors whose rows share their
+// 16-byte phase (flat_ok, and every partial pointer aligned) take
+// rms_flat_row instead.
+template <typename T, bool F32P, int WS = 0>
+__global__ void __launch_bounds__(kMaxThreads, 2) rms_elem_kernel(ElemParams p) {
+    static_assert(!F32P || WS == 0, "binary32 partials use the run-time rank count");
+    __shared__ const uint4* s_ptr[ARF_MAX_W];
+    __shared__ float s_warp[2][kMaxThreads / 32];
+    prologue(s_ptr, p.lc, p.W);
+    __syncthreads();
+    if constexpr (!F32P) {
+        if (vector_layout(p, s_ptr)) {  // the same answer in every thread of every CTA
+            int it = 0;
+            for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++it) rms_flat_row<T, WS>(p, s_ptr, row, it, s_warp);
+            return;
+        }
+    }
     int it = 0;
     for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++it) {
         float ss = 0.0f;
@@ -304,26 +317,6 @@ __device__ __forceinline__ void rms_elem_rows(const ElemParams& p, const uint4* 
             p.out[row * p.ldo + e] = narrow1<T>(__fmul_rn(__fmul_rn(x, inv), g));
         }
     }
-}
-
-// kARResidualRMSNorm: one CTA per row (rows grid-stride). Tensors whose rows
-// share their 16-byte phase (flat_ok, and every partial pointer aligned) take
-// rms_flat_row, the others rms_elem_rows.
-template <typename T, bool F32P, int WS = 0>
-__global__ void __launch_bounds__(kMaxThreads, 2) rms_elem_kernel(ElemParams p) {
-    static_assert(!F32P || WS == 0, "binary32 partials use the run-time rank count");
-    __shared__ const uint4* s_ptr[ARF_MAX_W];
-    __shared__ float s_warp[2][kMaxThreads / 32];
-    prologue(s_ptr, p.lc, p.W);
-    __syncthreads();
-    if constexpr (!F32P) {
-        if (vector_layout(p, s_ptr)) {  // the same answer in every thread of every CTA
-            int it = 0;
-            for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++it) rms_flat_row<T, WS>(p, s_ptr, row, it, s_warp);
-            return;
-        }
-    }
-    rms_elem_rows<T, F32P>(p, s_ptr, s_warp);
 }
 
 }  // namespace arf

@@ -147,20 +147,6 @@ constexpr size_t bulk_dyn_smem(int W, int stages, int threads, int C) {
 constexpr size_t bulk_ar_dyn_smem(int W, int stages, int threads) {
     return (size_t)stages * (size_t)W * (size_t)threads * 16u;
 }
-// The register row kernel of kARResidualRMSNorm on rows at any 16-byte phase
-// (arf_vrow.cuh, an elementwise-path plan with vpt > 1): the vectors a row of
-// H elements can span at the worst phase (7); its dynamic shared memory
-// (gamma with eight zero elements on either side, in whole 16-byte vectors);
-// whether the instance (W, vectors per thread) exists: W compiled in and a
-// row's loads plus the next row's fitting in registers (vpt * (W + 1) <= 18).
-__host__ __device__ constexpr int64_t vrow_max_vectors(int64_t H) { return (H + 14) / 8; }
-__host__ __device__ constexpr size_t vrow_smem(int64_t H) { return (size_t)((H + 16 + 7) / 8) * 16u; }
-__host__ __device__ constexpr bool vrow_compiled(int ws, int nv) {
-    return (ws == 1 || ws == 2 || ws == 4 || ws == 8) && (nv == 2 || nv == 4 || nv == 8) && nv * (ws + 1) <= 18;
-}
-// Its __shared__ arrays (pointers and warp sums), with the 1 KB the SM keeps.
-constexpr int kVrowStaticSmem = 8 * ARF_MAX_W + 2 * (kMaxThreads / 32) * 4 + 1024;
-
 // Default wait limit of the bulk kernel: 2^31 SM cycles, about a second.
 constexpr long long kBulkSpinLimit = 1ll << 31;
 

@@ -4,7 +4,6 @@
 
 #include "arf_bulk.cuh"
 #include "arf_elem.cuh"
-#include "arf_vrow.cuh"
 
 namespace arf {
 
@@ -254,31 +253,13 @@ ElemFn elem_kernel_for(bool rms, bool f32p, int W) {
     }
 }
 
-// The register row kernel (W compiled in, nv vectors per thread).
-template <typename T>
-ElemFn vrow_kernel_for(int ws, int nv) {
-#define ARF_VROW_CASE(W, N) \
-    if (ws == W && nv == N) return rms_vrow_kernel<T, W, N>;
-    ARF_VROW_CASE(1, 2) ARF_VROW_CASE(1, 4) ARF_VROW_CASE(1, 8)
-    ARF_VROW_CASE(2, 2) ARF_VROW_CASE(2, 4)
-    ARF_VROW_CASE(4, 2)
-    ARF_VROW_CASE(8, 2)
-#undef ARF_VROW_CASE
-    return nullptr;
-}
-
 template <typename T>
 cudaError_t launch_elem_t(const ElemParams& p, const arf_plan_t& plan, bool rms, cudaStream_t s, bool f32p) {
-    // kARResidualRMSNorm plans with vpt > 1: the register row kernel (binary32
-    // partials have no such instance and take the elementwise kernel)
-    const bool vrow = rms && plan.vpt > 1 && !f32p;
-    ElemFn fn = vrow ? vrow_kernel_for<T>(plan.w_spec, plan.vpt) : elem_kernel_for<T>(rms, f32p, p.W);
-    if (!fn) return cudaErrorInvalidValue;
+    ElemFn fn = elem_kernel_for<T>(rms, f32p, p.W);
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.grid);
     cfg.blockDim = dim3((unsigned)plan.threads);
-    cfg.dynamicSmemBytes = vrow ? vrow_smem(p.H) : 0;
     cfg.stream = s;
     if (p.lc.pdl) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -304,12 +285,6 @@ cudaError_t configure_kernels_t(bool clusters, int max_dyn_smem) {
                 }
     for (int ws : ws_list) {
         for (RmsFn fn : {async_kernel_for<T>(ws), bulk_kernel_for<T>(ws), bulk_ar_kernel_for<T>(ws)}) {
-            if (!fn) continue;
-            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
-            if (e != cudaSuccess) return e;
-        }
-        for (int nv : {2, 4, 8}) {
-            ElemFn fn = vrow_kernel_for<T>(ws, nv);
             if (!fn) continue;
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
             if (e != cudaSuccess) return e;

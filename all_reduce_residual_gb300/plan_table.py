@@ -106,19 +106,6 @@ def candidates(caps, pattern, W, H):
                 for per in (1, 2, 4, 8):
                     if per * t <= caps.max_threads_per_sm:
                         out.append((PATH_ELEM, t, 1, 1, 0, 0, GRID_RESIDENT, per))
-        if pattern == "rmsnorm" and ws in (1, 2, 4, 8):
-            # the register row kernel: a row's vectors in registers at any phase
-            need = (H + 14) // 8
-            for nv in (2, 4, 8):
-                if nv * (ws + 1) > 18:
-                    continue
-                t = max(32, -(-(-(-need // nv)) // 32) * 32)
-                if t > MAX_THREADS:
-                    continue
-                out.append((PATH_ELEM, t, nv, 1, ws, 0, GRID_ROWS, 0))
-                for per in (1, 2, 3, 4):
-                    if per * t <= caps.max_threads_per_sm:
-                        out.append((PATH_ELEM, t, nv, 1, ws, 0, GRID_RESIDENT, per))
         return out
     C = H // 8
     if pattern == "allreduce":

@@ -89,11 +89,7 @@ typedef enum arf_path {
                              aligned): 16-byte vectors with per-row heads and
                              tails where every tensor is 16-byte aligned and all
                              row strides agree modulo 8, else one element per
-                             thread per step. With vpt > 1 (kARResidualRMSNorm,
-                             W in {1,2,4,8} compiled in, vpt * (W + 1) <= 18):
-                             the register row kernel, which holds a row's
-                             vectors in registers at any 16-byte phase and
-                             prefetches the next row */
+                             thread per step */
     ARF_PATH_BULK = 5     /* either pattern, 16-bit partials: each CTA walks
                              its rows in column blocks of `threads` chunks;
                              one thread keeps `stages` blocks in flight as TMA
@@ -124,9 +120,8 @@ typedef struct arf_device_caps {
 typedef struct arf_plan {
     int path;     /* arf_path_t */
     int threads;  /* threads per CTA, a multiple of 32 in [32, 512] */
-    int vpt;      /* 16-byte chunks per thread per row (row/cluster paths and
-                     the elementwise path's register row kernel) or chunks
-                     per thread per loop trip (flat path): 1, 2, 4 or 8 */
+    int vpt;      /* 16-byte chunks per thread per row (row/cluster paths) or
+                     chunks per thread per loop trip (flat path): 1, 2, 4 or 8 */
     int cluster;  /* CTAs per row (cluster path: 2, 4, 8 or 16; else 1) */
     int grid;     /* CTAs launched; a multiple of `cluster` */
     int w_spec;   /* rank count compiled into the kernel, or 0 for the generic

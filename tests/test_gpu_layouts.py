@@ -307,93 +307,3 @@ def test_flat_range_needs_contiguous_rows_and_whole_chunks(ws):
         run_case(ws, AR, "bf16", 2, 4, 4098, pads=(8, 0, 8, 0), plan=plan)
     assert e.value.status == arf.ARF_ERR_UNSUPPORTED
     run_case(ws, AR, "bf16", 2, 4, 4098, pads=(8, 0, 8, 0))  # the planner's plan on the strided rows
-
-
-def vrow_plans(ws, W, M, H):
-    """Explicit plans of the register row kernel (elementwise path, vpt > 1)
-    for these sizes: every compiled vectors-per-thread count, with one CTA per
-    row, a resident grid and a single CTA."""
-    caps = ws.caps
-    need = (H + 14) // 8
-    out = []
-    for nv in (2, 4, 8):
-        if W not in (1, 2, 4, 8) or nv * (W + 1) > 18:
-            continue
-        t = max(32, -(-(-(-need // nv)) // 32) * 32)
-        if t > 512:
-            continue
-        for grid in sorted({M, min(M, 2 * caps.num_sms), 1}):
-            p = arf.Plan(path=arf.ARF_PATH_ELEM, threads=t, vpt=nv, cluster=1, grid=grid, w_spec=W, stages=0)
-            assert arf.arf_plan_check(caps, p, RMS, W, M, H, arf.ARF_BF16) == arf.ARF_OK, p
-            out.append(p)
-    return out
-
-
-@pytest.mark.parametrize("W,M,H", [(2, 37, 4098), (1, 9, 1), (4, 11, 7), (8, 5, 13), (2, 13, 1001), (1, 8, 7170),
-                                   (4, 33, 4099), (8, 6, 7175), (2, 5, 8), (1, 19, 4096), (1, 3, 32760)])
-@pytest.mark.parametrize("pads", [(0, 0, 0, 0), (3, 3, 3, 3), (11, 3, 19, 27), (1, 2, 3, 4)])
-def test_register_row_kernel(ws, W, M, H, pads):
-    """kARResidualRMSNorm on the register row kernel against the oracle:
-    rows at every 16-byte phase (contiguous odd H; strides congruent modulo 8),
-    and strides that are not congruent (pads (1, 2, 3, 4)), which the kernel
-    hands to its elementwise rows."""
-    plans = vrow_plans(ws, W, M, H)
-    assert plans
-    for i, plan in enumerate(plans):
-        run_case(ws, RMS, "fp16" if (M + i) % 3 == 0 else "bf16", W, M, H, pads=pads, plan=plan, seed=H + i)
-
-
-@pytest.mark.parametrize("W", [1, 2, 8])
-def test_register_row_kernel_in_place_and_gamma_offset(ws, W):
-    """residual_out == residual, and gamma at a 2-byte offset, on the register
-    row kernel (H = 4098, every phase), against the oracle."""
-    from gpu_util import oracle_run, to_device
-    M, H = 300, 4098
-    inp = wl.make_inputs(wl.custom(W, M, H, "bf16", 0.7, 1e-6, config_id=4200 + W))
-    P, R, G = to_device(inp)
-    gbuf = torch.zeros(H + 8, dtype=torch.int16, device="cuda")
-    Gd = gbuf[1:1 + H].view(torch.bfloat16)
-    Gd.copy_(G)
-    for plan in vrow_plans(ws, W, M, H):
-        buf = R.clone()
-        out, ro = arf.run(ws, RMS, P, buf, Gd, inp.workload.eps, residual_out=buf, plan=plan)
-        torch.cuda.synchronize()
-        got = (wl.codes(out.cpu()), wl.codes(ro.cpu()))
-        assert_parity(DT["bf16"], RMS, got, oracle_run(RMS, inp), f"W={W} plan={plan}")
-
-
-def test_register_row_kernel_unaligned_partial(ws):
-    """A partial at a 2-byte offset: the register row kernel finds it and runs
-    its elementwise rows instead; the result still matches the oracle."""
-    M, H, W = 17, 4098, 2
-    rng = np.random.default_rng(17)
-    P = [codes_of(rng, oracle.BF16, (M, H), 1.0) for _ in range(W)]
-    R = codes_of(rng, oracle.BF16, (M, H), 1.0)
-    G = pins.nearest_codes(oracle.BF16, 0.5 + rng.random(H))
-    buf = torch.zeros(M * H + 16, dtype=torch.int16, device="cuda")
-    P0 = buf[1:1 + M * H].view(torch.bfloat16).view(M, H)
-    P0.copy_(wl.from_codes(P[0], "bf16").cuda())
-    Pd = [P0, wl.from_codes(P[1], "bf16").cuda()]
-    Rd, Gd = wl.from_codes(R, "bf16").cuda(), wl.from_codes(G, "bf16").cuda()
-    for plan in vrow_plans(ws, W, M, H):
-        out, ro = arf.run(ws, RMS, Pd, Rd, Gd, 1e-6, plan=plan)
-        torch.cuda.synchronize()
-        ref = oracle.run(oracle.AR_RESIDUAL_RMSNORM, P, R, G, 1e-6, dtype=oracle.BF16)
-        assert_parity(oracle.BF16, RMS, (host_codes(out), host_codes(ro)), ref, f"plan={plan}")
-
-
-def test_register_row_plan_rules(ws):
-    """Plans the register row kernel cannot take are refused."""
-    caps = ws.caps
-    ok = arf.Plan(path=arf.ARF_PATH_ELEM, threads=288, vpt=2, cluster=1, grid=4, w_spec=2, stages=0)
-    assert arf.arf_plan_check(caps, ok, RMS, 2, 4, 4098, arf.ARF_BF16) == arf.ARF_OK
-    bad = [dict(threads=256),                  # 256 x 2 vectors cannot cover a 514-vector row
-           dict(w_spec=0),                     # the rank count must be compiled in
-           dict(vpt=8),                        # 8 x (2 + 1) > 18 vectors in registers
-           dict(vpt=3)]
-    for change in bad:
-        p = arf.Plan(**{**{k: getattr(ok, k) for k, _ in arf.Plan._fields_}, **change})
-        assert arf.arf_plan_check(caps, p, RMS, 2, 4, 4098, arf.ARF_BF16) == arf.ARF_ERR_UNSUPPORTED, change
-    assert arf.arf_plan_check(caps, ok, AR, 2, 4, 4098, arf.ARF_BF16) == arf.ARF_ERR_UNSUPPORTED  # RMS only
-    w12 = arf.Plan(path=arf.ARF_PATH_ELEM, threads=288, vpt=2, cluster=1, grid=4, w_spec=12, stages=0)
-    assert arf.arf_plan_check(caps, w12, RMS, 12, 4, 4098, arf.ARF_BF16) == arf.ARF_ERR_UNSUPPORTED
