@@ -329,17 +329,17 @@ def run_arf(args):
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kname,
                 "algorithmic_bytes_per_launch": bytes_call[dom],
                 "peak_source": f"{peak_src} hbm_gbs (copy)",
-                "frac_basis": "cold: mean event time per launch in the timed steps",
+                "frac_basis": "cold, mean event time per launch",
                 "steady_frac": round(bytes_call[dom] / (steady_us * 1e-6) / 1e9 / peak, 4),
                 "steady_us": round(steady_us, 3),
-                "steady_basis": "graph of 20 back-to-back launches; each pays the L2 write-backs of the last",
+                "steady_basis": "graph of 20 back-to-back launches",
                 "dram_over_algorithmic": round(traffic / bytes_call[dom], 4) if traffic else None}
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(statistics.mean(step_ms), 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded N(0,s) partials, residual N(0,1), gamma U(0.5,1.5), rounded to the I/O dtype)",
+        "data": "synthetic: seeded N(0,s) partials, N(0,1) residual, U(0.5,1.5) gamma",
         "config": {"workload": f"{w.name}: W={w.W} M={w.M} H={w.H} {w.dtype}, one {' + one '.join(pats)} call per step",
                    "W": w.W, "M": w.M, "H": w.H, "io_dtype": w.dtype, "accumulate": "f32",
                    "bytes_per_step": step_bytes, "l2": flush.describe(), "parallelism": f"replicas x{world}",
@@ -511,7 +511,7 @@ def roofline_context(ws, dev, flush, w, pattern, call_ms):
     copy_us = cold_event_us(lambda: dst.copy_(src), flush, stream)
     read_us = cold_event_us(read_pass, flush, stream)
     call_us = statistics.mean(call_ms) * 1e3
-    return {"pattern": pattern, "call_us": round(call_us, 3), "copy_same_bytes_us": round(copy_us, 3),
+    return {"call_us": round(call_us, 3), "copy_same_bytes_us": round(copy_us, 3),
             "read_only_pass_same_reads_us": round(read_us, 3),
             "call_over_read_only": round(call_us / read_us, 3)}
 
