@@ -1,10 +1,12 @@
 // arf_api.cu: the C ABI of include/arf.h: validation, launch planning,
 // dispatch, and the host-buffer entry point.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <climits>
+#include <initializer_list>
 #include <cstring>
 #include <map>
 #include <vector>
@@ -28,6 +30,13 @@ struct arf_workspace {
     // error the lookup returned.
     void* static_staging = nullptr;
     cudaError_t static_staging_err = cudaErrorInvalidValue;
+    // arf_run_host's pipelined form: a stream for the host-to-device copies
+    // and one for the device-to-host copies, forked from and joined back into
+    // the caller's stream with the events; host_mu keeps one call's records
+    // and waits from interleaving with another's.
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_in = nullptr, ev_done = nullptr, ev_join = nullptr;
+    std::mutex host_mu;
 };
 
 namespace {
@@ -147,6 +156,20 @@ extern "C" const char* arf_status_string(arf_status_t s) {
     return "unknown status";
 }
 
+namespace {
+
+// Free what a workspace holds on its device (the current device).
+void release_device_resources(arf_workspace* ws) {
+    if (ws->wait_timeouts) (void)cudaFree(ws->wait_timeouts);
+    ws->wait_timeouts = nullptr;
+    for (cudaStream_t* st : {&ws->h2d, &ws->d2h})
+        if (*st) (void)cudaStreamDestroy(*st), *st = nullptr;
+    for (cudaEvent_t* ev : {&ws->ev_fork, &ws->ev_in, &ws->ev_done, &ws->ev_join})
+        if (*ev) (void)cudaEventDestroy(*ev), *ev = nullptr;
+}
+
+}  // namespace
+
 extern "C" arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out) {
     if (!ws_out) return ARF_ERR_INVALID_ARG;
     *ws_out = nullptr;
@@ -168,8 +191,12 @@ extern "C" arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out
     }
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&ws->wait_timeouts), 256);
     if (e == cudaSuccess) e = cudaMemset(ws->wait_timeouts, 0, 256);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ws->h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ws->d2h, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&ws->ev_fork, &ws->ev_in, &ws->ev_done, &ws->ev_join})
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) {
-        if (ws->wait_timeouts) (void)cudaFree(ws->wait_timeouts);
+        release_device_resources(ws);
         delete ws;
         (void)cudaGetLastError();
         return ARF_ERR_CUDA;
@@ -228,7 +255,7 @@ extern "C" arf_status_t arf_workspace_destroy(arf_workspace_t ws) {
         int cur = -1;
         const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != ws->device &&
                               cudaSetDevice(ws->device) == cudaSuccess;
-        (void)cudaFree(ws->wait_timeouts);
+        release_device_resources(ws);
         if (switched) (void)cudaSetDevice(cur);
         (void)cudaGetLastError();
     }
@@ -1171,6 +1198,89 @@ Staging staging_layout(arf_pattern_t pattern, int W, int64_t M, int64_t H) {
 
 }  // namespace
 
+namespace {
+
+// Row blocks of arf_run_host's pipelined form: one per 4 MiB of an [M,H]
+// tensor, at most 8; 1 = the plain form (copies in, kernel, copies out, all
+// on the caller's stream). Host-to-device and device-to-host copies run at
+// once only on separate streams; on GB300 (pinned memory over NVLink-C2C)
+// one direction moves about 200 GB/s whatever the number of streams, both
+// directions together 250-270 GB/s.
+int host_pipeline_blocks(int64_t M, int64_t H) {
+    const int64_t plane = M * H * 2;
+    const int64_t b = plane / (4ll << 20);
+    return (int)std::min<int64_t>(std::min<int64_t>(b, 8), M);
+}
+
+// Pipelined arf_run_host over `blocks` blocks of rows: block b's inputs are
+// copied in on ws->h2d, its kernel runs on the caller's stream once they have
+// landed, and its outputs are copied out on ws->d2h, so block b's outputs
+// travel while block b+1's inputs do. The kernels take the partial pointers
+// by value (each block's pointers are offsets into the staging planes). Both
+// copy streams start after the caller's earlier work (ev_fork) and the
+// caller's stream waits for the last copy out (ev_join), so the call is
+// ordered with other work on `stream` as the plain form is, under stream
+// capture too.
+arf_status_t run_host_pipelined(arf_workspace_t ws, arf_pattern_t pattern, int W, const void* const* partials_host,
+                                const void* residual_host, const void* gamma_host, float eps, void* out_host,
+                                void* residual_out_host, int64_t M, int64_t H, arf_dtype_t dtype, char* base,
+                                const Staging& L, int blocks, cudaStream_t stream) {
+    const bool rms = pattern == ARF_AR_RESIDUAL_RMSNORM;
+    const size_t row = (size_t)H * 2;
+    const int64_t rows_per = ceil_div(M, blocks);
+    std::lock_guard<std::mutex> lock(ws->host_mu);
+    cudaError_t e = cudaEventRecord(ws->ev_fork, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ws->h2d, ws->ev_fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ws->d2h, ws->ev_fork, 0);
+    if (rms && e == cudaSuccess)
+        e = cudaMemcpyAsync(base + L.gamma, gamma_host, row, cudaMemcpyHostToDevice, ws->h2d);
+    arf_run_opts_t opts = {};
+    opts.partials_by_value = 1;
+    opts.pdl = 2;  // each kernel follows an event wait: nothing to overlap
+    const void* ptrs[ARF_MAX_W];
+    arf_status_t st = ARF_OK;
+    for (int64_t r0 = 0; r0 < M && e == cudaSuccess && st == ARF_OK; r0 += rows_per) {
+        const int64_t mb = std::min<int64_t>(rows_per, M - r0);
+        const size_t off = (size_t)r0 * row, nb = (size_t)mb * row;
+        for (int r = 0; r < W && e == cudaSuccess; ++r) {
+            char* dst = base + L.p0 + (size_t)r * L.plane + off;
+            e = cudaMemcpyAsync(dst, static_cast<const char*>(partials_host[r]) + off, nb, cudaMemcpyHostToDevice,
+                                ws->h2d);
+            ptrs[r] = dst;
+        }
+        if (rms && e == cudaSuccess)
+            e = cudaMemcpyAsync(base + L.residual + off, static_cast<const char*>(residual_host) + off, nb,
+                                cudaMemcpyHostToDevice, ws->h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(ws->ev_in, ws->h2d);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ws->ev_in, 0);
+        if (e != cudaSuccess) break;
+        st = run_impl(ws, &opts, pattern, W, ptrs, rms ? base + L.residual + off : nullptr,
+                      rms ? base + L.gamma : nullptr, eps, base + L.out + off,
+                      rms ? base + L.residual_out + off : nullptr, mb, H, dtype, stream);
+        if (st != ARF_OK) break;
+        e = cudaEventRecord(ws->ev_done, stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ws->d2h, ws->ev_done, 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<char*>(out_host) + off, base + L.out + off, nb, cudaMemcpyDeviceToHost,
+                                ws->d2h);
+        if (rms && e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<char*>(residual_out_host) + off, base + L.residual_out + off, nb,
+                                cudaMemcpyDeviceToHost, ws->d2h);
+    }
+    // Join both copy streams back into the caller's stream, also after a
+    // failure part-way, so that no capture is left with an unjoined stream.
+    cudaError_t j = cudaEventRecord(ws->ev_join, ws->h2d);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(stream, ws->ev_join, 0);
+    if (j == cudaSuccess) j = cudaEventRecord(ws->ev_join, ws->d2h);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(stream, ws->ev_join, 0);
+    if (e == cudaSuccess) e = j;
+    if (st != ARF_OK) return st;
+    if (e != cudaSuccess) return cuda_fail(ws, e);
+    return ARF_OK;
+}
+
+}  // namespace
+
 extern "C" size_t arf_host_staging_bytes(arf_pattern_t pattern, int W, int64_t M, int64_t H, arf_dtype_t dtype) {
     if (arf_supports(nullptr, pattern, W, M, H, dtype) != ARF_OK) return 0;
     return staging_layout(pattern, W, M, H).total;
@@ -1204,6 +1314,10 @@ extern "C" arf_status_t arf_run_host(arf_workspace_t ws, arf_pattern_t pattern, 
 
     char* base = static_cast<char*>(staging_dev);
     const size_t bytes = (size_t)M * (size_t)H * 2;
+    const int blocks = host_pipeline_blocks(M, H);
+    if (blocks > 1)
+        return run_host_pipelined(ws, pattern, W, partials_host, residual_host, gamma_host, eps, out_host,
+                                  residual_out_host, M, H, dtype, base, L, blocks, stream);
     cudaError_t e = arf::launch_fill_pointer_array(reinterpret_cast<const void**>(base + L.ptrs), base + L.p0,
                                                    (int64_t)L.plane, W, stream);
     for (int r = 0; r < W && e == cudaSuccess; ++r)

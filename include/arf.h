@@ -358,9 +358,22 @@ size_t arf_host_staging_bytes(arf_pattern_t pattern, int W, int64_t M, int64_t H
                               arf_dtype_t dtype);
 
 /* The epilogue on HOST buffers: copies the inputs to `staging_dev`, runs
- * the pattern there and copies the outputs back, all enqueued on `stream`
+ * the pattern there and copies the outputs back, all ordered on `stream`
  * (returns before they finish; synchronise the stream before reading the
  * outputs). Copies overlap other work only from page-locked host memory.
+ *
+ * Tensors of 8 MiB or more are pipelined in blocks of rows (one per 4 MiB,
+ * at most 8): a block's inputs are copied in on a stream of the workspace,
+ * its kernel runs on `stream` once they have landed, and its outputs are
+ * copied out on a second stream of the workspace while later blocks' inputs
+ * are still coming in. Both copy streams start after the work enqueued on
+ * `stream` before the call, and `stream` waits for the last copy out (event
+ * fork and join), so the call is ordered with other work on `stream` as a
+ * single-stream call would be, under stream capture too. Calls on one
+ * workspace are enqueued one at a time (the workspace holds a lock while
+ * enqueuing) and share its copy streams. Rows of different blocks never
+ * alias, so residual_out_host may be residual_host and out_host may be one
+ * of the partials' buffers, as in the single-stream form.
  *
  *   partials_host  HOST array of W host pointers, each to an [M,H] tensor
  *   residual_host, gamma_host, out_host, residual_out_host: host buffers with

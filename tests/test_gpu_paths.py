@@ -375,6 +375,77 @@ def test_host_buffer_entry_point(ws, name, pattern, pinned):
         assert_parity(DT[w.dtype], pattern, got, oracle_run(pattern, inp))
 
 
+# Tensors of 8 MiB and more take arf_run_host's pipelined form (one row block
+# per 4 MiB, at most 8): W = 4, M = 1501 gives 5 blocks of 301 rows, the last
+# of 297; tp16_8mib's shape 2 blocks (293 and 292 rows).
+PIPELINED = [(4, 1501, 7168, "bf16", 0.7), (16, 585, 7168, "fp16", 0.1)]
+
+
+@pytest.mark.parametrize("W,M,H,dtype,sigma", PIPELINED)
+def test_host_buffer_pipelined(ws, W, M, H, dtype, sigma):
+    """The pipelined host-buffer form (copies on the workspace's two copy
+    streams, kernels per row block on the caller's stream): both patterns
+    match the oracle, twice in a row, on a side stream, in place (residual_out
+    is the residual buffer) and with out written over the first partial."""
+    inp = inputs(W, M, H, dtype, sigma=sigma, cid=910)
+    d = DT[dtype]
+    tdt = wl.TORCH_DTYPE[dtype]
+    P = [p.pin_memory() for p in inp.partials]
+    R, G = inp.residual.pin_memory(), inp.gamma.pin_memory()
+    side = torch.cuda.Stream()
+    for pat in (AR, RMS):
+        ref = oracle_run(pat, inp)
+        out = torch.empty_like(R).pin_memory()
+        ro = torch.empty_like(R).pin_memory()
+        runner = arf.HostRunner(ws, pat, W, M, H, tdt)
+        for k in range(2):
+            out.fill_(0)
+            ro.fill_(0)
+            runner(P, R, G, 1e-6, out, ro, stream=side)
+            side.synchronize()
+            got = (wl.codes(out), wl.codes(ro) if pat == RMS else None)
+            assert_parity(d, pat, got, ref, f"pipelined call {k}")
+    # in place: residual_out written over the residual's host buffer
+    Rin = inp.residual.clone().pin_memory()
+    out = torch.empty_like(R).pin_memory()
+    arf.HostRunner(ws, RMS, W, M, H, tdt)(P, Rin, G, 1e-6, out, Rin)
+    torch.cuda.synchronize()
+    assert_parity(d, RMS, (wl.codes(out), wl.codes(Rin)), oracle_run(RMS, inp), "pipelined in place")
+    # kAllReduce into the first partial's host buffer
+    P2 = [p.clone().pin_memory() for p in inp.partials]
+    arf.HostRunner(ws, AR, W, M, H, tdt)(P2, None, None, 0.0, P2[0], None)
+    torch.cuda.synchronize()
+    assert_parity(d, AR, (wl.codes(P2[0]), None), oracle_run(AR, inp), "pipelined out = partial 0")
+
+
+def test_host_buffer_pipelined_graph(ws):
+    """The pipelined form captured into a CUDA graph (its copy streams fork
+    from and join back into the capturing stream) and replayed."""
+    W, M, H = 4, 1501, 7168
+    inp = inputs(W, M, H, sigma=0.7, cid=911)
+    P = [p.pin_memory() for p in inp.partials]
+    R, G = inp.residual.pin_memory(), inp.gamma.pin_memory()
+    out = torch.empty_like(R).pin_memory()
+    ro = torch.empty_like(R).pin_memory()
+    runner = arf.HostRunner(ws, RMS, W, M, H, torch.bfloat16)
+    runner(P, R, G, 1e-6, out, ro)  # plans the block shapes outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            runner(P, R, G, 1e-6, out, ro, stream=s)
+    torch.cuda.synchronize()
+    ref = oracle_run(RMS, inp)
+    for k in range(2):
+        out.fill_(0)
+        ro.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert_parity(oracle.BF16, RMS, (wl.codes(out), wl.codes(ro)), ref, f"graph replay {k}")
+
+
 @pytest.mark.parametrize("by_value,pdl", [(True, False), (False, True), (True, True)])
 @pytest.mark.parametrize("W,M,H", [(8, 1, 7168), (2, 128, 4096), (8, 300, 7168), (17, 5, 264)])
 @pytest.mark.parametrize("pattern", [AR, RMS])
