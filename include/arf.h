@@ -143,6 +143,8 @@ typedef struct arf_workspace* arf_workspace_t;
  * Makes `device` current on the calling thread. Allocates the workspace's
  * only device memory here: 256 bytes holding the bulk kernel's wait-timeout
  * counter (arf_workspace_wait_timeouts); no later call allocates for it.
+ * Also creates the two non-blocking streams and four events of
+ * arf_run_host's pipelined form; arf_workspace_destroy releases them all.
  * Errors: ws_out NULL -> INVALID_ARG; no such device or a CUDA failure -> CUDA. */
 arf_status_t arf_workspace_create(int device, arf_workspace_t* ws_out);
 
