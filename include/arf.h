@@ -38,9 +38,10 @@
  * Ownership. The caller owns every tensor and the pointer array; they must
  * stay valid until the stream work completes. The library keeps no tensor
  * pointer after a call returns. A workspace owns host state (device id, SM
- * count, cluster limits, plan cache) and one 256-byte device word, the bulk
- * kernel's wait-timeout counter, allocated at creation and freed at
- * destruction; no call allocates device memory.
+ * count, cluster limits, plan cache), one 256-byte device word, the bulk
+ * kernel's wait-timeout counter, and two copy streams with four events for
+ * arf_run_host, all made at creation and released at destruction; no call
+ * allocates device memory.
  *
  * Errors. Every entry point returns a status and never throws. On any error
  * nothing is launched and no output is written.
