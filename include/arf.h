@@ -301,10 +301,16 @@ typedef struct arf_run_opts {
                                 pointers (as arf_run). 1: `partials` is a HOST
                                 array of W device pointers; the values are
                                 copied into the kernel launch, so the kernel
-                                reads no pointer array (one dependent memory
-                                round trip less); a captured graph keeps the
-                                values, and the host array may be reused as
-                                soon as the call returns. */
+                                reads no pointer array; a captured graph keeps
+                                the values, and the host array may be reused
+                                as soon as the call returns. Not faster: on
+                                GB300 at decode sizes (W = 8, H = 7168,
+                                M = 1..64) the launch's larger parameter block
+                                (room for ARF_MAX_W pointers) costs more than
+                                the pointer-array read it saves: cold level or
+                                up to 0.8 us slower, warm in CUDA graphs
+                                0.1-0.4 us slower. It is for callers that have
+                                no device pointer array. */
     int pdl;                 /* programmatic dependent launch: the kernel may
                                 be scheduled while the previous kernel in the
                                 stream still runs, and waits
