@@ -1227,7 +1227,9 @@ arf_status_t run_host_pipelined(arf_workspace_t ws, arf_pattern_t pattern, int W
                                 const Staging& L, int blocks, cudaStream_t stream) {
     const bool rms = pattern == ARF_AR_RESIDUAL_RMSNORM;
     const size_t row = (size_t)H * 2;
-    const int64_t rows_per = ceil_div(M, blocks);
+    // whole multiples of 8 rows, so that every block starts on a 16-byte
+    // boundary whatever H (the 16-byte kernels then take every block)
+    const int64_t rows_per = ceil_div(ceil_div(M, blocks), 8) * 8;
     std::lock_guard<std::mutex> lock(ws->host_mu);
     cudaError_t e = cudaEventRecord(ws->ev_fork, stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ws->h2d, ws->ev_fork, 0);

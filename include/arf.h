@@ -372,7 +372,8 @@ size_t arf_host_staging_bytes(arf_pattern_t pattern, int W, int64_t M, int64_t H
  * outputs). Copies overlap other work only from page-locked host memory.
  *
  * Tensors of 8 MiB or more are pipelined in blocks of rows (one per 4 MiB,
- * at most 8): a block's inputs are copied in on a stream of the workspace,
+ * at most 8; rows per block a multiple of 8, so that each block starts on a
+ * 16-byte boundary for any H): a block's inputs are copied in on a stream of the workspace,
  * its kernel runs on `stream` once they have landed, and its outputs are
  * copied out on a second stream of the workspace while later blocks' inputs
  * are still coming in. Both copy streams start after the work enqueued on

@@ -376,9 +376,11 @@ def test_host_buffer_entry_point(ws, name, pattern, pinned):
 
 
 # Tensors of 8 MiB and more take arf_run_host's pipelined form (one row block
-# per 4 MiB, at most 8): W = 4, M = 1501 gives 5 blocks of 301 rows, the last
-# of 297; tp16_8mib's shape 2 blocks (293 and 292 rows).
-PIPELINED = [(4, 1501, 7168, "bf16", 0.7), (16, 585, 7168, "fp16", 0.1)]
+# per 4 MiB, at most 8, rows per block rounded up to a multiple of 8): W = 4,
+# M = 1501 gives 5 blocks of 304 rows, the last of 285; tp16_8mib's shape 2
+# blocks (296 and 289 rows); H = 4098 (not a multiple of 8) 2 blocks of 552
+# and 548 rows.
+PIPELINED = [(4, 1501, 7168, "bf16", 0.7), (16, 585, 7168, "fp16", 0.1), (2, 1100, 4098, "bf16", 0.5)]
 
 
 @pytest.mark.parametrize("W,M,H,dtype,sigma", PIPELINED)
