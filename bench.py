@@ -61,6 +61,8 @@ def parse():
                     help="accepted for older command lines; the sweep runs only with --sweep-out")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the cold per-call fractions of the other configurations of 8 MiB and more")
     ap.add_argument("--m", type=int, default=None, help="override the workload's row count M (for profiling)")
     ap.add_argument("--pattern", choices=PATTERNS, default=None,
                     help="time only this pattern of the workload (for profiling one kernel)")
@@ -329,10 +331,10 @@ def run_arf(args):
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kname,
                 "algorithmic_bytes_per_launch": bytes_call[dom],
                 "peak_source": f"{peak_src} hbm_gbs (copy)",
-                "frac_basis": "cold, mean event time per launch",
+                "frac_basis": "cold mean per launch",
                 "steady_frac": round(bytes_call[dom] / (steady_us * 1e-6) / 1e9 / peak, 4),
                 "steady_us": round(steady_us, 3),
-                "steady_basis": "graph of 20 back-to-back launches",
+                "steady_basis": "20 back-to-back in a graph",
                 "dram_over_algorithmic": round(traffic / bytes_call[dom], 4) if traffic else None}
 
     result = {
@@ -341,21 +343,23 @@ def run_arf(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic: seeded N(0,s) partials, N(0,1) residual, U(0.5,1.5) gamma",
         "config": {"workload": f"{w.name}: W={w.W} M={w.M} H={w.H} {w.dtype}, one {' + one '.join(pats)} call per step",
-                   "W": w.W, "M": w.M, "H": w.H, "io_dtype": w.dtype, "accumulate": "f32",
+                   "W": w.W, "M": w.M, "H": w.H, "io_dtype": w.dtype,
                    "bytes_per_step": step_bytes, "l2": flush.describe(), "parallelism": f"replicas x{world}",
                    "plans": {p: plan_str(plans[p]) for p in pats},
-                   "plan_source": "explicit (--plan)" if plan is not None else "planner"},
+                   **({"plan_source": "explicit (--plan)"} if plan is not None else {})},
         "us_per_call": {p: round(statistics.mean(v) * 1e3, 3) for p, v in per_call.items()},
         "frac_per_call": {p: round(bytes_call[p] / (statistics.mean(v) * 1e-3) / 1e9 / peak, 4)
                           for p, v in per_call.items()},
         "roofline": roofline,
         "gpu_launches": len(pats) * K,
         "clocks": {**clk.summary(),
-                   "window": "warm-up and timed steps" + (", then untimed steps to 1 s" if t_timed < 1.0 else "")},
+                   "window": "warm-up, timed" + (", padded to 1 s" if t_timed < 1.0 else "")},
     }
     if not args.no_e2e:
         result["e2e"] = e2e_leg(ws, w, inp, pats, flush, dev, K, world)
     result["roofline_context"] = roofline_context(ws, dev, flush, w, dom, per_call[dom])
+    if world == 1 and not args.no_configs and args.m is None and plan is None:
+        result["frac_other_configs"] = other_configs(ws, dev, flush, peak, skip=w.name)
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(w, inp, budget_s=10.0)
     if args.sweep_out and world == 1:  # the scaling runs (N > 1) time the headline only
@@ -512,8 +516,51 @@ def roofline_context(ws, dev, flush, w, pattern, call_ms):
     read_us = cold_event_us(read_pass, flush, stream)
     call_us = statistics.mean(call_ms) * 1e3
     return {"call_us": round(call_us, 3), "copy_same_bytes_us": round(copy_us, 3),
-            "read_only_pass_same_reads_us": round(read_us, 3),
-            "call_over_read_only": round(call_us / read_us, 3)}
+            "read_only_pass_same_reads_us": round(read_us, 3)}
+
+
+# The configurations of 8 MiB and more per partial besides the headline's,
+# with the M values the 80 % target covers: k3_tp8 at M = 1024 and 2048
+# (14 and 28 MiB per partial), tp4_80mib and tp16_8mib (8 MiB, fp16).
+OTHER_CONFIGS = (("k3_tp8", 1024), ("k3_tp8", 2048), ("tp4_80mib", None), ("tp16_8mib", None))
+
+
+def other_configs(ws, dev, flush, peak, skip):
+    """Cold per-call fraction of the measured copy rate for each pattern of
+    the other 8 MiB+ configurations, timed like the headline's calls (clean
+    L2 flush and a random 0-2 us spin before each call; mean of 50). The
+    first calls on freshly made inputs read slower (tp16_8mib: 39.6 us over
+    its first 20 cold calls, 29.5 us after), so each pattern is first run 30
+    times, each time after a flush."""
+    import torch
+
+    import all_reduce_residual_gb300 as arf
+    from all_reduce_residual_gb300 import workloads as wl
+
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for name, M in OTHER_CONFIGS:
+        if name == skip:
+            continue
+        w = wl.WORKLOADS[name].with_m(M) if M else wl.WORKLOADS[name]
+        inp = wl.make_inputs(w, device=dev)
+        P, R, G = inp.partials, inp.residual, inp.gamma
+        ptrs = arf.pointer_array(P, dev)
+        o, ro = torch.empty_like(R), torch.empty_like(R)
+        key = f"{name} M={w.M}"
+        out[key] = {}
+        for pat in w.patterns:
+            def fn():
+                arf.run(ws, pat, P, R, G, w.eps, out=o, residual_out=ro if pat == "rmsnorm" else None, ptrs=ptrs)
+
+            for _ in range(30):
+                flush.zero_()
+                fn()
+            us = cold_event_us(fn, flush, stream)
+            out[key]["ar" if pat == "allreduce" else "rms"] = round(w.bytes_per_call(pat) / us / 1e3 / peak, 4)
+        del inp, P, R, G, ptrs, o, ro
+        torch.cuda.empty_cache()
+    return out
 
 
 def sweep(ws, dev, flush, peak):
