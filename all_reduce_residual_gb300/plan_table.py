@@ -229,6 +229,13 @@ def main():
                                 plan=pl)
                     return f
 
+                # The first cold calls on freshly made inputs read slower (on
+                # GB300, W = 16 fp16 M = 585: 39.6 us over the first 20, 29.5
+                # us after): warm up on the library's plan before scoring.
+                warm = runner(lib_plan)
+                for _ in range(30):
+                    flush()
+                    warm()
                 scored = []
                 for c, pl in cands:
                     f = runner(pl)
