@@ -420,6 +420,47 @@ def test_host_buffer_pipelined(ws, W, M, H, dtype, sigma):
     assert_parity(d, AR, (wl.codes(P2[0]), None), oracle_run(AR, inp), "pipelined out = partial 0")
 
 
+def test_host_buffer_pipelined_two_threads(ws):
+    """Two host threads drive pipelined calls on one workspace, each on its
+    own stream with its own staging and buffers: the workspace's shared copy
+    streams and events must not mix one call's ordering with the other's."""
+    import threading
+
+    shapes = [(4, 1501, 7168, 0.7, 912), (2, 2400, 4096, 0.5, 913)]
+    results, errors = {}, []
+
+    def worker(k, W, M, H, sigma, cid):
+        try:
+            inp = inputs(W, M, H, sigma=sigma, cid=cid)
+            P = [p.pin_memory() for p in inp.partials]
+            R, G = inp.residual.pin_memory(), inp.gamma.pin_memory()
+            out = torch.empty_like(R).pin_memory()
+            ro = torch.empty_like(R).pin_memory()
+            runner = arf.HostRunner(ws, RMS, W, M, H, torch.bfloat16)
+            s = torch.cuda.Stream()
+            got = []
+            for _ in range(3):
+                out.fill_(0)
+                ro.fill_(0)
+                runner(P, R, G, 1e-6, out, ro, stream=s)
+                s.synchronize()
+                got.append((wl.codes(out).copy(), wl.codes(ro).copy()))
+            results[k] = (inp, got)
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(k, *sh)) for k, sh in enumerate(shapes)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for k, (inp, got) in results.items():
+        ref = oracle_run(RMS, inp)
+        for i, g in enumerate(got):
+            assert_parity(oracle.BF16, RMS, g, ref, f"thread {k} call {i}")
+
+
 def test_host_buffer_pipelined_graph(ws):
     """The pipelined form captured into a CUDA graph (its copy streams fork
     from and join back into the capturing stream) and replayed."""
