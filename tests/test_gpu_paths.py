@@ -133,6 +133,17 @@ def test_ragged_and_extreme_shapes(ws, M, H, pattern):
         assert ws.plan(RMS, 4, M, H, torch.bfloat16).path == arf.ARF_PATH_BULK
 
 
+@pytest.mark.parametrize("W,M,H,dtype", [(64, 2, 524288, "bf16"), (64, 300, 7168, "fp16"), (64, 1, 524288, "fp16"),
+                                         (1, 3, 524288, "bf16")])
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_maximum_sizes(ws, pattern, W, M, H, dtype):
+    """The build's limits together: ARF_MAX_W ranks, rows of ARF_MAX_H
+    elements (split over the largest cluster or the elementwise path), and
+    the generic rank count over many rows."""
+    assert W <= arf.ARF_MAX_W and H <= arf.ARF_MAX_H
+    check(ws, pattern, inputs(W, M, H, dtype, sigma=0.2), what=f"W={W} M={M} H={H} {dtype}")
+
+
 def test_zero_rows_launch_nothing(ws):
     P = [torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     out = torch.full((16,), 7, dtype=torch.int16, device="cuda")
