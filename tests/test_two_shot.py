@@ -111,3 +111,61 @@ def test_one_rank_on_the_gpu_matches_the_oracle(pattern):
     pat = arf.pattern_code(pattern)
     got = (wl.codes(out.cpu()), wl.codes(ro.cpu()) if ro is not None else None)
     assert_parity(GDT["bf16"], pat, got, oracle_run(pat, inp), f"two_shot G=1 {pattern}")
+
+
+def _gpu_rank(rank, world, port, cases, q):
+    """One rank of the two-shot form whose local step is the library's kernels
+    on cuda:0; the exchange is gloo on host tensors. The ranks' kernels never
+    wait on one another: each runs its own block to completion."""
+    import torch.distributed as dist
+
+    import all_reduce_residual_gb300 as arf
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ws = arf.Workspace(0)
+
+    def gpu_step(pattern, partials, residual, gamma, eps):
+        out, ro = arf.run(ws, pattern, [p.cuda() for p in partials], None if residual is None else residual.cuda(),
+                          None if gamma is None else gamma.cuda(), eps)
+        torch.cuda.synchronize()
+        return out.cpu(), None if ro is None else ro.cpu()
+
+    try:
+        for W, M, H, dtype, pattern in cases:
+            w = wl.custom(W, M, H, dtype, 0.7, 1e-6, config_id=980 + M)
+            inp = wl.make_inputs(w)
+            out, ro = ts.two_shot(pattern, inp.partials[rank], inp.residual, inp.gamma, w.eps, epilogue=gpu_step)
+            q.put((rank, (W, M, H, dtype, pattern), wl.codes(out), None if ro is None else wl.codes(ro)))
+    finally:
+        ws.close()
+        dist.destroy_process_group()
+
+
+@pytest.mark.gpu
+def test_two_ranks_with_the_library_epilogue_on_one_gpu():
+    """G = 2 through gloo, each rank's block on the library's kernels: every
+    rank ends with the oracle's one-call result (bitwise residual_out and
+    kAllReduce out, out within 1 ulp), ragged row counts included."""
+    from gpu_util import DT as GDT, assert_parity, oracle_run
+
+    world = 2
+    cases = [(2, 37, 7168, "bf16", "rmsnorm"), (2, 37, 7168, "bf16", "allreduce"), (2, 3, 4096, "fp16", "rmsnorm"),
+             (2, 1, 7168, "bf16", "rmsnorm")]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gpu_rank, args=(r, world, port, cases, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = [q.get(timeout=300) for _ in range(world * len(cases))]
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    import all_reduce_residual_gb300 as arf
+
+    for rank, (W, M, H, dtype, pattern), out, ro in got:
+        w = wl.custom(W, M, H, dtype, 0.7, 1e-6, config_id=980 + M)
+        inp = wl.make_inputs(w)
+        pat = arf.pattern_code(pattern)
+        assert_parity(GDT[dtype], pat, (out, ro), oracle_run(pat, inp), f"rank {rank} {pattern} M={M}")
