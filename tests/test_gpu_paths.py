@@ -3,11 +3,12 @@ arf_run on the GPU, each checked against the CPU oracle.
 
 Covers: every launch plan shape (flat unroll factors, row and cluster paths
 with 2..16 CTAs, every chunks-per-thread count, grids smaller than the work),
-generic and specialised rank counts, W up to 64 and H up to 32768, ragged
+generic and specialised rank counts, W up to 64 and H up to 524288, ragged
 sizes, M = 0, in-place residual, input preservation, guard bands around the
 outputs, run-to-run determinism, rank-order permutations, the hand-worked
 rows, non-finite inputs, rejected calls, workspace churn, CUDA-graph replay
-and the host-buffer entry point."""
+and the host-buffer entry point (plain and pipelined, pinned and pageable,
+from two threads, under graph capture)."""
 import ctypes
 
 import numpy as np
@@ -429,6 +430,21 @@ def test_host_buffer_pipelined(ws, W, M, H, dtype, sigma):
     arf.HostRunner(ws, AR, W, M, H, tdt)(P2, None, None, 0.0, P2[0], None)
     torch.cuda.synchronize()
     assert_parity(d, AR, (wl.codes(P2[0]), None), oracle_run(AR, inp), "pipelined out = partial 0")
+
+
+@pytest.mark.parametrize("pattern", [AR, RMS])
+def test_host_buffer_pipelined_pageable(ws, pattern):
+    """The pipelined form on pageable (not page-locked) host buffers, where
+    the copies may block the calling thread: same results as the oracle."""
+    W, M, H = 4, 1501, 7168
+    inp = inputs(W, M, H, sigma=0.7, cid=914)
+    P = [p.clone() for p in inp.partials]
+    R, G = inp.residual.clone(), inp.gamma.clone()
+    out, ro = torch.empty_like(R), torch.empty_like(R)
+    arf.HostRunner(ws, pattern, W, M, H, torch.bfloat16)(P, R, G, 1e-6, out, ro)
+    torch.cuda.synchronize()
+    got = (wl.codes(out), wl.codes(ro) if pattern == RMS else None)
+    assert_parity(oracle.BF16, pattern, got, oracle_run(pattern, inp), "pipelined, pageable")
 
 
 def test_host_buffer_pipelined_two_threads(ws):
